@@ -1,0 +1,94 @@
+"""ctypes mirror of ``include/gr00t.h`` and the library loader.
+
+Argument marshalling only: no step of the denoise loop runs here.  Loading
+fails loudly when the compiled library is missing; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+HEADER = os.path.join(ROOT, "include", "gr00t.h")
+LIB_PATH = os.path.join(PKG, "libgr00t.so")
+
+ABI_VERSION = 1
+OK, EINVAL, ENOMEM, ECUDA, ESTATE, EUNSUPPORTED, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
+FAMILY_EXPERT, FAMILY_DIT = 0, 1
+DTYPE_FP32, DTYPE_BF16 = 0, 1
+MLP_GELU, MLP_GEGLU = 0, 1
+MEM_HOST, MEM_DEVICE = 0, 1
+OPT_USE_GRAPH, OPT_GEMM_PATH, OPT_WAIT_LIMIT, OPT_ATTN_PATH, OPT_TIME_KERNEL = 1, 2, 3, 4, 5
+KCLASS_QKV_GEMM, KCLASS_ATTENTION, KCLASS_O_GEMM, KCLASS_UP_GEMM, KCLASS_DOWN_GEMM, KCLASS_NORM = 1, 2, 3, 4, 5, 6
+INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES, INFO_DEVICE_BYTES, INFO_ERROR_FLAG = 1, 2, 3, 4
+
+STATUS_NAMES = {OK: "OK", EINVAL: "EINVAL", ENOMEM: "ENOMEM", ECUDA: "ECUDA", ESTATE: "ESTATE",
+                EUNSUPPORTED: "EUNSUPPORTED", ETIMEOUT: "ETIMEOUT"}
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "abi_version", "family", "dtype", "layers", "hidden", "q_heads", "kv_heads", "head_dim",
+        "mlp_dim", "mlp_kind", "horizon", "action_dim", "state_tokens", "time_dim", "time_mlp",
+        "direction", "max_batch", "max_prefix", "max_steps")] + [
+        ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float)]
+
+
+_VP = ctypes.c_void_p
+_VPP = ctypes.POINTER(ctypes.c_void_p)
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("location", ctypes.c_int32)] + [(n, _VP) for n in (
+        "time_mlp_in_w", "time_mlp_in_b", "time_mlp_out_w", "time_mlp_out_b", "cond_w", "cond_b",
+        "action_in_w", "action_in_b", "enc_w1", "enc_b1", "enc_w2", "enc_b2", "enc_w3", "enc_b3",
+        "action_out_w", "action_out_b")] + [(n, _VPP) for n in ("qkv_w", "o_w", "up_w", "down_w")]
+
+
+# exported symbol -> (restype, argtypes)
+SIGNATURES = {
+    "gr00t_validate_geometry": (ctypes.c_int, [ctypes.POINTER(Geometry), ctypes.c_char_p, ctypes.c_size_t]),
+    "gr00t_create": (ctypes.c_int, [ctypes.POINTER(Geometry), ctypes.POINTER(Weights), _VP,
+                                    ctypes.POINTER(_VP)]),
+    "gr00t_bind_prefix_kv": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VPP, _VPP, _VP, _VP, _VP]),
+    "gr00t_set_schedule": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int]),
+    "gr00t_denoise": (ctypes.c_int, [_VP, _VP, _VP]),
+    "gr00t_denoise_host": (ctypes.c_int, [_VP, _VP, _VP]),
+    "gr00t_denoise_step": (ctypes.c_int, [_VP, ctypes.c_int, _VP, _VP]),
+    "gr00t_destroy": (ctypes.c_int, [_VP]),
+    "gr00t_last_error": (ctypes.c_char_p, [_VP]),
+    "gr00t_set_option": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int64]),
+    "gr00t_get_info": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]),
+    "gr00t_kernel_times": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
+                                          ctypes.POINTER(ctypes.c_int)]),
+}
+
+_lib = None
+
+
+def header_functions(path: str = HEADER) -> list[str]:
+    """Names of the functions ``include/gr00t.h`` declares."""
+    text = open(path).read()
+    return sorted(set(re.findall(r"\b(gr00t_[a-z_]+)\s*\(", text)))
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libgr00t.so (built by ``flow_matching_vla_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(
+            f"{p} is missing: build it with `python -m flow_matching_vla_gb300.build` "
+            "(the denoise loop has no CPU fallback)")
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib

@@ -1,0 +1,88 @@
+// GEMM epilogues of the denoise step, applied to adjacent output pairs (n, n+1).
+//
+// Pairs make every fused epilogue local to one thread or two adjacent lanes:
+//  * RoPE (rotate-half, "Optimizing GR00T-N1.7 Training" 3.3): the Q/K weight
+//    rows are stored interleaved, row 2i = original row i, row 2i+1 = original
+//    row i + hd/2, so a pair is exactly one rotation (x_i, x_{i+hd/2}).
+//  * GeGLU: gate/up rows interleaved, row 2f = gate f, row 2f+1 = up f.
+//  * gated residual h += gate * acc ("pi0.5 Design": AdaRMS gate).
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace g3 {
+
+template <typename T>
+__device__ __forceinline__ void store_pair(T* p, float a0, float a1);
+template <>
+__device__ __forceinline__ void store_pair<float>(float* p, float a0, float a1) {
+  *reinterpret_cast<float2*>(p) = make_float2(a0, a1);
+}
+template <>
+__device__ __forceinline__ void store_pair<bf16>(bf16* p, float a0, float a1) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a0, a1);
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, float a1) {
+  switch (e.kind) {
+    case EPI_STORE: {
+      if (e.bias) {
+        a0 += e.bias[n];
+        a1 += e.bias[n + 1];
+      }
+      if (e.act == ACT_SWISH) {
+        a0 = swishf(a0);
+        a1 = swishf(a1);
+      } else if (e.act == ACT_GELU) {
+        a0 = gelu_tanhf(a0);
+        a1 = gelu_tanhf(a1);
+      }
+      const long long r = e.rg ? (long long)(m / e.rg) * e.rs + e.ro + m % e.rg : (long long)m;
+      if (e.out_f32)
+        store_pair<float>((float*)e.out + r * e.ldo + n, a0, a1);
+      else
+        store_pair<T>((T*)e.out + r * e.ldo + n, a0, a1);
+      break;
+    }
+    case EPI_ROPE: {
+      T* o = (T*)e.out + (long long)m * e.ldo;
+      if (n < e.rope_cols) {
+        const int head = n / e.hd, i = (n % e.hd) >> 1, half = e.hd >> 1;
+        const float2 cs = e.rope_tab[(m % e.tok_rope) * half + i];
+        o[head * e.hd + i] = from_f<T>(a0 * cs.x - a1 * cs.y);
+        o[head * e.hd + i + half] = from_f<T>(a1 * cs.x + a0 * cs.y);
+      } else {
+        store_pair<T>(o + n, a0, a1);
+      }
+      break;
+    }
+    case EPI_RESID_GATED: {
+      const T* g = (const T*)e.gate + (long long)(m / e.tok) * e.gate_bstride + n;
+      float2* h = reinterpret_cast<float2*>(e.resid + (long long)m * e.ldr + n);
+      float2 v = *h;
+      v.x += to_f(g[0]) * a0;
+      v.y += to_f(g[1]) * a1;
+      *h = v;
+      break;
+    }
+    case EPI_RESID: {
+      float2* h = reinterpret_cast<float2*>(e.resid + (long long)m * e.ldr + n);
+      float2 v = *h;
+      v.x += a0;
+      v.y += a1;
+      *h = v;
+      break;
+    }
+    case EPI_GEGLU: {
+      T* o = (T*)e.out + (long long)m * e.ldo + (n >> 1);
+      *o = from_f<T>(gelu_tanhf(a0) * a1);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+}  // namespace g3

@@ -1,0 +1,118 @@
+// Host-side launch interface of the denoise-loop kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace g3 {
+
+enum DType : int { DT_F32 = 0, DT_BF16 = 1 };
+
+// ---- GEMM epilogues ---------------------------------------------------------
+// Every GEMM computes acc[m][n] = sum_k A[m][k] * W[n][k] (fp32 accumulation)
+// and hands adjacent output pairs (n, n+1), n even, to one epilogue.
+enum EpiKind : int {
+  EPI_STORE = 0,        // out[r(m)][n] = act(acc + bias[n])            (act dtype, or fp32 if out_f32)
+  EPI_ROPE = 1,         // fused Q/K RoPE: rows < rope_cols hold rotate-half pairs (see runtime)
+  EPI_RESID_GATED = 2,  // h[m][n] += gate[m / tok][n] * acc            (fp32 residual)
+  EPI_RESID = 3,        // h[m][n] += acc
+  EPI_GEGLU = 4,        // out[m][n/2] = gelu(acc[n]) * acc[n+1]          (interleaved gate/up rows)
+};
+enum Act : int { ACT_NONE = 0, ACT_SWISH = 1, ACT_GELU = 2 };
+
+struct Epi {
+  int kind = EPI_STORE;
+  int act = ACT_NONE;
+  int out_f32 = 0;          // EPI_STORE: write fp32 instead of the activation dtype
+  void* out = nullptr;      // output matrix
+  int ldo = 0;              // its leading dimension (elements)
+  const float* bias = nullptr;  // [N] fp32, nullable
+  // row remap for EPI_STORE: r(m) = (m / rg) * rs + ro + m % rg   (rg = 0: r(m) = m)
+  int rg = 0, rs = 0, ro = 0;
+  // residual epilogues
+  float* resid = nullptr;   // fp32 [M][ldr]
+  int ldr = 0;
+  const void* gate = nullptr;  // activation dtype; gate for row m: gate + (m / tok) * gate_bstride
+  long long gate_bstride = 0;
+  int tok = 1;
+  // RoPE: columns [0, rope_cols) are (Hq + Hkv) heads of rotate-half pairs, head_dim hd
+  int rope_cols = 0, hd = 0;
+  const float2* rope_tab = nullptr;  // [tok_rope][hd/2] (cos, sin) for positions P + j
+  int tok_rope = 1;                  // token rows per sample
+};
+
+struct GemmArgs {
+  const void* A = nullptr;  // activations [M][lda]
+  int lda = 0;
+  const void* W = nullptr;  // weights [N][ldw]
+  int ldw = 0;
+  int M = 0, N = 0, K = 0;
+  Epi epi;
+};
+
+// CUDA-core GEMM (any shape with N even).
+cudaError_t gemm_simt(DType dt, const GemmArgs& a, cudaStream_t s);
+
+// ---- normalisation / projection kernels ------------------------------------
+enum NormKind : int { NORM_RMS = 0, NORM_LN = 1 };
+struct NormArgs {
+  int kind = NORM_RMS;
+  float eps = 1e-6f;
+  const void* mod = nullptr;     // activation dtype; row for sample b: mod + b * mod_bstride
+  long long mod_bstride = 0;
+  int scale_off = 0, shift_off = 0;   // offsets of scale and shift inside the row
+  int tok = 1;                   // token rows per sample
+};
+
+// out[m] = norm(h[m]) * (1 + scale) + shift for m < M (mod == nullptr: plain norm)
+cudaError_t adanorm(DType dt, const float* h, int D, int M, void* out, NormArgs na, cudaStream_t s);
+
+// EXPERT step head: h[m] = x[m] W_in^T + b_in (fp32), then out[m] = AdaRMS(h[m]).
+cudaError_t expert_in(DType dt, const float* x, int A, const void* w_in, const float* b_in, float* h,
+                      int D, int M, void* out, NormArgs na, cudaStream_t s);
+
+// Final norm + action_out_proj + Euler: rows m < M of the action tokens.
+// h row of action token m: (m / H) * tok + ro + m % H.  v = norm(h) W_out^T + b_out;
+// v_out[m] = v (nullable); if do_euler: x[m] += dt[k] * v.
+cudaError_t out_euler(DType dt, const float* h, int D, int M, int H, int ro, const void* w_out,
+                      const float* b_out, int A, NormArgs na, float* x, const float* dts, int k,
+                      int do_euler, float* v_out, cudaStream_t s);
+
+// DIT step head: a[m] = x[m] W1^T + b1 (activation dtype) for the M action rows, and the
+// state tokens copied into the residual rows (b * tok + j, j < ns) from state [B][ns][D].
+cudaError_t dit_in(DType dt, const float* x, int A, const void* w1, const float* b1, void* a_out,
+                   int D, int M, const float* state, int ns, int tok, int B, float* h,
+                   cudaStream_t s);
+
+// ---- attention ----------------------------------------------------------------
+struct AttnArgs {
+  const void* q = nullptr;  // query of (b, t, head): q + (b*Tq + t)*ldq + head*Dh
+  int ldq = 0;
+  int B = 0, Tq = 0, Hq = 0, Hkv = 1, Dh = 0;
+  const void* const* table = nullptr;  // device pointer table (prefix K/V, masks)
+  int k_slot = -1, v_slot = -1, mask_slot = -1;  // slots in the table (-1: none)
+  int P = 0;                // prefix keys per sample: table[k_slot] is [B][P][Hkv][Dh]
+  const void* ks = nullptr; // suffix keys of (b, j, kvh): ks + (b*Tq + j)*lds + kvh*Dh
+  const void* vs = nullptr;
+  int lds = 0;
+  int S = 0;                // suffix keys per sample
+  void* out = nullptr;      // output of (b, t, head): out + (b*Tq + t)*ldo + head*Dh
+  int ldo = 0;
+};
+cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s);
+
+// ---- schedule / bind / create helpers --------------------------------------------
+// temb[k*B + b][E] (activation dtype) of tau_k; dts[k] = tau_{k+1} - tau_k.
+cudaError_t time_embed(DType dt, int T, int B, int E, int direction, void* temb, float* dts,
+                       cudaStream_t s);
+// tab[j][i] = (cos, sin)((P + j) * theta^(-2i/hd)), j < H, i < hd/2
+cudaError_t rope_table(int P, int H, int hd, float theta, float2* tab, cudaStream_t s);
+
+enum PermMode : int { PERM_NONE = 0, PERM_ROPE = 1, PERM_GEGLU = 2 };
+// dst row r <- src row perm(r); rows of row_bytes bytes (multiple of 16, 16B-aligned pointers)
+cudaError_t permute_rows(const void* src, void* dst, int rows, int row_bytes, int mode, int p0,
+                         int p1, cudaStream_t s);
+// dst[i] = float(src[i]) for a DType source
+cudaError_t to_f32(DType dt, const void* src, float* dst, long long n, cudaStream_t s);
+
+}  // namespace g3

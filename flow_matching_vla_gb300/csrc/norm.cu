@@ -1,0 +1,195 @@
+// Adaptive norms and the small projections at the ends of a denoise step.
+//
+//  * AdaRMS ("pi0.5 Design", Component contract): y = rms_norm(h) (1 + scale) + shift,
+//    scale/shift read from the step's modulation row of the sample.
+//  * AdaLayerNorm ("GR00T N1.7", Build-time constants): y = LN(h) (1 + scale) + shift,
+//    (scale, shift) for the blocks and (shift, scale) for the final norm.
+//  * Step head / tail: action_in_proj fused with the first AdaRMS; final norm +
+//    action_out_proj + the device Euler update x += dt * v (vla.cpp Eq. (1)).
+//
+// One CTA per token row; the row is staged in shared memory in fp32 and the
+// reduction is fp32 (the fp32-reduction RMSNorm of "Optimizing GR00T-N1.7
+// Training", 3.3).  These kernels move a few hundred KB per step; they are
+// latency-bound, not bandwidth-bound.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace g3 {
+
+namespace {
+
+// Normalise the fp32 row in shared memory (in place) and apply the modulation.
+template <typename T>
+__device__ void norm_row(float* row, int D, int m, const NormArgs& na, float* red) {
+  float mean = 0.f;
+  if (na.kind == NORM_LN) {
+    float s = 0.f;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) s += row[i];
+    mean = block_sum(s, red) / (float)D;
+  }
+  float q = 0.f;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    const float d = row[i] - mean;
+    q += d * d;
+  }
+  const float r = rsqrtf(block_sum(q, red) / (float)D + na.eps);
+  const T* mod = na.mod ? (const T*)na.mod + (long long)(m / na.tok) * na.mod_bstride : nullptr;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) {
+    float y = (row[i] - mean) * r;
+    if (mod) y = y * (1.f + to_f(mod[na.scale_off + i])) + to_f(mod[na.shift_off + i]);
+    row[i] = y;
+  }
+  __syncthreads();
+}
+
+template <typename T>
+__global__ void adanorm_kernel(const float* __restrict__ h, int D, T* __restrict__ out,
+                               NormArgs na) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + D;
+  const int m = blockIdx.x;
+  const float* hr = h + (long long)m * D;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) row[i] = hr[i];
+  norm_row<T>(row, D, m, na, red);
+  T* o = out + (long long)m * D;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) o[i] = from_f<T>(row[i]);
+}
+
+template <typename T>
+__global__ void expert_in_kernel(const float* __restrict__ x, int A, const T* __restrict__ w_in,
+                                 const float* __restrict__ b_in, float* __restrict__ h, int D,
+                                 T* __restrict__ out, NormArgs na) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + D;
+  float* xs = sm + D + 33;
+  const int m = blockIdx.x;
+  for (int a = threadIdx.x; a < A; a += blockDim.x) xs[a] = x[(long long)m * A + a];
+  __syncthreads();
+  float* hr = h + (long long)m * D;
+  for (int f = threadIdx.x; f < D; f += blockDim.x) {
+    const T* w = w_in + (long long)f * A;
+    float acc = b_in[f];
+    for (int a = 0; a < A; ++a) acc = fmaf(xs[a], to_f(w[a]), acc);
+    row[f] = acc;
+    hr[f] = acc;
+  }
+  __syncthreads();
+  norm_row<T>(row, D, m, na, red);
+  T* o = out + (long long)m * D;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) o[i] = from_f<T>(row[i]);
+}
+
+template <typename T>
+__global__ void out_euler_kernel(const float* __restrict__ h, int D, int H, int ro, int tok,
+                                 const T* __restrict__ w_out, const float* __restrict__ b_out,
+                                 int A, NormArgs na, float* __restrict__ x,
+                                 const float* __restrict__ dts, int k, int do_euler,
+                                 float* __restrict__ v_out) {
+  extern __shared__ float sm[];
+  float* row = sm;
+  float* red = sm + D;
+  const int m = blockIdx.x;                       // action row b * H + j
+  const long long hrow = (long long)(m / H) * tok + ro + m % H;
+  const float* hr = h + hrow * D;
+  for (int i = threadIdx.x; i < D; i += blockDim.x) row[i] = hr[i];
+  // the modulation row is indexed per sample: pass the residual row so m / tok = b
+  norm_row<T>(row, D, (int)hrow, na, red);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int a = warp; a < A; a += nw) {
+    const T* w = w_out + (long long)a * D;
+    float acc = 0.f;
+    for (int i = lane; i < D; i += 32) acc = fmaf(row[i], to_f(w[i]), acc);
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      const float v = acc + b_out[a];
+      if (v_out) v_out[(long long)m * A + a] = v;
+      if (do_euler) x[(long long)m * A + a] += dts[k] * v;
+    }
+  }
+}
+
+template <typename T>
+__global__ void dit_in_kernel(const float* __restrict__ x, int A, const T* __restrict__ w1,
+                              const float* __restrict__ b1, T* __restrict__ a_out, int D, int M,
+                              const float* __restrict__ state, int ns, int tok,
+                              float* __restrict__ h) {
+  extern __shared__ float xs[];
+  const int blk = blockIdx.x;
+  if (blk >= M) {  // state-token rows: copy the bound embedding into the residual stream
+    const int idx = blk - M, b = idx / ns, j = idx % ns;
+    const float* src = state + ((long long)b * ns + j) * D;
+    float* dst = h + ((long long)b * tok + j) * D;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) dst[i] = src[i];
+    return;
+  }
+  for (int a = threadIdx.x; a < A; a += blockDim.x) xs[a] = x[(long long)blk * A + a];
+  __syncthreads();
+  for (int f = threadIdx.x; f < D; f += blockDim.x) {
+    const T* w = w1 + (long long)f * A;
+    float acc = b1[f];
+    for (int a = 0; a < A; ++a) acc = fmaf(xs[a], to_f(w[a]), acc);
+    a_out[(long long)blk * D + f] = from_f<T>(acc);
+  }
+}
+
+inline int threads_for(int D) { return D <= 512 ? 128 : 256; }
+
+}  // namespace
+
+cudaError_t adanorm(DType dt, const float* h, int D, int M, void* out, NormArgs na,
+                    cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  const size_t smem = (D + 33) * sizeof(float);
+  if (dt == DT_F32)
+    adanorm_kernel<float><<<M, threads_for(D), smem, s>>>(h, D, (float*)out, na);
+  else
+    adanorm_kernel<bf16><<<M, threads_for(D), smem, s>>>(h, D, (bf16*)out, na);
+  return cudaGetLastError();
+}
+
+cudaError_t expert_in(DType dt, const float* x, int A, const void* w_in, const float* b_in,
+                      float* h, int D, int M, void* out, NormArgs na, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  const size_t smem = (D + 33 + A) * sizeof(float);
+  if (dt == DT_F32)
+    expert_in_kernel<float><<<M, threads_for(D), smem, s>>>(x, A, (const float*)w_in, b_in, h, D,
+                                                            (float*)out, na);
+  else
+    expert_in_kernel<bf16><<<M, threads_for(D), smem, s>>>(x, A, (const bf16*)w_in, b_in, h, D,
+                                                           (bf16*)out, na);
+  return cudaGetLastError();
+}
+
+cudaError_t out_euler(DType dt, const float* h, int D, int M, int H, int ro, const void* w_out,
+                      const float* b_out, int A, NormArgs na, float* x, const float* dts, int k,
+                      int do_euler, float* v_out, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  const size_t smem = (D + 33) * sizeof(float);
+  const int tok = na.tok;
+  if (dt == DT_F32)
+    out_euler_kernel<float><<<M, 256, smem, s>>>(h, D, H, ro, tok, (const float*)w_out, b_out, A,
+                                                 na, x, dts, k, do_euler, v_out);
+  else
+    out_euler_kernel<bf16><<<M, 256, smem, s>>>(h, D, H, ro, tok, (const bf16*)w_out, b_out, A,
+                                                na, x, dts, k, do_euler, v_out);
+  return cudaGetLastError();
+}
+
+cudaError_t dit_in(DType dt, const float* x, int A, const void* w1, const float* b1, void* a_out,
+                   int D, int M, const float* state, int ns, int tok, int B, float* h,
+                   cudaStream_t s) {
+  const int blocks = M + (state ? B * ns : 0);
+  if (blocks <= 0) return cudaSuccess;
+  const size_t smem = A * sizeof(float);
+  if (dt == DT_F32)
+    dit_in_kernel<float><<<blocks, threads_for(D), smem, s>>>(x, A, (const float*)w1, b1,
+                                                              (float*)a_out, D, M, state, ns, tok, h);
+  else
+    dit_in_kernel<bf16><<<blocks, threads_for(D), smem, s>>>(x, A, (const bf16*)w1, b1,
+                                                             (bf16*)a_out, D, M, state, ns, tok, h);
+  return cudaGetLastError();
+}
+
+}  // namespace g3

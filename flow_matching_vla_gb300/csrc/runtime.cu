@@ -1,0 +1,913 @@
+// C ABI of the denoise loop: context, weight re-layout, bind, schedule, denoise.
+//
+// The step structure follows "pi0.5 Design" (expert) and "GR00T N1.7" (DiT):
+// the prefix K/V is bound once, the time conditioning is hoisted into a
+// modulation table that re-runs only when (steps, batch) change, and the T
+// Euler steps (vla.cpp Eq. (1)) replay as one CUDA graph.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "gr00t.h"
+#include "kernels.h"
+
+using namespace g3;
+
+struct gr00t_ctx {
+  gr00t_geometry g{};
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  std::string err;
+
+  // derived sizes
+  DType dt = DT_BF16;
+  size_t esz = 2;            // bytes per weight / activation element
+  int D = 0, L = 0, Hq = 0, Hkv = 1, Dh = 0, F = 0, H = 0, A = 0, Ns = 0, E = 0;
+  int tok = 0;               // token rows per sample: H + Ns
+  int S = 0, R = 0;          // modulation sites and row width
+  int qd = 0;                // Hq * Dh
+  int Mmax = 0;
+  std::vector<int> nqkv;     // rows of each layer's qkv projection
+
+  // one device arena
+  char* arena = nullptr;
+  size_t arena_bytes = 0;
+
+  // weights (activation dtype), biases (fp32)
+  std::vector<void*> w_qkv, w_o, w_up, w_down;
+  void *w_tin = nullptr, *w_tout = nullptr, *w_cond = nullptr, *w_in = nullptr, *w_out = nullptr;
+  void *w_enc1 = nullptr, *w_enc2 = nullptr, *w_enc3 = nullptr;
+  float *b_tin = nullptr, *b_tout = nullptr, *b_cond = nullptr, *b_in = nullptr, *b_out = nullptr;
+  float *b_enc1 = nullptr, *b_enc2 = nullptr, *b_enc3 = nullptr;
+
+  // activations
+  float* h = nullptr;
+  void *n = nullptr, *qkv = nullptr, *att = nullptr, *u = nullptr, *a_enc = nullptr, *e_enc = nullptr;
+  float *x = nullptr, *xtmp = nullptr;
+  // schedule
+  void *temb = nullptr, *t1 = nullptr, *cvec = nullptr, *mod = nullptr;
+  float *dts = nullptr, *atb = nullptr;
+  float2* rope_tab = nullptr;
+  const void** table = nullptr;   // device pointer table: K_l, V_l (2L), text, image, state
+  int* err_flag = nullptr;
+
+  // state
+  bool bound = false, scheduled = false;
+  int bB = 0, bP = 0, sT = 0, sB = 0;
+  std::vector<const void*> host_table;
+
+  // graph cache (one entry)
+  cudaGraphExec_t gexec = nullptr;
+  int gT = -1, gB = -1, gP = -1;
+
+  // options
+  int opt_graph = 1, opt_gemm = 0, opt_attn = 0;
+  long long wait_limit = 1 << 22;
+  int launches = 0;  // kernel launches of the last enqueued step
+
+  // per-kernel timing: event pairs around every launch of one kernel class
+  int time_class = 0;
+  std::vector<cudaEvent_t> tev;
+  int tev_used = 0;
+  bool capturing = false;
+};
+
+namespace {
+
+thread_local std::string g_create_err;
+
+int set_err(gr00t_ctx* c, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c)
+    c->err = buf;
+  else
+    g_create_err = buf;
+  return code;
+}
+
+#define CK(ctx, call)                                                                      \
+  do {                                                                                     \
+    cudaError_t e_ = (call);                                                               \
+    if (e_ != cudaSuccess)                                                                 \
+      return set_err((ctx), GR00T_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+int validate(const gr00t_geometry* g, char* msg, size_t len) {
+  auto bad = [&](int code, const char* why) {
+    if (msg && len) snprintf(msg, len, "%s", why);
+    return code;
+  };
+  if (!g) return bad(GR00T_EINVAL, "geometry is NULL");
+  if (g->abi_version != GR00T_ABI_VERSION) return bad(GR00T_EINVAL, "abi_version mismatch");
+  if (g->family != GR00T_FAMILY_EXPERT && g->family != GR00T_FAMILY_DIT)
+    return bad(GR00T_EINVAL, "unknown family");
+  if (g->dtype != GR00T_DTYPE_FP32 && g->dtype != GR00T_DTYPE_BF16)
+    return bad(GR00T_EINVAL, "unknown dtype");
+  if (g->mlp_kind != GR00T_MLP_GELU && g->mlp_kind != GR00T_MLP_GEGLU)
+    return bad(GR00T_EINVAL, "unknown mlp_kind");
+  if (g->layers < 1 || g->layers > 512) return bad(GR00T_EINVAL, "layers out of range [1, 512]");
+  if (g->hidden < 64 || g->hidden > 8192 || g->hidden % 64)
+    return bad(GR00T_EINVAL, "hidden must be a multiple of 64 in [64, 8192]");
+  if (g->mlp_dim < 64 || g->mlp_dim % 64 || g->mlp_dim > 65536)
+    return bad(GR00T_EINVAL, "mlp_dim must be a multiple of 64 in [64, 65536]");
+  if (g->q_heads < 1 || g->head_dim < 2 || g->head_dim % 2 || g->head_dim > 256)
+    return bad(GR00T_EINVAL, "head_dim must be even and <= 256, q_heads >= 1");
+  if ((g->q_heads * g->head_dim) % 64) return bad(GR00T_EINVAL, "q_heads*head_dim must be a multiple of 64");
+  if (g->horizon < 1 || g->horizon > 4096) return bad(GR00T_EINVAL, "horizon out of range");
+  if (g->action_dim < 1 || g->action_dim > 1024) return bad(GR00T_EINVAL, "action_dim out of range");
+  if (g->time_dim < 4 || g->time_dim % 2 || g->time_dim > 65536) return bad(GR00T_EINVAL, "time_dim must be even, >= 4");
+  if (g->time_mlp != 0 && g->time_mlp != 1) return bad(GR00T_EINVAL, "time_mlp must be 0 or 1");
+  if (g->direction != -1 && g->direction != 1) return bad(GR00T_EINVAL, "direction must be -1 or +1");
+  if (g->max_batch < 1 || g->max_batch > 65536) return bad(GR00T_EINVAL, "max_batch out of range");
+  if (g->max_steps < 1 || g->max_steps > 4096) return bad(GR00T_EINVAL, "max_steps out of range");
+  if (g->max_prefix < 0 || g->max_prefix > (1 << 20)) return bad(GR00T_EINVAL, "max_prefix out of range");
+  if (!(g->norm_eps > 0.f)) return bad(GR00T_EINVAL, "norm_eps must be > 0");
+  if (g->family == GR00T_FAMILY_EXPERT) {
+    if (g->kv_heads != 1)
+      return bad(GR00T_EINVAL, "expert family needs kv_heads == 1 (the head fold is exact only with one KV head)");
+    if (g->state_tokens != 0) return bad(GR00T_EINVAL, "expert family has no state tokens");
+    if (!(g->rope_theta > 0.f)) return bad(GR00T_EINVAL, "rope_theta must be > 0");
+  } else {
+    if (g->kv_heads != g->q_heads) return bad(GR00T_EINVAL, "DiT family needs kv_heads == q_heads");
+    if (g->state_tokens < 0 || g->state_tokens > 16) return bad(GR00T_EINVAL, "state_tokens out of range");
+    if (g->max_prefix < 1) return bad(GR00T_EINVAL, "DiT family needs max_prefix >= 1");
+    if (g->q_heads * g->head_dim != g->hidden)
+      return bad(GR00T_EINVAL, "DiT family needs q_heads*head_dim == hidden");
+  }
+  const long long mmax = (long long)g->max_batch * (g->horizon + g->state_tokens);
+  if (mmax > (1 << 24)) return bad(GR00T_EINVAL, "max_batch * tokens too large");
+  if (msg && len) msg[0] = 0;
+  return GR00T_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Plan {
+  std::vector<std::pair<void**, size_t>> req;
+  void add(void** p, size_t bytes) { req.emplace_back(p, bytes); }
+  size_t total() const {
+    size_t t = 0;
+    for (auto& r : req) t += align256(r.second);
+    return t;
+  }
+};
+
+void plan_buffers(gr00t_ctx* c, Plan& pl) {
+  const size_t es = c->esz;
+  const int L = c->L, D = c->D, E = c->E;
+  const bool dit = c->g.family == GR00T_FAMILY_DIT;
+  c->w_qkv.assign(L, nullptr);
+  c->w_o.assign(L, nullptr);
+  c->w_up.assign(L, nullptr);
+  c->w_down.assign(L, nullptr);
+  const int up_rows = (c->g.mlp_kind == GR00T_MLP_GEGLU ? 2 : 1) * c->F;
+  for (int l = 0; l < L; ++l) {
+    pl.add(&c->w_qkv[l], (size_t)c->nqkv[l] * D * es);
+    pl.add(&c->w_o[l], (size_t)D * c->qd * es);
+    pl.add(&c->w_up[l], (size_t)up_rows * D * es);
+    pl.add(&c->w_down[l], (size_t)D * c->F * es);
+  }
+  if (c->g.time_mlp) {
+    pl.add(&c->w_tin, (size_t)E * E * es);
+    pl.add(&c->w_tout, (size_t)E * E * es);
+    pl.add((void**)&c->b_tin, (size_t)E * 4);
+    pl.add((void**)&c->b_tout, (size_t)E * 4);
+  }
+  pl.add(&c->w_cond, (size_t)c->S * c->R * E * es);
+  pl.add((void**)&c->b_cond, (size_t)c->S * c->R * 4);
+  if (!dit) {
+    pl.add(&c->w_in, (size_t)D * c->A * es);
+    pl.add((void**)&c->b_in, (size_t)D * 4);
+  } else {
+    pl.add(&c->w_enc1, (size_t)D * c->A * es);
+    pl.add((void**)&c->b_enc1, (size_t)D * 4);
+    pl.add(&c->w_enc2, (size_t)D * (D + E) * es);
+    pl.add((void**)&c->b_enc2, (size_t)D * 4);
+    pl.add(&c->w_enc3, (size_t)D * D * es);
+    pl.add((void**)&c->b_enc3, (size_t)D * 4);
+  }
+  pl.add(&c->w_out, (size_t)c->A * D * es);
+  pl.add((void**)&c->b_out, (size_t)c->A * 4);
+
+  int nq = 0;
+  for (int v : c->nqkv) nq = v > nq ? v : nq;
+  const size_t M = c->Mmax;
+  const size_t MA = (size_t)c->g.max_batch * c->H;
+  pl.add((void**)&c->h, M * D * 4);
+  pl.add(&c->n, M * D * es);
+  pl.add(&c->qkv, M * nq * es);
+  pl.add(&c->att, M * c->qd * es);
+  pl.add(&c->u, M * c->F * es);
+  pl.add((void**)&c->x, MA * c->A * 4);
+  pl.add((void**)&c->xtmp, MA * c->A * 4);
+  if (dit) {
+    pl.add(&c->a_enc, MA * D * es);
+    pl.add(&c->e_enc, MA * D * es);
+  }
+  const size_t TB = (size_t)c->g.max_steps * c->g.max_batch;
+  pl.add(&c->temb, TB * E * es);
+  if (c->g.time_mlp) {
+    pl.add(&c->t1, TB * E * es);
+    pl.add(&c->cvec, TB * E * es);
+  }
+  pl.add(&c->mod, TB * c->S * c->R * es);
+  pl.add((void**)&c->dts, (size_t)c->g.max_steps * 4);
+  if (dit) pl.add((void**)&c->atb, (size_t)c->g.max_steps * D * 4);
+  if (!dit) pl.add((void**)&c->rope_tab, (size_t)c->H * (c->Dh / 2) * sizeof(float2));
+  pl.add((void**)&c->table, (size_t)(2 * L + 3) * sizeof(void*));
+  pl.add((void**)&c->err_flag, 64);
+}
+
+// Copy one weight matrix [rows][cols] into library memory, re-laid-out by ``mode``.
+int upload_matrix(gr00t_ctx* c, const void* src, bool on_dev, void* dst, int rows, int cols,
+                  int mode, int p0, int p1, void* staging) {
+  const size_t row_bytes = (size_t)cols * c->esz;
+  const size_t bytes = row_bytes * rows;
+  if (mode == PERM_NONE) {
+    CK(c, cudaMemcpyAsync(dst, src, bytes, on_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                          c->stream));
+    return GR00T_OK;
+  }
+  const void* s = src;
+  if (!on_dev || ((uintptr_t)src & 15)) {
+    CK(c, cudaMemcpyAsync(staging, src, bytes, on_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                          c->stream));
+    s = staging;
+  }
+  CK(c, permute_rows(s, dst, rows, (int)row_bytes, mode, p0, p1, c->stream));
+  // the staging buffer is reused by the next matrix: order host copies after this permute
+  CK(c, cudaStreamSynchronize(c->stream));
+  return GR00T_OK;
+}
+
+int upload_bias(gr00t_ctx* c, const void* src, bool on_dev, float* dst, long long n, void* staging) {
+  const void* s = src;
+  if (!on_dev) {
+    CK(c, cudaMemcpyAsync(staging, src, n * c->esz, cudaMemcpyHostToDevice, c->stream));
+    s = staging;
+  }
+  CK(c, to_f32(c->dt, s, dst, n, c->stream));
+  CK(c, cudaStreamSynchronize(c->stream));
+  return GR00T_OK;
+}
+
+int check_weights(gr00t_ctx* c, const gr00t_weights* w) {
+  if (!w) return set_err(c, GR00T_EINVAL, "weights is NULL");
+  if (w->location != GR00T_MEM_HOST && w->location != GR00T_MEM_DEVICE)
+    return set_err(c, GR00T_EINVAL, "weights.location must be GR00T_MEM_HOST or GR00T_MEM_DEVICE");
+  const bool dit = c->g.family == GR00T_FAMILY_DIT;
+  if (!w->cond_w || !w->cond_b || !w->action_out_w || !w->action_out_b)
+    return set_err(c, GR00T_EINVAL, "cond_w/cond_b/action_out_w/action_out_b are required");
+  if (c->g.time_mlp && (!w->time_mlp_in_w || !w->time_mlp_in_b || !w->time_mlp_out_w || !w->time_mlp_out_b))
+    return set_err(c, GR00T_EINVAL, "time_mlp set but time MLP weights missing");
+  if (!dit && (!w->action_in_w || !w->action_in_b))
+    return set_err(c, GR00T_EINVAL, "expert family needs action_in_w/action_in_b");
+  if (dit && (!w->enc_w1 || !w->enc_b1 || !w->enc_w2 || !w->enc_b2 || !w->enc_w3 || !w->enc_b3))
+    return set_err(c, GR00T_EINVAL, "DiT family needs enc_w1..enc_b3");
+  if (!w->qkv_w || !w->o_w || !w->up_w || !w->down_w)
+    return set_err(c, GR00T_EINVAL, "per-layer weight arrays are required");
+  for (int l = 0; l < c->L; ++l)
+    if (!w->qkv_w[l] || !w->o_w[l] || !w->up_w[l] || !w->down_w[l])
+      return set_err(c, GR00T_EINVAL, "layer %d has a NULL weight", l);
+  return GR00T_OK;
+}
+
+int upload_weights(gr00t_ctx* c, const gr00t_weights* w) {
+  const bool on_dev = w->location == GR00T_MEM_DEVICE;
+  const int D = c->D, E = c->E;
+  const bool dit = c->g.family == GR00T_FAMILY_DIT;
+  const bool geglu = c->g.mlp_kind == GR00T_MLP_GEGLU;
+  // staging: the largest matrix
+  size_t big = (size_t)c->S * c->R * E;
+  for (int l = 0; l < c->L; ++l) {
+    big = std::max(big, (size_t)c->nqkv[l] * D);
+    big = std::max(big, (size_t)(geglu ? 2 : 1) * c->F * D);
+  }
+  void* staging = nullptr;
+  CK(c, cudaMalloc(&staging, big * c->esz + 256));
+  int rc = GR00T_OK;
+  auto M = [&](const void* s, void* d, int rows, int cols, int mode, int p0, int p1) {
+    if (rc == GR00T_OK) rc = upload_matrix(c, s, on_dev, d, rows, cols, mode, p0, p1, staging);
+  };
+  auto Bv = [&](const void* s, float* d, long long n) {
+    if (rc == GR00T_OK) rc = upload_bias(c, s, on_dev, d, n, staging);
+  };
+  for (int l = 0; l < c->L; ++l) {
+    const bool rope = !dit;  // expert: q heads and the k head carry rotate-half RoPE
+    M(w->qkv_w[l], c->w_qkv[l], c->nqkv[l], D, rope ? PERM_ROPE : PERM_NONE,
+      (c->Hq + c->Hkv) * c->Dh, c->Dh);
+    M(w->o_w[l], c->w_o[l], D, c->qd, PERM_NONE, 0, 0);
+    M(w->up_w[l], c->w_up[l], (geglu ? 2 : 1) * c->F, D, geglu ? PERM_GEGLU : PERM_NONE, c->F, 0);
+    M(w->down_w[l], c->w_down[l], D, c->F, PERM_NONE, 0, 0);
+  }
+  if (c->g.time_mlp) {
+    M(w->time_mlp_in_w, c->w_tin, E, E, PERM_NONE, 0, 0);
+    M(w->time_mlp_out_w, c->w_tout, E, E, PERM_NONE, 0, 0);
+    Bv(w->time_mlp_in_b, c->b_tin, E);
+    Bv(w->time_mlp_out_b, c->b_tout, E);
+  }
+  M(w->cond_w, c->w_cond, c->S * c->R, E, PERM_NONE, 0, 0);
+  Bv(w->cond_b, c->b_cond, (long long)c->S * c->R);
+  if (!dit) {
+    M(w->action_in_w, c->w_in, D, c->A, PERM_NONE, 0, 0);
+    Bv(w->action_in_b, c->b_in, D);
+  } else {
+    M(w->enc_w1, c->w_enc1, D, c->A, PERM_NONE, 0, 0);
+    Bv(w->enc_b1, c->b_enc1, D);
+    M(w->enc_w2, c->w_enc2, D, D + E, PERM_NONE, 0, 0);
+    Bv(w->enc_b2, c->b_enc2, D);
+    M(w->enc_w3, c->w_enc3, D, D, PERM_NONE, 0, 0);
+    Bv(w->enc_b3, c->b_enc3, D);
+  }
+  M(w->action_out_w, c->w_out, c->A, D, PERM_NONE, 0, 0);
+  Bv(w->action_out_b, c->b_out, c->A);
+  cudaError_t e1 = cudaStreamSynchronize(c->stream);
+  cudaError_t e2 = cudaFree(staging);
+  if (rc != GR00T_OK) return rc;
+  if (e1 != cudaSuccess || e2 != cudaSuccess)
+    return set_err(c, GR00T_ECUDA, "weight upload failed: %s",
+                   cudaGetErrorString(e1 != cudaSuccess ? e1 : e2));
+  return GR00T_OK;
+}
+
+// ---- the step ------------------------------------------------------------------
+
+// Timing brackets: with GR00T_OPT_TIME_KERNEL set to a class, every launch of
+// that class sits between two events (event-record nodes when captured).
+void tmark(gr00t_ctx* c, int cls) {
+  if (!c->time_class || cls != c->time_class || c->tev_used >= (int)c->tev.size()) return;
+  cudaEvent_t ev = c->tev[c->tev_used++];
+  if (c->capturing)
+    cudaEventRecordWithFlags(ev, c->stream, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, c->stream);
+}
+
+int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
+  ++c->launches;
+  tmark(c, cls);
+  CK(c, gemm_simt(c->dt, a, c->stream));
+  tmark(c, cls);
+  return GR00T_OK;
+}
+
+#define RC(x)                          \
+  do {                                 \
+    int rc_ = (x);                     \
+    if (rc_ != GR00T_OK) return rc_;   \
+  } while (0)
+
+inline const char* ptr_at(const void* p, long long elems, size_t esz) {
+  return (const char*)p + elems * (long long)esz;
+}
+
+// Enqueue one denoise step k on the stream: x (fp32 [B][H][A]) in; v_out
+// (nullable) receives the velocity; with do_euler x += dt_k * v.
+int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
+  c->launches = 0;
+  const int B = c->bB, P = c->bP, D = c->D, L = c->L, H = c->H, tok = c->tok;
+  const int M = B * tok, MA = B * H, R = c->R;
+  const long long bstride = (long long)c->S * R;
+  const size_t es = c->esz;
+  const char* mod_k = ptr_at(c->mod, (long long)k * B * bstride, es);
+  const bool dit = c->g.family == GR00T_FAMILY_DIT;
+  cudaStream_t s = c->stream;
+
+  auto site = [&](int si) { return (const void*)(mod_k + (long long)si * R * es); };
+  NormArgs base;
+  base.eps = c->g.norm_eps;
+  base.mod_bstride = bstride;
+  base.tok = tok;
+
+  if (!dit) {
+    NormArgs na = base;
+    na.kind = NORM_RMS;
+    na.mod = site(0);
+    na.scale_off = 0;
+    na.shift_off = D;
+    ++c->launches;
+    tmark(c, GR00T_KCLASS_NORM);
+    CK(c, expert_in(c->dt, x, c->A, c->w_in, c->b_in, c->h, D, M, c->n, na, s));
+    tmark(c, GR00T_KCLASS_NORM);
+    const int nq = c->nqkv[0];
+    for (int l = 0; l < L; ++l) {
+      GemmArgs g;
+      g.A = c->n; g.lda = D; g.W = c->w_qkv[l]; g.ldw = D; g.M = M; g.N = nq; g.K = D;
+      g.epi.kind = EPI_ROPE; g.epi.out = c->qkv; g.epi.ldo = nq;
+      g.epi.rope_cols = (c->Hq + 1) * c->Dh; g.epi.hd = c->Dh; g.epi.rope_tab = c->rope_tab;
+      g.epi.tok_rope = tok;
+      RC(gemm(c, g, GR00T_KCLASS_QKV_GEMM));
+
+      AttnArgs at;
+      at.q = c->qkv; at.ldq = nq; at.B = B; at.Tq = tok; at.Hq = c->Hq; at.Hkv = 1; at.Dh = c->Dh;
+      at.table = c->table; at.k_slot = 2 * l; at.v_slot = 2 * l + 1; at.P = P;
+      at.ks = ptr_at(c->qkv, (long long)c->qd, es); at.vs = ptr_at(c->qkv, (long long)c->qd + c->Dh, es);
+      at.lds = nq; at.S = tok; at.out = c->att; at.ldo = c->qd;
+      ++c->launches;
+      tmark(c, GR00T_KCLASS_ATTENTION);
+      CK(c, attention_simt(c->dt, at, s));
+      tmark(c, GR00T_KCLASS_ATTENTION);
+
+      GemmArgs go;
+      go.A = c->att; go.lda = c->qd; go.W = c->w_o[l]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
+      go.epi.kind = EPI_RESID_GATED; go.epi.resid = c->h; go.epi.ldr = D;
+      go.epi.gate = ptr_at(site(2 * l), 2LL * D, es); go.epi.gate_bstride = bstride; go.epi.tok = tok;
+      RC(gemm(c, go, GR00T_KCLASS_O_GEMM));
+
+      NormArgs n2 = na;
+      n2.mod = site(2 * l + 1);
+      ++c->launches;
+      tmark(c, GR00T_KCLASS_NORM);
+      CK(c, adanorm(c->dt, c->h, D, M, c->n, n2, s));
+      tmark(c, GR00T_KCLASS_NORM);
+
+      GemmArgs gu;
+      gu.A = c->n; gu.lda = D; gu.W = c->w_up[l]; gu.ldw = D; gu.M = M; gu.K = D;
+      if (c->g.mlp_kind == GR00T_MLP_GEGLU) {
+        gu.N = 2 * c->F; gu.epi.kind = EPI_GEGLU;
+      } else {
+        gu.N = c->F; gu.epi.kind = EPI_STORE; gu.epi.act = ACT_GELU;
+      }
+      gu.epi.out = c->u; gu.epi.ldo = c->F;
+      RC(gemm(c, gu, GR00T_KCLASS_UP_GEMM));
+
+      GemmArgs gd;
+      gd.A = c->u; gd.lda = c->F; gd.W = c->w_down[l]; gd.ldw = c->F; gd.M = M; gd.N = D; gd.K = c->F;
+      gd.epi.kind = EPI_RESID_GATED; gd.epi.resid = c->h; gd.epi.ldr = D;
+      gd.epi.gate = ptr_at(site(2 * l + 1), 2LL * D, es); gd.epi.gate_bstride = bstride; gd.epi.tok = tok;
+      RC(gemm(c, gd, GR00T_KCLASS_DOWN_GEMM));
+
+      if (l + 1 < L) {
+        NormArgs n3 = na;
+        n3.mod = site(2 * l + 2);
+        ++c->launches;
+        tmark(c, GR00T_KCLASS_NORM);
+        CK(c, adanorm(c->dt, c->h, D, M, c->n, n3, s));
+        tmark(c, GR00T_KCLASS_NORM);
+      }
+    }
+    NormArgs nf = na;
+    nf.mod = site(2 * L);
+    ++c->launches;
+    tmark(c, GR00T_KCLASS_NORM);
+    CK(c, out_euler(c->dt, c->h, D, MA, H, 0, c->w_out, c->b_out, c->A, nf, x, c->dts, k, do_euler,
+                    v_out, s));
+    tmark(c, GR00T_KCLASS_NORM);
+    return GR00T_OK;
+  }
+
+  // ---- DiT family ----
+  const int E = c->E, Ns = c->Ns;
+  ++c->launches;
+  tmark(c, GR00T_KCLASS_NORM);
+  CK(c, dit_in(c->dt, x, c->A, c->w_enc1, c->b_enc1, c->a_enc, D, MA, (const float*)c->host_table[2 * L + 2],
+               Ns, tok, B, c->h, s));
+  tmark(c, GR00T_KCLASS_NORM);
+  {
+    GemmArgs g;  // e = swish(a W2[:, :D]^T + atb_k), atb_k holds W2's time half and b2
+    g.A = c->a_enc; g.lda = D; g.W = c->w_enc2; g.ldw = D + E; g.M = MA; g.N = D; g.K = D;
+    g.epi.kind = EPI_STORE; g.epi.act = ACT_SWISH; g.epi.bias = c->atb + (long long)k * D;
+    g.epi.out = c->e_enc; g.epi.ldo = D;
+    RC(gemm(c, g));
+    GemmArgs g3a;  // action tokens into the residual rows after the state tokens
+    g3a.A = c->e_enc; g3a.lda = D; g3a.W = c->w_enc3; g3a.ldw = D; g3a.M = MA; g3a.N = D; g3a.K = D;
+    g3a.epi.kind = EPI_STORE; g3a.epi.out_f32 = 1; g3a.epi.bias = c->b_enc3; g3a.epi.out = c->h;
+    g3a.epi.ldo = D; g3a.epi.rg = H; g3a.epi.rs = tok; g3a.epi.ro = Ns;
+    RC(gemm(c, g3a));
+  }
+  NormArgs na = base;
+  na.kind = NORM_LN;
+  na.scale_off = 0;
+  na.shift_off = D;
+  for (int i = 0; i < L; ++i) {
+    NormArgs n1 = na;
+    n1.mod = site(i);
+    ++c->launches;
+    tmark(c, GR00T_KCLASS_NORM);
+    CK(c, adanorm(c->dt, c->h, D, M, c->n, n1, s));
+    tmark(c, GR00T_KCLASS_NORM);
+    const int nq = c->nqkv[i];
+    GemmArgs g;
+    g.A = c->n; g.lda = D; g.W = c->w_qkv[i]; g.ldw = D; g.M = M; g.N = nq; g.K = D;
+    g.epi.kind = EPI_STORE; g.epi.out = c->qkv; g.epi.ldo = nq;
+    RC(gemm(c, g, GR00T_KCLASS_QKV_GEMM));
+    AttnArgs at;
+    at.q = c->qkv; at.ldq = nq; at.B = B; at.Tq = tok; at.Hq = c->Hq; at.Hkv = c->Hkv; at.Dh = c->Dh;
+    at.table = c->table; at.out = c->att; at.ldo = c->qd;
+    if (i % 2 == 0) {  // cross-attention into the bound VL context
+      at.k_slot = 2 * i; at.v_slot = 2 * i + 1; at.P = P;
+      at.mask_slot = (i % 4 == 0) ? 2 * L : 2 * L + 1;
+      if (!c->host_table[at.mask_slot]) at.mask_slot = -1;
+      at.S = 0;
+    } else {  // self-attention over the state + action tokens
+      at.P = 0; at.ks = ptr_at(c->qkv, (long long)c->qd, es); at.vs = ptr_at(c->qkv, 2LL * c->qd, es);
+      at.lds = nq; at.S = tok;
+    }
+    ++c->launches;
+    tmark(c, GR00T_KCLASS_ATTENTION);
+    CK(c, attention_simt(c->dt, at, s));
+    tmark(c, GR00T_KCLASS_ATTENTION);
+    GemmArgs go;
+    go.A = c->att; go.lda = c->qd; go.W = c->w_o[i]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
+    go.epi.kind = EPI_RESID; go.epi.resid = c->h; go.epi.ldr = D;
+    RC(gemm(c, go, GR00T_KCLASS_O_GEMM));
+    NormArgs n3 = na;
+    n3.mod = nullptr;
+    ++c->launches;
+    tmark(c, GR00T_KCLASS_NORM);
+    CK(c, adanorm(c->dt, c->h, D, M, c->n, n3, s));
+    tmark(c, GR00T_KCLASS_NORM);
+    GemmArgs gu;
+    gu.A = c->n; gu.lda = D; gu.W = c->w_up[i]; gu.ldw = D; gu.M = M; gu.N = c->F; gu.K = D;
+    gu.epi.kind = EPI_STORE; gu.epi.act = ACT_GELU; gu.epi.out = c->u; gu.epi.ldo = c->F;
+    RC(gemm(c, gu, GR00T_KCLASS_UP_GEMM));
+    GemmArgs gd;
+    gd.A = c->u; gd.lda = c->F; gd.W = c->w_down[i]; gd.ldw = c->F; gd.M = M; gd.N = D; gd.K = c->F;
+    gd.epi.kind = EPI_RESID; gd.epi.resid = c->h; gd.epi.ldr = D;
+    RC(gemm(c, gd, GR00T_KCLASS_DOWN_GEMM));
+  }
+  NormArgs nf = na;
+  nf.mod = site(L);
+  nf.scale_off = D;  // final row splits (shift, scale)
+  nf.shift_off = 0;
+  ++c->launches;
+  tmark(c, GR00T_KCLASS_NORM);
+  CK(c, out_euler(c->dt, c->h, D, MA, H, Ns, c->w_out, c->b_out, c->A, nf, x, c->dts, k, do_euler,
+                  v_out, s));
+  tmark(c, GR00T_KCLASS_NORM);
+  return GR00T_OK;
+}
+
+int ensure_graph(gr00t_ctx* c) {
+  if (c->gexec && c->gT == c->sT && c->gB == c->bB && c->gP == c->bP) return GR00T_OK;
+  if (c->gexec) {
+    cudaGraphExecDestroy(c->gexec);
+    c->gexec = nullptr;
+  }
+  cudaGraph_t graph = nullptr;
+  CK(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+  c->capturing = true;
+  c->tev_used = 0;
+  int rc = GR00T_OK;
+  for (int k = 0; k < c->sT && rc == GR00T_OK; ++k) rc = enqueue_step(c, k, c->x, nullptr, 1);
+  c->capturing = false;
+  cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
+  if (rc != GR00T_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (e != cudaSuccess) return set_err(c, GR00T_ECUDA, "graph capture failed: %s", cudaGetErrorString(e));
+  e = cudaGraphInstantiate(&c->gexec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) {
+    c->gexec = nullptr;
+    return set_err(c, GR00T_ECUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  }
+  c->gT = c->sT;
+  c->gB = c->bB;
+  c->gP = c->bP;
+  return GR00T_OK;
+}
+
+int check_ready(gr00t_ctx* c) {
+  if (!c->bound) return set_err(c, GR00T_ESTATE, "no prefix K/V bound (call gr00t_bind_prefix_kv)");
+  if (!c->scheduled) return set_err(c, GR00T_ESTATE, "no schedule (call gr00t_set_schedule)");
+  if (c->bB != c->sB)
+    return set_err(c, GR00T_ESTATE, "batch of the bind (%d) differs from the schedule's (%d)", c->bB, c->sB);
+  return GR00T_OK;
+}
+
+int run_loop(gr00t_ctx* c) {
+  if (c->opt_graph) {
+    RC(ensure_graph(c));
+    CK(c, cudaGraphLaunch(c->gexec, c->stream));
+  } else {
+    c->tev_used = 0;
+    for (int k = 0; k < c->sT; ++k) RC(enqueue_step(c, k, c->x, nullptr, 1));
+  }
+  return GR00T_OK;
+}
+
+void free_ctx(gr00t_ctx* c) {
+  if (!c) return;
+  if (c->stream) cudaStreamSynchronize(c->stream);
+  if (c->gexec) cudaGraphExecDestroy(c->gexec);
+  for (cudaEvent_t e : c->tev) cudaEventDestroy(e);
+  if (c->arena) cudaFree(c->arena);
+  if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+  delete c;
+}
+
+}  // namespace
+
+// ---- exported ------------------------------------------------------------------
+
+extern "C" int gr00t_validate_geometry(const gr00t_geometry* g, char* msg, size_t msg_len) {
+  return validate(g, msg, msg_len);
+}
+
+extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, void* stream,
+                            gr00t_ctx** out) {
+  if (!out) return set_err(nullptr, GR00T_EINVAL, "out is NULL");
+  *out = nullptr;
+  char msg[256];
+  int rc = validate(g, msg, sizeof msg);
+  if (rc != GR00T_OK) return set_err(nullptr, rc, "invalid geometry: %s", msg);
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  cudaDeviceProp prop;
+  if (e == cudaSuccess) e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return set_err(nullptr, GR00T_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  if (!(prop.major == 10 && prop.minor == 3))
+    return set_err(nullptr, GR00T_EUNSUPPORTED, "device %s is sm_%d%d; this library is built for sm_103a",
+                   prop.name, prop.major, prop.minor);
+
+  gr00t_ctx* c = new gr00t_ctx();
+  c->g = *g;
+  c->dt = g->dtype == GR00T_DTYPE_BF16 ? DT_BF16 : DT_F32;
+  c->esz = c->dt == DT_BF16 ? 2 : 4;
+  c->D = g->hidden; c->L = g->layers; c->Hq = g->q_heads; c->Hkv = g->kv_heads; c->Dh = g->head_dim;
+  c->F = g->mlp_dim; c->H = g->horizon; c->A = g->action_dim; c->Ns = g->state_tokens; c->E = g->time_dim;
+  c->tok = c->H + c->Ns;
+  c->qd = c->Hq * c->Dh;
+  const bool dit = g->family == GR00T_FAMILY_DIT;
+  c->S = dit ? c->L + 1 : 2 * c->L + 1;
+  c->R = (dit ? 2 : 3) * c->D;
+  c->Mmax = g->max_batch * c->tok;
+  c->nqkv.resize(c->L);
+  for (int l = 0; l < c->L; ++l)
+    c->nqkv[l] = (dit && l % 2 == 0) ? c->qd : c->qd + 2 * c->Hkv * c->Dh;
+  rc = check_weights(c, w);
+  if (rc != GR00T_OK) {
+    g_create_err = c->err;
+    delete c;
+    return rc;
+  }
+  if (stream) {
+    c->stream = (cudaStream_t)stream;
+  } else {
+    e = cudaStreamCreate(&c->stream);
+    if (e != cudaSuccess) {
+      delete c;
+      return set_err(nullptr, GR00T_ECUDA, "cudaStreamCreate failed: %s", cudaGetErrorString(e));
+    }
+    c->own_stream = true;
+  }
+  Plan pl;
+  plan_buffers(c, pl);
+  c->arena_bytes = pl.total();
+  e = cudaMalloc((void**)&c->arena, c->arena_bytes);
+  if (e != cudaSuccess) {
+    c->arena = nullptr;
+    set_err(nullptr, GR00T_ENOMEM, "cudaMalloc of %zu bytes failed: %s", c->arena_bytes, cudaGetErrorString(e));
+    free_ctx(c);
+    return GR00T_ENOMEM;
+  }
+  size_t off = 0;
+  for (auto& r : pl.req) {
+    *r.first = c->arena + off;
+    off += align256(r.second);
+  }
+  rc = upload_weights(c, w);
+  if (rc == GR00T_OK) {
+    e = cudaMemsetAsync(c->err_flag, 0, 64, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->table, 0, (2 * c->L + 3) * sizeof(void*), c->stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+    if (e != cudaSuccess) rc = set_err(c, GR00T_ECUDA, "init failed: %s", cudaGetErrorString(e));
+  }
+  if (rc != GR00T_OK) {
+    g_create_err = c->err;
+    free_ctx(c);
+    return rc;
+  }
+  c->host_table.assign(2 * c->L + 3, nullptr);
+  *out = c;
+  return GR00T_OK;
+}
+
+extern "C" int gr00t_bind_prefix_kv(gr00t_ctx* c, int batch, int prefix, const void* const* k,
+                                    const void* const* v, const uint8_t* text_mask,
+                                    const uint8_t* image_mask, const float* state_tokens) {
+  if (!c) return GR00T_EINVAL;
+  const bool dit = c->g.family == GR00T_FAMILY_DIT;
+  if (batch < 1 || batch > c->g.max_batch)
+    return set_err(c, GR00T_EINVAL, "batch %d outside [1, %d]", batch, c->g.max_batch);
+  if (prefix < (dit ? 1 : 0) || prefix > c->g.max_prefix)
+    return set_err(c, GR00T_EINVAL, "prefix %d outside [%d, %d]", prefix, dit ? 1 : 0, c->g.max_prefix);
+  if (!dit && (text_mask || image_mask))
+    return set_err(c, GR00T_EINVAL, "the expert family takes no mask (its head fold needs the all-ones mask)");
+  if (!dit && state_tokens) return set_err(c, GR00T_EINVAL, "the expert family has no state tokens");
+  if (dit && c->Ns > 0 && !state_tokens) return set_err(c, GR00T_EINVAL, "state_tokens required");
+  if (prefix > 0 && (!k || !v)) return set_err(c, GR00T_EINVAL, "k/v pointer arrays are NULL");
+  std::vector<const void*> t(2 * c->L + 3, nullptr);
+  for (int l = 0; l < c->L; ++l) {
+    if (dit && l % 2 == 1) continue;
+    if (prefix == 0) continue;
+    if (!k[l] || !v[l]) return set_err(c, GR00T_EINVAL, "layer %d K/V pointer is NULL", l);
+    t[2 * l] = k[l];
+    t[2 * l + 1] = v[l];
+  }
+  t[2 * c->L] = text_mask;
+  t[2 * c->L + 1] = image_mask;
+  t[2 * c->L + 2] = state_tokens;
+  CK(c, cudaMemcpyAsync(c->table, t.data(), t.size() * sizeof(void*), cudaMemcpyHostToDevice, c->stream));
+  if (!dit) CK(c, rope_table(prefix, c->H, c->Dh, c->g.rope_theta, c->rope_tab, c->stream));
+  // masks / state are read through host_table at capture (slot presence, state pointer)
+  const bool layout_change = c->bB != batch || c->bP != prefix ||
+                             (c->host_table[2 * c->L] == nullptr) != (text_mask == nullptr) ||
+                             (c->host_table[2 * c->L + 1] == nullptr) != (image_mask == nullptr) ||
+                             c->host_table[2 * c->L + 2] != state_tokens;
+  if (layout_change && c->gexec) {
+    cudaGraphExecDestroy(c->gexec);
+    c->gexec = nullptr;
+  }
+  c->host_table = t;
+  c->bB = batch;
+  c->bP = prefix;
+  c->bound = true;
+  return GR00T_OK;
+}
+
+extern "C" int gr00t_set_schedule(gr00t_ctx* c, int steps, int batch) {
+  if (!c) return GR00T_EINVAL;
+  if (steps < 1 || steps > c->g.max_steps)
+    return set_err(c, GR00T_EINVAL, "steps %d outside [1, %d]", steps, c->g.max_steps);
+  if (batch < 1 || batch > c->g.max_batch)
+    return set_err(c, GR00T_EINVAL, "batch %d outside [1, %d]", batch, c->g.max_batch);
+  if (c->scheduled && c->sT == steps && c->sB == batch) return GR00T_OK;
+  const int TB = steps * batch, E = c->E, D = c->D;
+  c->launches = 0;
+  CK(c, time_embed(c->dt, steps, batch, E, c->g.direction, c->temb, c->dts, c->stream));
+  const void* cin = c->temb;
+  if (c->g.time_mlp) {
+    GemmArgs a;
+    a.A = c->temb; a.lda = E; a.W = c->w_tin; a.ldw = E; a.M = TB; a.N = E; a.K = E;
+    a.epi.kind = EPI_STORE; a.epi.act = ACT_SWISH; a.epi.bias = c->b_tin; a.epi.out = c->t1; a.epi.ldo = E;
+    RC(gemm(c, a));
+    GemmArgs b2 = a;
+    b2.A = c->t1; b2.W = c->w_tout; b2.epi.bias = c->b_tout; b2.epi.out = c->cvec;
+    RC(gemm(c, b2));
+    cin = c->cvec;
+  }
+  GemmArgs m;
+  m.A = cin; m.lda = E; m.W = c->w_cond; m.ldw = E; m.M = TB; m.N = c->S * c->R; m.K = E;
+  m.epi.kind = EPI_STORE; m.epi.bias = c->b_cond; m.epi.out = c->mod; m.epi.ldo = c->S * c->R;
+  RC(gemm(c, m));
+  if (c->g.family == GR00T_FAMILY_DIT) {
+    // action_time_bias [steps][D] = W2[:, D:] temb(tau_k) + b2, from the b = 0 rows
+    GemmArgs t;
+    t.A = c->temb; t.lda = batch * E; t.W = (const char*)c->w_enc2 + (size_t)D * c->esz; t.ldw = D + E;
+    t.M = steps; t.N = D; t.K = E;
+    t.epi.kind = EPI_STORE; t.epi.out_f32 = 1; t.epi.bias = c->b_enc2; t.epi.out = c->atb; t.epi.ldo = D;
+    RC(gemm(c, t));
+  }
+  if (c->gexec && (c->gT != steps || c->gB != batch)) {
+    cudaGraphExecDestroy(c->gexec);
+    c->gexec = nullptr;
+  }
+  c->sT = steps;
+  c->sB = batch;
+  c->scheduled = true;
+  return GR00T_OK;
+}
+
+extern "C" int gr00t_denoise(gr00t_ctx* c, const float* x_noise, float* actions) {
+  if (!c) return GR00T_EINVAL;
+  if (!x_noise || !actions) return set_err(c, GR00T_EINVAL, "x_noise/actions is NULL");
+  RC(check_ready(c));
+  const size_t bytes = (size_t)c->bB * c->H * c->A * sizeof(float);
+  CK(c, cudaMemcpyAsync(c->x, x_noise, bytes, cudaMemcpyDeviceToDevice, c->stream));
+  RC(run_loop(c));
+  CK(c, cudaMemcpyAsync(actions, c->x, bytes, cudaMemcpyDeviceToDevice, c->stream));
+  return GR00T_OK;
+}
+
+extern "C" int gr00t_denoise_host(gr00t_ctx* c, const float* x_noise_host, float* actions_host) {
+  if (!c) return GR00T_EINVAL;
+  if (!x_noise_host || !actions_host) return set_err(c, GR00T_EINVAL, "x_noise/actions is NULL");
+  RC(check_ready(c));
+  const size_t bytes = (size_t)c->bB * c->H * c->A * sizeof(float);
+  CK(c, cudaMemcpyAsync(c->x, x_noise_host, bytes, cudaMemcpyHostToDevice, c->stream));
+  RC(run_loop(c));
+  CK(c, cudaMemcpyAsync(actions_host, c->x, bytes, cudaMemcpyDeviceToHost, c->stream));
+  CK(c, cudaStreamSynchronize(c->stream));
+  return GR00T_OK;
+}
+
+extern "C" int gr00t_denoise_step(gr00t_ctx* c, int k, const float* x_in, float* v_out) {
+  if (!c) return GR00T_EINVAL;
+  if (!x_in || !v_out) return set_err(c, GR00T_EINVAL, "x_in/v_out is NULL");
+  RC(check_ready(c));
+  if (k < 0 || k >= c->sT) return set_err(c, GR00T_EINVAL, "step %d outside [0, %d)", k, c->sT);
+  const size_t bytes = (size_t)c->bB * c->H * c->A * sizeof(float);
+  CK(c, cudaMemcpyAsync(c->xtmp, x_in, bytes, cudaMemcpyDeviceToDevice, c->stream));
+  RC(enqueue_step(c, k, c->xtmp, v_out, 0));
+  return GR00T_OK;
+}
+
+extern "C" int gr00t_destroy(gr00t_ctx* c) {
+  if (!c) return GR00T_EINVAL;
+  free_ctx(c);
+  return GR00T_OK;
+}
+
+extern "C" const char* gr00t_last_error(const gr00t_ctx* c) {
+  return c ? c->err.c_str() : g_create_err.c_str();
+}
+
+extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
+  if (!c) return GR00T_EINVAL;
+  switch (option) {
+    case GR00T_OPT_USE_GRAPH:
+      c->opt_graph = value ? 1 : 0;
+      return GR00T_OK;
+    case GR00T_OPT_GEMM_PATH:
+      if (value != 0 && value != 1) return set_err(c, GR00T_EINVAL, "GEMM path must be 0 or 1");
+      c->opt_gemm = (int)value;
+      break;
+    case GR00T_OPT_ATTN_PATH:
+      if (value != 0 && value != 1) return set_err(c, GR00T_EINVAL, "attention path must be 0 or 1");
+      c->opt_attn = (int)value;
+      break;
+    case GR00T_OPT_WAIT_LIMIT:
+      if (value < 0) return set_err(c, GR00T_EINVAL, "wait limit must be >= 0");
+      c->wait_limit = value;
+      break;
+    case GR00T_OPT_TIME_KERNEL: {
+      if (value < 0 || value > GR00T_KCLASS_NORM) return set_err(c, GR00T_EINVAL, "unknown kernel class");
+      c->time_class = (int)value;
+      const size_t need = value ? (size_t)2 * c->g.max_steps * (2 * c->L + 4) : 0;
+      while (c->tev.size() < need) {
+        cudaEvent_t e;
+        CK(c, cudaEventCreate(&e));
+        c->tev.push_back(e);
+      }
+      break;
+    }
+    default:
+      return set_err(c, GR00T_EINVAL, "unknown option %d", option);
+  }
+  if (c->gexec) {  // kernels baked into the graph change
+    cudaGraphExecDestroy(c->gexec);
+    c->gexec = nullptr;
+  }
+  return GR00T_OK;
+}
+
+extern "C" int gr00t_get_info(gr00t_ctx* c, int what, int64_t* value) {
+  if (!c || !value) return GR00T_EINVAL;
+  switch (what) {
+    case GR00T_INFO_KERNELS_PER_STEP:
+      *value = c->launches;
+      return GR00T_OK;
+    case GR00T_INFO_WEIGHT_BYTES: {
+      long long b = 0;
+      const int up_rows = (c->g.mlp_kind == GR00T_MLP_GEGLU ? 2 : 1) * c->F;
+      for (int l = 0; l < c->L; ++l)
+        b += ((long long)c->nqkv[l] * c->D + (long long)c->D * c->qd + (long long)up_rows * c->D +
+              (long long)c->D * c->F) * c->esz;
+      b += (long long)c->A * c->D * c->esz;
+      if (c->g.family == GR00T_FAMILY_EXPERT)
+        b += (long long)c->D * c->A * c->esz;
+      else
+        b += ((long long)c->D * c->A + (long long)c->D * c->D * 2) * c->esz;
+      *value = b;
+      return GR00T_OK;
+    }
+    case GR00T_INFO_DEVICE_BYTES:
+      *value = (int64_t)c->arena_bytes;
+      return GR00T_OK;
+    case GR00T_INFO_ERROR_FLAG: {
+      int f = 0;
+      CK(c, cudaMemcpyAsync(&f, c->err_flag, sizeof f, cudaMemcpyDeviceToHost, c->stream));
+      CK(c, cudaStreamSynchronize(c->stream));
+      *value = f;
+      return GR00T_OK;
+    }
+    default:
+      return set_err(c, GR00T_EINVAL, "unknown info %d", what);
+  }
+}
+
+extern "C" int gr00t_kernel_times(gr00t_ctx* c, float* ms, int max, int* count) {
+  if (!c || !count || (max > 0 && !ms)) return GR00T_EINVAL;
+  CK(c, cudaStreamSynchronize(c->stream));
+  const int pairs = c->tev_used / 2;
+  int n = 0;
+  for (int i = 0; i < pairs && n < max; ++i) {
+    float t = 0.f;
+    CK(c, cudaEventElapsedTime(&t, c->tev[2 * i], c->tev[2 * i + 1]));
+    ms[n++] = t;
+  }
+  *count = n;
+  return GR00T_OK;
+}

@@ -1,0 +1,273 @@
+/*
+ * gr00t.h -- C ABI of the GB300 (sm_103a) flow-matching action-expert denoise loop.
+ *
+ * The library runs the hot path of a flow-matching Vision-Language-Action
+ * policy: the action expert's denoise loop.  The prefix (vision-language)
+ * K/V is computed elsewhere and bound once; the library hoists the time
+ * conditioning, then integrates an action chunk from noise with T Euler
+ * steps, each step one evaluation of the expert stack.
+ *
+ * Two model families share the interface:
+ *   GR00T_FAMILY_EXPERT -- pi0.5-style action expert ("pi0.5 Design",
+ *       TensorRT Edge-LLM developer guide): AdaRMS norms, a single shared KV
+ *       head, attention over prefix K/V ++ the action tokens' own K/V.
+ *   GR00T_FAMILY_DIT    -- GR00T-N1.7-style DiT head ("GR00T N1.7",
+ *       TensorRT Edge-LLM developer guide): AdaLayerNorm, blocks alternating
+ *       cross-attention into the VL context and self-attention over the
+ *       state + action tokens.
+ *
+ * Conventions shared by every call:
+ *   - Every function returns GR00T_OK (0) or a negative GR00T_E* status.
+ *     gr00t_last_error() gives a one-line text for the context's last error.
+ *   - Work is enqueued on the CUDA stream given to gr00t_create and is
+ *     asynchronous unless stated otherwise.  A context is not thread-safe
+ *     (one stream, one caller), as the pages' runtimes are not.
+ *   - Matrices are row-major.  Weights use the nn.Linear layout [out, in].
+ *   - "bf16" tensors are raw IEEE bfloat16 bit patterns (uint16_t).
+ *   - Nothing here allocates on a call except gr00t_create (and graph
+ *     instantiation on the first denoise of a new (steps, batch, prefix)).
+ *   - No call ever falls back to the CPU.  Without a usable sm_103a device
+ *     gr00t_create returns GR00T_ECUDA.
+ */
+#ifndef GR00T_H_
+#define GR00T_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GR00T_ABI_VERSION 1
+
+/* ---- status codes ------------------------------------------------------ */
+#define GR00T_OK 0
+#define GR00T_EINVAL (-1)      /* bad argument or geometry; nothing was done   */
+#define GR00T_ENOMEM (-2)      /* a device allocation failed                   */
+#define GR00T_ECUDA (-3)       /* a CUDA runtime/driver call failed            */
+#define GR00T_ESTATE (-4)      /* call out of order (e.g. denoise before bind) */
+#define GR00T_EUNSUPPORTED (-5)/* valid request this build does not implement  */
+#define GR00T_ETIMEOUT (-6)    /* a bounded device wait gave up                */
+
+/* ---- enumerations ------------------------------------------------------ */
+#define GR00T_FAMILY_EXPERT 0
+#define GR00T_FAMILY_DIT 1
+#define GR00T_DTYPE_FP32 0
+#define GR00T_DTYPE_BF16 1
+#define GR00T_MLP_GELU 0       /* u = gelu_tanh(n W_up^T)                        */
+#define GR00T_MLP_GEGLU 1      /* u = gelu_tanh(n W_gate^T) * (n W_up^T)         */
+#define GR00T_MEM_HOST 0
+#define GR00T_MEM_DEVICE 1
+
+/*
+ * Geometry of one expert.  Validated by gr00t_create before anything is
+ * allocated ("GR00T N1.7": a mismatch fails before a network is created;
+ * "pi0.5 Design": a configuration the runtime does not implement is refused
+ * at load rather than run).
+ *
+ * EXPERT family: kv_heads must be 1 (the head fold is exact only with a
+ * single KV head and an all-ones mask, "pi0.5 Design", Attention and the K/V
+ * pool); the modulation table has 2*layers+1 sites of width 3*hidden, packed
+ * (scale, shift, gate), site 2i = layer i input norm, 2i+1 = its post-
+ * attention norm, 2*layers = final norm ("pi0.5 Design", Component contract).
+ * DIT family: kv_heads == q_heads; layers even; blocks alternate cross-
+ * attention (even index) and self-attention (odd index) ("GR00T N1.7",
+ * action); layers+1 sites of width 2*hidden, (scale, shift) for blocks and
+ * (shift, scale) for the final norm ("GR00T N1.7", Build-time constants).
+ */
+typedef struct gr00t_geometry {
+  int32_t abi_version;   /* GR00T_ABI_VERSION                                */
+  int32_t family;        /* GR00T_FAMILY_*                                    */
+  int32_t dtype;         /* GR00T_DTYPE_*: weight, K/V and activation type    */
+  int32_t layers;        /* transformer layers / DiT blocks                   */
+  int32_t hidden;        /* D, residual width (multiple of 64)               */
+  int32_t q_heads;       /* query heads                                      */
+  int32_t kv_heads;      /* K/V heads (EXPERT: 1; DIT: q_heads)              */
+  int32_t head_dim;      /* Dh (EXPERT: 64 or 256; DIT: 48)                   */
+  int32_t mlp_dim;       /* F, MLP width (multiple of 64)                     */
+  int32_t mlp_kind;      /* GR00T_MLP_*                                       */
+  int32_t horizon;       /* H, action tokens per chunk                        */
+  int32_t action_dim;    /* A, command dimensions per action                  */
+  int32_t state_tokens;  /* DIT: state tokens ahead of the actions (0 or 1)   */
+  int32_t time_dim;      /* E, sinusoidal time-embedding width (even, >= 4)   */
+  int32_t time_mlp;      /* 1: c = swish(W_out swish(W_in temb + b) + b)      */
+  int32_t direction;     /* -1: integrate tau 1 -> 0; +1: tau 0 -> 1          */
+  int32_t max_batch;     /* largest batch a schedule/bind may use             */
+  int32_t max_prefix;    /* largest prefix / VL-context length                */
+  int32_t max_steps;     /* largest denoise step count                        */
+  float rope_theta;      /* RoPE base (EXPERT family)                         */
+  float norm_eps;        /* epsilon of RMSNorm / LayerNorm                    */
+} gr00t_geometry;
+
+/*
+ * Weights, all in the geometry's dtype (fp32 or bf16), nn.Linear [out, in].
+ * ``location`` says whether every pointer is host or device memory.  The
+ * library COPIES them into its own re-laid-out device buffers during
+ * gr00t_create; the caller may free them as soon as it returns.
+ * Pointers a family does not use must be NULL.
+ *
+ *   time_mlp_{in,out}_w [E, E], _b [E]       if time_mlp
+ *   cond_w [S, R, E], cond_b [S, R]          the S adaptive-norm Denses
+ *                                            ("pi0.5 Design": 37 [3072,1024])
+ *   EXPERT: action_in_w [D, A], action_in_b [D]
+ *   DIT:    enc_w1 [D, A], enc_b1 [D], enc_w2 [D, D+E] acting on
+ *           concat(W1 x + b1, temb(tau)), enc_b2 [D], enc_w3 [D, D], enc_b3 [D]
+ *   action_out_w [A, D], action_out_b [A]
+ *   per layer l (arrays of ``layers`` pointers):
+ *     qkv_w[l]  EXPERT: [Hq*Dh + 2*Dh, D] rows (q heads, k, v)
+ *               DIT even l: [Hq*Dh, D] (q only); odd l: [3*Hq*Dh, D] (q, k, v)
+ *     o_w[l]    [D, Hq*Dh]
+ *     up_w[l]   GEGLU: [2F, D], rows [0,F) gate, [F,2F) up;  GELU: [F, D]
+ *     down_w[l] [D, F]
+ */
+typedef struct gr00t_weights {
+  int32_t location; /* GR00T_MEM_HOST or GR00T_MEM_DEVICE */
+  const void* time_mlp_in_w;
+  const void* time_mlp_in_b;
+  const void* time_mlp_out_w;
+  const void* time_mlp_out_b;
+  const void* cond_w;
+  const void* cond_b;
+  const void* action_in_w;
+  const void* action_in_b;
+  const void* enc_w1;
+  const void* enc_b1;
+  const void* enc_w2;
+  const void* enc_b2;
+  const void* enc_w3;
+  const void* enc_b3;
+  const void* action_out_w;
+  const void* action_out_b;
+  const void* const* qkv_w;
+  const void* const* o_w;
+  const void* const* up_w;
+  const void* const* down_w;
+} gr00t_weights;
+
+typedef struct gr00t_ctx gr00t_ctx;
+
+/*
+ * Check a geometry without touching the GPU.  Returns GR00T_OK or
+ * GR00T_EINVAL / GR00T_EUNSUPPORTED; ``msg`` (may be NULL) receives a
+ * NUL-terminated reason of at most ``msg_len`` bytes.
+ */
+int gr00t_validate_geometry(const gr00t_geometry* g, char* msg, size_t msg_len);
+
+/*
+ * Create a context on the current CUDA device: validate the geometry, copy
+ * and re-lay-out the weights, allocate every buffer the loop needs for
+ * (max_batch, max_prefix, max_steps).  ``stream`` is a cudaStream_t (may be
+ * NULL for the legacy default stream); every later call enqueues on it.
+ * The device must be sm_103 (GB300).  On failure *out is NULL and nothing
+ * stays allocated.  Synchronous.
+ */
+int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, void* stream, gr00t_ctx** out);
+
+/*
+ * Bind the per-request prefix / VL-context K/V for the whole denoise loop
+ * ("GR00T N1.7", Who runs what: runs once, its outputs stay bound for the
+ * whole denoise loop; "pi0.5 Design": prefix K/V (bound once)).
+ *
+ * ``k``, ``v``: arrays of ``layers`` DEVICE pointers, each to a contiguous
+ * [batch, prefix, kv_heads, head_dim] tensor in the geometry's dtype.  EXPERT:
+ * every layer, keys already rotated by RoPE at positions 0..prefix-1.  DIT:
+ * even layers only (odd entries ignored, may be NULL).  The memory is
+ * BORROWED: the caller keeps it alive and unchanged until the next bind or
+ * gr00t_destroy.  The pointers land in a device-side table, so a rebind at
+ * the same (batch, prefix) reuses the captured graph.
+ *
+ * ``text_mask``/``image_mask``: DIT only, DEVICE uint8 [batch, prefix],
+ * 1 = visible; block i reads the text mask when i % 4 == 0 and the image
+ * mask otherwise ("GR00T N1.7", action).  NULL = all visible.  Must be NULL
+ * for EXPERT (its head fold needs the all-ones mask).
+ * ``state_tokens``: DIT only, DEVICE fp32 [batch, state_tokens, hidden], the
+ * embedded robot state placed ahead of the action tokens; borrowed.
+ * 1 <= batch <= max_batch; 0 <= prefix <= max_prefix (EXPERT), 1 <= prefix
+ * (DIT).  Enqueues a small copy on the stream.
+ */
+int gr00t_bind_prefix_kv(gr00t_ctx* ctx, int batch, int prefix, const void* const* k,
+                         const void* const* v, const uint8_t* text_mask,
+                         const uint8_t* image_mask, const float* state_tokens);
+
+/*
+ * Hoist the time conditioning for a step count and batch ("pi0.5 Design",
+ * cond component: the time embedder and the AdaRMS Denses move out of the
+ * per-step graph and re-run only when the step count or batch changes;
+ * "GR00T N1.7", Build-time constants).  Builds the modulation table
+ * [steps * batch, sites, row] (rows [step][request]), the Euler step sizes
+ * on the uniform grid of vla.cpp Eq. (1), and for DIT the action_time_bias
+ * [steps, hidden].  A call with the same (steps, batch) as the last one is a
+ * no-op.  1 <= steps <= max_steps; 1 <= batch <= max_batch.
+ */
+int gr00t_set_schedule(gr00t_ctx* ctx, int steps, int batch);
+
+/*
+ * Run the whole denoise loop: T = steps Euler steps x_{k+1} = x_k +
+ * (tau_{k+1} - tau_k) v(x_k, tau_k) (vla.cpp Eq. (1)), starting from the
+ * caller's noise.  ``x_noise`` and ``actions`` are DEVICE fp32 [batch,
+ * horizon, action_dim] (batch of the last bind, which must equal the last
+ * schedule's); they may alias.  Returns the model-space chunk (before any
+ * policy unnormalisation).  Requires a bind and a schedule (GR00T_ESTATE
+ * otherwise).  The T steps replay as one CUDA graph captured on the first
+ * call for a (steps, batch, prefix).  Asynchronous on the stream.
+ */
+int gr00t_denoise(gr00t_ctx* ctx, const float* x_noise, float* actions);
+
+/*
+ * gr00t_denoise with HOST buffers: copies ``x_noise`` in, runs the loop,
+ * copies the chunk out and synchronises the stream before returning.
+ * Page-locked host memory gives asynchronous copies; pageable works.
+ */
+int gr00t_denoise_host(gr00t_ctx* ctx, const float* x_noise_host, float* actions_host);
+
+/*
+ * One velocity evaluation at step k of the current schedule (teacher
+ * forcing, for tests): ``v_out`` = v(x_in, tau_k); x_in is not modified.
+ * DEVICE fp32 [batch, horizon, action_dim].  0 <= k < steps.  Runs eagerly.
+ */
+int gr00t_denoise_step(gr00t_ctx* ctx, int k, const float* x_in, float* v_out);
+
+/* Free everything the context owns (synchronises its stream first). */
+int gr00t_destroy(gr00t_ctx* ctx);
+
+/* Text of the context's last error ("" if none).  ctx may be NULL: the
+ * last error of a failed gr00t_create on this thread. */
+const char* gr00t_last_error(const gr00t_ctx* ctx);
+
+/* ---- options and introspection ----------------------------------------- */
+#define GR00T_OPT_USE_GRAPH 1     /* 1 (default): replay the loop as a CUDA graph */
+#define GR00T_OPT_GEMM_PATH 2     /* 0: tensor-core path where supported (default), 1: CUDA-core path */
+#define GR00T_OPT_WAIT_LIMIT 3    /* spin-wait iteration limit of bounded device waits (>= 0) */
+#define GR00T_OPT_ATTN_PATH 4     /* 0: tensor-core attention where supported (default), 1: CUDA-core */
+#define GR00T_OPT_TIME_KERNEL 5   /* bracket every launch of one kernel class with timing events
+                                     (GR00T_KCLASS_*, 0 = off); read with gr00t_kernel_times */
+int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
+
+#define GR00T_INFO_KERNELS_PER_STEP 1   /* kernel launches of one denoise step            */
+#define GR00T_INFO_WEIGHT_BYTES 2       /* bytes of weights one step reads                */
+#define GR00T_INFO_DEVICE_BYTES 3       /* device memory the context owns                 */
+#define GR00T_INFO_ERROR_FLAG 4         /* device error word (bounded waits), 0 if clean  */
+int gr00t_get_info(gr00t_ctx* ctx, int what, int64_t* value);
+
+/* Kernel classes of one denoise step, for GR00T_OPT_TIME_KERNEL. */
+#define GR00T_KCLASS_QKV_GEMM 1    /* fused Q/K/V projection (+ RoPE epilogue)          */
+#define GR00T_KCLASS_ATTENTION 2   /* attention over prefix ++ suffix K/V                */
+#define GR00T_KCLASS_O_GEMM 3      /* output projection + (gated) residual               */
+#define GR00T_KCLASS_UP_GEMM 4     /* MLP gate/up projection + GeGLU / GeLU              */
+#define GR00T_KCLASS_DOWN_GEMM 5   /* MLP down projection + (gated) residual             */
+#define GR00T_KCLASS_NORM 6        /* adaptive norms, step head and tail                 */
+
+/*
+ * Durations in milliseconds of the launches bracketed under
+ * GR00T_OPT_TIME_KERNEL during the most recent gr00t_denoise (CUDA events on
+ * the context's stream, recorded inside the captured graph).  Writes at most
+ * ``max`` values to ``ms`` and their number to ``*count``.  Synchronises the
+ * stream.
+ */
+int gr00t_kernel_times(gr00t_ctx* ctx, float* ms, int max, int* count);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GR00T_H_ */

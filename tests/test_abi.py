@@ -1,0 +1,125 @@
+"""Host-side checks that need no GPU: the library loads, exports what the
+header declares, validates geometries, and refuses bad calls with statuses."""
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from flow_matching_vla_gb300 import build
+    build.build()
+    from flow_matching_vla_gb300 import _abi
+    return _abi.load()
+
+
+def test_every_declared_function_is_exported(lib):
+    from flow_matching_vla_gb300 import _abi
+    declared = _abi.header_functions()
+    assert len(declared) >= 12
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    for name in declared:
+        assert name in exported, name
+        assert name in _abi.SIGNATURES, name
+        getattr(lib, name)
+
+
+def test_library_is_sm103a_only(lib):
+    from flow_matching_vla_gb300 import _abi
+    out = subprocess.run(["cuobjdump", "--list-elf", _abi.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    assert "sm_103a" in out.stdout
+    assert all("sm_103" in l for l in out.stdout.splitlines() if ".cubin" in l)
+
+
+@pytest.mark.parametrize("name", sorted(synth.CONFIGS))
+def test_workload_geometries_validate(lib, name):
+    import flow_matching_vla_gb300 as fmv
+    rc, msg = fmv.validate_geometry(synth.config(name))
+    assert rc == 0, msg
+
+
+@pytest.mark.parametrize("field,value,needle", [
+    ("kv_heads", 2, "kv_heads"),
+    ("hidden", 100, "hidden"),
+    ("direction", 0, "direction"),
+    ("head_dim", 512, "head_dim"),
+    ("max_steps", 0, "max_steps"),
+    ("layers", 0, "layers"),
+    ("mlp_kind", 7, "mlp_kind"),
+    ("norm_eps", 0.0, "norm_eps"),
+])
+def test_bad_geometry_is_refused(lib, field, value, needle):
+    import flow_matching_vla_gb300 as fmv
+    g = synth.config("pi05")
+    g[field] = value
+    if field == "max_steps":
+        g["steps"] = value
+    rc, msg = fmv.validate_geometry(g)
+    assert rc == -1 and needle in msg
+
+
+def test_dit_geometry_rules(lib):
+    import flow_matching_vla_gb300 as fmv
+    g = synth.config("gr00t")
+    g["kv_heads"] = 1
+    assert fmv.validate_geometry(g)[0] == -1
+    g = synth.config("gr00t", prefix=0)
+    assert fmv.validate_geometry(g)[0] == -1
+
+
+def test_create_refuses_before_touching_cuda(lib):
+    from flow_matching_vla_gb300 import _abi
+    import flow_matching_vla_gb300 as fmv
+    g = synth.config("pi05")
+    g["kv_heads"] = 3
+    geo = fmv._geometry(g)
+    ctx = ctypes.c_void_p(1)
+    w = _abi.Weights()
+    rc = lib.gr00t_create(ctypes.byref(geo), ctypes.byref(w), None, ctypes.byref(ctx))
+    assert rc == -1 and ctx.value is None
+    assert b"kv_heads" in lib.gr00t_last_error(None)
+    # NULL out pointer
+    assert lib.gr00t_create(ctypes.byref(geo), ctypes.byref(w), None, None) == -1
+
+
+def test_null_context_calls_are_einval(lib):
+    assert lib.gr00t_set_schedule(None, 1, 1) == -1
+    assert lib.gr00t_denoise(None, None, None) == -1
+    assert lib.gr00t_destroy(None) == -1
+    v = ctypes.c_int64()
+    assert lib.gr00t_get_info(None, 1, ctypes.byref(v)) == -1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    code = ("import flow_matching_vla_gb300._abi as a; a.LIB_PATH='" + str(tmp_path / "nope.so") + "'\n"
+            "try:\n    a.load()\nexcept RuntimeError as e:\n    print('raised', e)\n")
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT)
+    assert "raised" in out.stdout and "no CPU fallback" in out.stdout
+
+
+def test_bench_work_accounting_matches_weight_shapes():
+    import bench
+    g = synth.config("pi05")
+    w = bench.kernel_work(g, 1, 968)
+    gemm_weight_bytes = sum(2 * int(np.prod(s)) for k, s in synth.weight_shapes(g).items() if "." in k)
+    # every weight byte of the 18 layers is read exactly once per denoise step
+    M = 50
+    act = 0
+    for name in ("qkv_gemm", "o_gemm", "up_gemm", "down_gemm"):
+        n, by, fl = w[name]
+        assert n == 18
+    total_w = sum(w[k][0] * w[k][1] for k in ("qkv_gemm", "o_gemm", "up_gemm", "down_gemm"))
+    assert gemm_weight_bytes < total_w < gemm_weight_bytes * 1.08   # + activations
+    kv = w["attention"][0] * w["attention"][1]
+    assert kv > 18 * 968 * 256 * 2 * 2

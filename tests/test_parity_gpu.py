@@ -1,0 +1,134 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Gates: fp32 workloads rel-L2 <= 1e-4 (velocity per step and final chunk);
+bf16 workloads per-step velocity rel-L2 <= 1e-2 (teacher forced: both sides
+step from the oracle's x_k) and final chunk max-abs <= 2e-2 (free running).
+Errors are vla.cpp Eq. (5).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+FP32_REL = 1e-4
+BF16_VEL_REL = 1e-2
+BF16_CHUNK_ABS = 2e-2
+
+
+def _fmv():
+    import flow_matching_vla_gb300 as fmv
+    return fmv
+
+
+def _trajectory(case, steps=None):
+    """Oracle x_k (fp64) and v_k for k = 0..T-1, plus x_T."""
+    g = case["geom"]
+    T = steps or g["steps"]
+    xT, vs = oracle.denoise(case, steps=T, record=True)
+    _, dts = oracle.schedule(g["direction"], T)
+    xs = [case["x_noise"].astype(np.float64)]
+    for k in range(T - 1):
+        xs.append(xs[-1] + dts[k] * vs[k])
+    return xs, vs, xT
+
+
+def _gates(case):
+    bf16 = case["geom"]["dtype"] == synth.DTYPE_BF16
+    return (BF16_VEL_REL, None) if bf16 else (FP32_REL, FP32_REL)
+
+
+def check_case(case, steps=None, samples=None):
+    """Run the GPU loop on ``case`` and compare with the oracle.
+
+    ``samples``: only compare these batch entries (the oracle runs them as
+    batch-1 problems on their own inputs); None compares all of them.
+    """
+    fmv = _fmv()
+    g = case["geom"]
+    T = steps or g["steps"]
+    loop, held = fmv.from_case(case, steps=T)
+    x0 = torch.from_numpy(case["x_noise"]).cuda()
+    out = loop.denoise(x0)
+    # teacher-forced velocities need the oracle trajectory of the compared samples
+    idx = list(range(g["batch"])) if samples is None else list(samples)
+    sub = case if samples is None else _subcase(case, idx)
+    xs, vs, xT = _trajectory(sub, T)
+    vel_tol, chunk_rel = _gates(case)
+    worst = 0.0
+    for k in range(T):
+        xk = np.zeros(case["x_noise"].shape, np.float32)
+        xk[idx] = xs[k].astype(np.float32)
+        v = loop.denoise_step(k, torch.from_numpy(xk).cuda()).cpu().numpy()[idx]
+        e_inf, e_rel = oracle.error_metrics(v, vs[k])
+        worst = max(worst, e_rel)
+        assert e_rel <= vel_tol, f"step {k}: velocity rel-L2 {e_rel:.3e} > {vel_tol}"
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()[idx]
+    e_inf, e_rel = oracle.error_metrics(got, xT)
+    if chunk_rel is not None:
+        assert e_rel <= chunk_rel, f"final chunk rel-L2 {e_rel:.3e}"
+    else:
+        assert e_inf <= BF16_CHUNK_ABS, f"final chunk max-abs {e_inf:.3e}"
+    assert np.all(np.isfinite(out.cpu().numpy()))
+    return loop, worst, e_inf, e_rel
+
+
+def _subcase(case, idx):
+    c = dict(case)
+    c["x_noise"] = case["x_noise"][idx]
+    c["K"] = [None if k is None else k[idx] for k in case["K"]]
+    c["V"] = [None if v is None else v[idx] for v in case["V"]]
+    for key in ("text_mask", "image_mask", "state"):
+        if case.get(key) is not None:
+            c[key] = case[key][idx]
+    c["geom"] = dict(case["geom"], batch=len(idx))
+    return c
+
+
+@pytest.mark.parametrize("name", ["tiny", "small_fp32", "small_dit_fp32"])
+def test_fp32_parity(name):
+    check_case(synth.make_case(name))
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "small_dit"])
+def test_bf16_parity_small(name):
+    check_case(synth.make_case(name))
+
+
+def test_dit_random_masks():
+    c = synth.make_case("small_dit")
+    c["text_mask"], c["image_mask"] = synth.make_masks(c["geom"], 0, kind="random")
+    check_case(c)
+
+
+def test_expert_empty_prefix_and_single_token():
+    check_case(synth.make_case("small_bf16", prefix=0, horizon=1, batch=2))
+
+
+def test_expert_fp32_empty_prefix():
+    check_case(synth.make_case("small_fp32", prefix=0))
+
+
+@pytest.mark.parametrize("steps", [1, 2, 5])
+def test_step_counts(steps):
+    check_case(synth.make_case("small_bf16"), steps=steps)
+
+
+def test_pi05_full_size():
+    check_case(synth.make_case("pi05"))
+
+
+def test_gr00t_full_size():
+    check_case(synth.make_case("gr00t"))
+
+
+def test_pi05_batch32_sampled():
+    check_case(synth.make_case("pi05_b32"), samples=[0, 31])
+
+
+def test_pi05_long_prefix_sampled():
+    check_case(synth.make_case("pi05_long"), samples=[0, 7])
