@@ -115,7 +115,7 @@ def test_expert_fp32_empty_prefix():
 
 @pytest.mark.parametrize("steps", [1, 2, 5])
 def test_step_counts(steps):
-    check_case(synth.make_case("small_bf16"), steps=steps)
+    check_case(synth.make_case("small_bf16", steps=steps))
 
 
 def test_pi05_full_size():
