@@ -1,0 +1,272 @@
+// Tensor-core GEMM for the denoise step: Y[M, N] = X[M, K] W[N, K]^T, bf16 in,
+// fp32 accumulate in tensor memory (tcgen05.mma, kind::f16), fused epilogues.
+//
+// Shapes are weight-streaming: N (weight rows) is large, M (token rows) is
+// 50..1600.  The weight therefore plays the MMA's M role ("swap-AB"): each
+// CTA owns 128 weight rows and BN tokens, D[128, BN] lives in TMEM.
+//
+//  * TMA (cp.async.bulk.tensor, 128-byte swizzle) streams 128x64 weight tiles
+//    (L2 evict-first) and BNx64 activation tiles (L2 evict-last) through a
+//    STAGES-deep mbarrier ring; one thread issues loads, one issues MMAs.
+//  * Split-K across a thread-block cluster (1 x 1 x S, S <= 16): every CTA of
+//    the cluster accumulates a K slice, parks its fp32 partial in its own
+//    shared memory, and after a cluster barrier each CTA reduces 128/S rows
+//    over the S partials through distributed shared memory, in rank order
+//    (deterministic), and applies the epilogue to them.
+//  * Programmatic dependent launch: weight tiles (which no earlier kernel
+//    writes) are prefetched before griddepcontrol.wait; activations after.
+//  * Every mbarrier wait is bounded; on timeout the CTA records an error
+//    flag for the host, drains its own in-flight copies and exits normally.
+#include <cooperative_groups.h>
+#include <cudaTypedefs.h>
+
+#include "epilogue.cuh"
+#include "gemm_tc.h"
+#include "tc_ptx.cuh"
+
+namespace g3 {
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int BM = 128;  // weight rows per CTA (MMA M)
+constexpr int BK = 64;   // K elements per stage: one 128-byte swizzle row of bf16
+constexpr int A_BYTES = BM * BK * 2;
+
+template <int BN, int STAGES>
+struct TcSmem {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int PIPE = STAGES * STAGE_BYTES;
+  static constexpr int RED = BN * BM * 4;  // fp32 partial, reuses the pipeline buffers
+  static_assert(RED <= PIPE, "partial must fit in the pipeline buffers");
+  static constexpr int BAR = (2 * STAGES + 1) * 8 + 16;
+  static constexpr int TOTAL = PIPE + BAR + 1024;  // + alignment slack
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(128, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
+                   int N, int kb_per_split, Epi e, int* err, long long wait_limit) {
+  using L = TcSmem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::PIPE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* done = empty + STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(smem);
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int S = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
+  const int kb0 = blockIdx.z * kb_per_split;
+  const int nkb = kb_per_split;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    ptx::mbar_init(done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmX);
+  }
+  if (warp == 2) ptx::tmem_alloc(tmem_slot, BN);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  ptx::pdl_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pw = ptx::policy_evict_first(), px = ptx::policy_evict_last();
+      // weights first: no earlier kernel writes them, so they stream before the dependency wait
+      const int pre = nkb < STAGES ? nkb : STAGES;
+      for (int i = 0; i < pre; ++i) {
+        ptx::mbar_arrive_expect_tx(&full[i], L::STAGE_BYTES);
+        ptx::tma_load_2d(sA + i * A_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0, pw);
+      }
+      ptx::pdl_wait();
+      int issued = pre;
+      bool ok = true;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES) {
+          if (!ptx::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, wait_limit)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+          ptx::tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, n0, pw);
+          issued = i + 1;
+        }
+        ptx::tma_load_2d(sB + s * L::B_BYTES, &tmX, &full[s], (kb0 + i) * BK, m0, px);
+      }
+      if (!ok) {
+        atomicExch(abort_flag, 1);
+        atomicExch(err, 1);
+        // drain: wait (bounded) for the copies this thread armed last on each stage
+        for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
+          ptx::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, wait_limit);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (!ptx::mbar_wait(&full[s], (i / STAGES) & 1, wait_limit)) {
+          atomicExch(abort_flag, 1);
+          atomicExch(err, 1);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint64_t ad = ptx::sdesc_sw128(ptx::smem_u32(sA + s * A_BYTES));
+        const uint64_t bd = ptx::sdesc_sw128(ptx::smem_u32(sB + s * L::B_BYTES));
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k)  // 16 bf16 = 32 bytes = 2 descriptor units per MMA
+          ptx::mma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (i | k) != 0);
+        ptx::mma_commit(&empty[s]);
+      }
+      ptx::mma_commit(done);
+    }
+  }
+  __syncwarp();
+  // every thread but the producer (which waited before its activation loads)
+  // waits for the previous kernel before touching activation memory
+  if (threadIdx.x != 0) ptx::pdl_wait();
+
+  // accumulator -> own shared memory, transposed to [token][row] (conflict-free)
+  if (!ptx::mbar_wait(done, 0, wait_limit)) {
+    atomicExch(abort_flag, 1);
+    atomicExch(err, 1);
+  }
+  __syncthreads();
+  ptx::tc_fence_after();
+  const int row = warp * 32 + lane;
+  if (!*abort_flag) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float v[16];
+      ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) red[(c0 + j) * BM + row] = v[j];
+    }
+  }
+  ptx::tc_fence_before();
+  cluster.sync();
+
+  // rank r reduces rows [r*R, r*R + R) over the S partials, in rank order
+  const bool aborted = *abort_flag != 0;
+  const int R = BM / S, pairs = R / 2;
+  if (!aborted) {
+    for (int it = threadIdx.x; it < pairs * BN; it += blockDim.x) {
+      const int p = it % pairs, j = it / pairs;
+      const int r0 = rank * R + 2 * p;
+      const int m = m0 + j, n = n0 + r0;
+      if (m >= M || n >= N) continue;
+      float a0 = 0.f, a1 = 0.f;
+      for (int s = 0; s < S; ++s) {
+        const float* peer = cluster.map_shared_rank(red, s);
+        const float2 v = *reinterpret_cast<const float2*>(peer + j * BM + r0);
+        a0 += v.x;
+        a1 += v.y;
+      }
+      epi_pair<bf16>(e, m, n, a0, a1);
+    }
+  }
+  cluster.sync();  // peers finished reading this CTA's partial
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, BN);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+template <int BN, int STAGES>
+cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int S, int* err,
+                   long long lim, cudaStream_t s, bool pdl) {
+  using L = TcSmem<BN, STAGES>;
+  auto kern = gemm_tc_kernel<BN, STAGES>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e1 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e1 != cudaSuccess) return e1;
+    e1 = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e1 != cudaSuccess) return e1;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.N + BM - 1) / BM, (a.M + BN - 1) / BN, S);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = L::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = S;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const int KB = a.K / BK;
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, err, lim);
+}
+
+}  // namespace
+
+cudaError_t tc_make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld,
+                        int box_rows) {
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&g_encode, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode) return cudaErrorNotSupported;
+  }
+  if (((uintptr_t)ptr & 15) || (ld * 2) % 16 || cols % BK) return cudaErrorInvalidValue;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+TcPlan tc_plan(int M, int N, int K, int sm_count) {
+  TcPlan p;
+  p.BN = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+  const int KB = K / BK;
+  const long long tiles = (long long)((N + BM - 1) / BM) * ((M + p.BN - 1) / p.BN);
+  p.S = 1;
+  while (p.S < 16 && KB % (2 * p.S) == 0 && tiles * 2 * p.S <= sm_count + sm_count / 16) p.S *= 2;
+  return p;
+}
+
+bool tc_supported(int M, int N, int K) { return M > 0 && N > 0 && K > 0 && K % BK == 0 && N % 2 == 0; }
+
+cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
+                    int* err, long long wait_limit, cudaStream_t s, bool pdl) {
+  if (!tc_supported(a.M, a.N, a.K) || (a.K / BK) % p.S) return cudaErrorInvalidValue;
+  switch (p.BN) {
+    case 64: return launch<64, 4>(tw, tx, a, p.S, err, wait_limit, s, pdl);
+    case 128: return launch<128, 4>(tw, tx, a, p.S, err, wait_limit, s, pdl);
+    case 256: return launch<256, 4>(tw, tx, a, p.S, err, wait_limit, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace g3

@@ -1,0 +1,26 @@
+// Host interface of the tcgen05 tensor-core GEMM (internal to the library).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+
+namespace g3 {
+
+struct TcPlan {
+  int BN = 64;  // token columns per CTA (MMA N): 64, 128 or 256
+  int S = 1;    // split-K factor = cluster size along K (power of two, <= 16)
+};
+
+// K-major bf16 tensor map over a [rows][cols] matrix with leading dimension
+// ``ld`` elements; box = 64 columns x box_rows rows, 128-byte swizzle.
+cudaError_t tc_make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld,
+                        int box_rows);
+bool tc_supported(int M, int N, int K);
+TcPlan tc_plan(int M, int N, int K, int sm_count);
+// W map: box_rows 128 over [N][K]; X map: box_rows plan.BN over [M][K].
+cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
+                    int* err, long long wait_limit, cudaStream_t s, bool pdl);
+
+}  // namespace g3

@@ -9,9 +9,12 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <string>
+#include <tuple>
 #include <vector>
 
+#include "gemm_tc.h"
 #include "gr00t.h"
 #include "kernels.h"
 
@@ -66,8 +69,13 @@ struct gr00t_ctx {
 
   // options
   int opt_graph = 1, opt_gemm = 0, opt_attn = 0;
-  long long wait_limit = 1 << 22;
+  long long wait_limit = 1 << 20;
   int launches = 0;  // kernel launches of the last enqueued step
+
+  // tensor-core GEMM: SM count and a cache of TMA descriptors
+  int sm_count = 148;
+  std::map<std::tuple<const void*, long long, long long, long long, int>, CUtensorMap> tmaps;
+  int opt_pdl = 1;
 
   // per-kernel timing: event pairs around every launch of one kernel class
   int time_class = 0;
@@ -351,10 +359,28 @@ void tmark(gr00t_ctx* c, int cls) {
     cudaEventRecord(ev, c->stream);
 }
 
+const CUtensorMap* tmap(gr00t_ctx* c, const void* ptr, long long rows, long long cols, long long ld,
+                        int box_rows) {
+  auto key = std::make_tuple(ptr, rows, cols, ld, box_rows);
+  auto it = c->tmaps.find(key);
+  if (it != c->tmaps.end()) return &it->second;
+  CUtensorMap m;
+  if (tc_make_map(&m, ptr, rows, cols, ld, box_rows) != cudaSuccess) return nullptr;
+  return &c->tmaps.emplace(key, m).first->second;
+}
+
 int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
   ++c->launches;
   tmark(c, cls);
-  CK(c, gemm_simt(c->dt, a, c->stream));
+  if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
+    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count);
+    const CUtensorMap* tw = tmap(c, a.W, a.N, a.K, a.ldw, 128);
+    const CUtensorMap* tx = tmap(c, a.A, a.M, a.K, a.lda, p.BN);
+    if (!tw || !tx) return set_err(c, GR00T_ECUDA, "TMA descriptor encode failed (alignment?)");
+    CK(c, gemm_tc(*tw, *tx, a, p, c->err_flag, c->wait_limit, c->stream, c->opt_pdl != 0));
+  } else {
+    CK(c, gemm_simt(c->dt, a, c->stream));
+  }
   tmark(c, cls);
   return GR00T_OK;
 }
@@ -633,6 +659,7 @@ extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, voi
 
   gr00t_ctx* c = new gr00t_ctx();
   c->g = *g;
+  c->sm_count = prop.multiProcessorCount;
   c->dt = g->dtype == GR00T_DTYPE_BF16 ? DT_BF16 : DT_F32;
   c->esz = c->dt == DT_BF16 ? 2 : 4;
   c->D = g->hidden; c->L = g->layers; c->Hq = g->q_heads; c->Hkv = g->kv_heads; c->Dh = g->head_dim;

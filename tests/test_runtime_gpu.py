@@ -110,3 +110,29 @@ def test_batch_mismatch_between_bind_and_schedule():
     with pytest.raises(fmv.Gr00tError) as ei:
         loop.denoise(torch.from_numpy(c["x_noise"]).cuda())
     assert ei.value.status == -4
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "small_dit"])
+def test_tensor_core_gemm_matches_cuda_core_gemm(name):
+    """Same inputs through both GEMM paths: only the fp32 summation order differs."""
+    fmv = _fmv()
+    c = synth.make_case(name)
+    loop, held = fmv.from_case(c)
+    x0 = torch.from_numpy(c["x_noise"]).cuda()
+    vs = []
+    for path in (0, 1):
+        loop.set_option(fmv.OPT_GEMM_PATH, path)
+        vs.append(loop.denoise_step(0, x0).cpu().numpy())
+    e_inf, e_rel = oracle.error_metrics(vs[0], vs[1])
+    assert e_rel < 5e-3, e_rel
+    assert loop.info(fmv.INFO_ERROR_FLAG) == 0
+
+
+@pytest.mark.parametrize("name", ["pi05", "pi05_b32"])
+def test_no_bounded_wait_timed_out(name):
+    fmv = _fmv()
+    c = synth.make_case(name)
+    loop, held = fmv.from_case(c)
+    x0 = torch.from_numpy(c["x_noise"]).cuda()
+    loop.denoise(x0)
+    assert loop.info(fmv.INFO_ERROR_FLAG) == 0
