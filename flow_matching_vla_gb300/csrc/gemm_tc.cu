@@ -175,13 +175,18 @@ __global__ void __launch_bounds__(128, 1)
       const int r0 = rank * R + 2 * p;
       const int m = m0 + j, n = n0 + r0;
       if (m >= M || n >= N) continue;
+      // issue the S partial loads together, then sum them in rank order
+      float2 v[16];
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+        if (s < S) v[s] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(red, s) + j * BM + r0);
       float a0 = 0.f, a1 = 0.f;
-      for (int s = 0; s < S; ++s) {
-        const float* peer = cluster.map_shared_rank(red, s);
-        const float2 v = *reinterpret_cast<const float2*>(peer + j * BM + r0);
-        a0 += v.x;
-        a1 += v.y;
-      }
+#pragma unroll
+      for (int s = 0; s < 16; ++s)
+        if (s < S) {
+          a0 += v[s].x;
+          a1 += v[s].y;
+        }
       epi_pair<bf16>(e, m, n, a0, a1);
     }
   }

@@ -101,6 +101,20 @@ struct AttnArgs {
 };
 cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s);
 
+// Tensor-core attention of the expert family (one KV head, heads folded into rows).
+struct AttnFoldArgs {
+  const void* qkv = nullptr;   // bf16 [B*H][ldq]: q heads at 0, suffix k at k_off, v at v_off
+  int ldq = 0, k_off = 0, v_off = 0;
+  int B = 0, H = 0, Hq = 0, Dh = 0, P = 0;
+  const void* const* table = nullptr;  // prefix K/V [B][P][Dh] at table[k_slot], table[v_slot]
+  int k_slot = 0, v_slot = 0;
+  void* out = nullptr;         // bf16 [B*H][ldo], head h at column h*Dh
+  int ldo = 0;
+};
+bool attn_fold_supported(int Dh);
+int attn_fold_splits(const AttnFoldArgs& a, int sm_count);
+cudaError_t attention_fold(const AttnFoldArgs& a, int S, cudaStream_t s, bool pdl);
+
 // ---- schedule / bind / create helpers --------------------------------------------
 // temb[k*B + b][E] (activation dtype) of tau_k; dts[k] = tau_{k+1} - tau_k.
 cudaError_t time_embed(DType dt, int T, int B, int E, int direction, void* temb, float* dts,

@@ -432,14 +432,23 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       g.epi.tok_rope = tok;
       RC(gemm(c, g, GR00T_KCLASS_QKV_GEMM));
 
-      AttnArgs at;
-      at.q = c->qkv; at.ldq = nq; at.B = B; at.Tq = tok; at.Hq = c->Hq; at.Hkv = 1; at.Dh = c->Dh;
-      at.table = c->table; at.k_slot = 2 * l; at.v_slot = 2 * l + 1; at.P = P;
-      at.ks = ptr_at(c->qkv, (long long)c->qd, es); at.vs = ptr_at(c->qkv, (long long)c->qd + c->Dh, es);
-      at.lds = nq; at.S = tok; at.out = c->att; at.ldo = c->qd;
       ++c->launches;
       tmark(c, GR00T_KCLASS_ATTENTION);
-      CK(c, attention_simt(c->dt, at, s));
+      if (c->dt == DT_BF16 && c->opt_attn == 0 && attn_fold_supported(c->Dh)) {
+        AttnFoldArgs af;
+        af.qkv = c->qkv; af.ldq = nq; af.k_off = c->qd; af.v_off = c->qd + c->Dh;
+        af.B = B; af.H = H; af.Hq = c->Hq; af.Dh = c->Dh; af.P = P;
+        af.table = c->table; af.k_slot = 2 * l; af.v_slot = 2 * l + 1;
+        af.out = c->att; af.ldo = c->qd;
+        CK(c, attention_fold(af, attn_fold_splits(af, c->sm_count), s, c->opt_pdl != 0));
+      } else {
+        AttnArgs at;
+        at.q = c->qkv; at.ldq = nq; at.B = B; at.Tq = tok; at.Hq = c->Hq; at.Hkv = 1; at.Dh = c->Dh;
+        at.table = c->table; at.k_slot = 2 * l; at.v_slot = 2 * l + 1; at.P = P;
+        at.ks = ptr_at(c->qkv, (long long)c->qd, es); at.vs = ptr_at(c->qkv, (long long)c->qd + c->Dh, es);
+        at.lds = nq; at.S = tok; at.out = c->att; at.ldo = c->qd;
+        CK(c, attention_simt(c->dt, at, s));
+      }
       tmark(c, GR00T_KCLASS_ATTENTION);
 
       GemmArgs go;
