@@ -12,6 +12,8 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
+#include "tc_ptx.cuh"
 
 namespace g3 {
 
@@ -21,6 +23,8 @@ constexpr int kMaxPerLane = 8;  // head_dim <= 256
 
 template <typename T>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
   const long long total = (long long)a.B * a.Tq * a.Hq;
@@ -87,16 +91,13 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
 
 }  // namespace
 
-cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s) {
+cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s, bool pdl) {
   const long long total = (long long)a.B * a.Tq * a.Hq;
   if (total <= 0) return cudaSuccess;
   if (a.Dh > 32 * kMaxPerLane || a.Hkv <= 0 || a.Hq % a.Hkv) return cudaErrorInvalidValue;
   const unsigned blocks = (unsigned)((total + 3) / 4);
-  if (dt == DT_F32)
-    attn_simt_kernel<float><<<blocks, 128, 0, s>>>(a);
-  else
-    attn_simt_kernel<bf16><<<blocks, 128, 0, s>>>(a);
-  return cudaGetLastError();
+  if (dt == DT_F32) return launch_k(attn_simt_kernel<float>, blocks, 128, 0, s, pdl, a);
+  return launch_k(attn_simt_kernel<bf16>, blocks, 128, 0, s, pdl, a);
 }
 
 }  // namespace g3

@@ -11,9 +11,10 @@
 // CTAs of one row tile form a thread-block cluster.  Each CTA runs an online
 // softmax over its key range with mma.sync m16n8k16 (bf16 in, fp32
 // accumulate): 4 warps x 16 rows, 64-key sub-tiles staged in XOR-swizzled
-// shared memory by cp.async.  The S partial (max, sum, O) triples are then
-// combined through distributed shared memory, in split order (deterministic),
-// each CTA finishing 64/S rows.
+// shared memory by cp.async (the bound prefix rows before the dependency
+// wait).  The S partial (max, sum, O) triples go to an L2-resident workspace;
+// after one cluster barrier each CTA combines 64/S rows in split order
+// (deterministic).  With S = 1 the CTA normalises and stores directly.
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -69,10 +70,8 @@ __device__ __forceinline__ int swz(int r, int c) {
 template <int DH>
 struct AttnSmem {
   static constexpr int TILE = ROWS * DH * 2;   // Q, K or V tile (64 rows)
-  static constexpr int OPART = ROWS * DH * 4;  // fp32 partial O
-  // tiles | sM, sL (read by peers) | local combine scratch (weights, sums, 1/sum)
-  static constexpr int TOTAL = 3 * TILE + 2 * ROWS * 4 + 3 * ROWS * 4 + 16;
-  static_assert(OPART + 2 * ROWS * 4 <= 3 * TILE + 2 * ROWS * 4, "partial fits");
+  // Q, K, V tiles | combine scratch (weights, sums, 1/sum)
+  static constexpr int TOTAL = 3 * TILE + 3 * ROWS * 4 + 16;
 };
 
 template <int DH>
@@ -82,9 +81,9 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
   bf16* sQ = reinterpret_cast<bf16*>(smem);
   bf16* sK = reinterpret_cast<bf16*>(smem + L::TILE);
   bf16* sV = reinterpret_cast<bf16*>(smem + 2 * L::TILE);
-  float* sO = reinterpret_cast<float*>(smem);                       // after the key loop
-  float* sM = reinterpret_cast<float*>(smem + 3 * L::TILE);
-  float* sL = sM + ROWS;
+  float* sW = reinterpret_cast<float*>(smem + 3 * L::TILE);   // combine scratch [S][RP]
+  float* sLs = sW + ROWS;
+  float* sInv = sLs + ROWS;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int S = (int)cluster.num_blocks();
@@ -100,38 +99,22 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
   constexpr int CH = DH / 8;  // 16-byte chunks per row
 
   ptx::pdl_launch_dependents();
-  ptx::pdl_wait();
-
+  // The bound prefix K/V and the pointer table are never written inside the
+  // loop: stage the first sub-tile's prefix rows before waiting on the kernel
+  // that produces this step's Q and suffix K/V.
   const bf16* Kp = reinterpret_cast<const bf16*>(a.table[a.k_slot]);
   const bf16* Vp = reinterpret_cast<const bf16*>(a.table[a.v_slot]);
   const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
-
-  // Q tile: folded row r = t * Hq + h -> qkv[(b*H + t) * ldq + h * DH]
-  for (int i = tid; i < ROWS * CH; i += 128) {
-    const int r = i / CH, c = i % CH;
-    const int gr = r0 + r;
-    const bool ok = gr < nrows;
-    const int t = ok ? gr / a.Hq : 0, h = ok ? gr % a.Hq : 0;
-    const bf16* src = qkv + ((long long)b * a.H + t) * a.ldq + h * DH + c * 8;
-    cp_async16(sQ + swz<DH>(r, c), src, ok);
-  }
-  cp_async_commit();
-
-  const float sl2 = rsqrtf((float)DH) * 1.4426950408889634f;  // 1/sqrt(d) * log2(e)
-  float o[DH / 8][4];
-#pragma unroll
-  for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  const int g = lane >> 2, tq = lane & 3;
-
-  for (int kt = k_begin; kt < k_end; kt += KT) {
-    __syncthreads();  // previous sub-tile fully consumed
+  // phase 0: prefix rows only, 1: suffix and out-of-range rows only, 2: all rows
+  auto issue_kv = [&](int kt, int phase) {
     for (int i = tid; i < KT * CH; i += 128) {
       const int r = i / CH, c = i % CH;
       const int s = kt + r;
+      const bool pre = s < a.P && s < k_end;
+      if ((phase == 0 && !pre) || (phase == 1 && pre)) continue;
       const bool ok = s < k_end;
       const bf16 *ks, *vs;
-      if (s < a.P) {
+      if (pre) {
         ks = Kp + ((long long)b * a.P + s) * DH;
         vs = Vp + ((long long)b * a.P + s) * DH;
       } else {
@@ -142,10 +125,37 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
       cp_async16(sK + swz<DH>(r, c), ok ? (const void*)(ks + c * 8) : (const void*)qkv, ok);
       cp_async16(sV + swz<DH>(r, c), ok ? (const void*)(vs + c * 8) : (const void*)qkv, ok);
     }
-    cp_async_commit();
+  };
+  if (k_begin < k_end) issue_kv(k_begin, 0);
+  ptx::pdl_wait();
+
+  // Q tile: folded row r = t * Hq + h -> qkv[(b*H + t) * ldq + h * DH]
+  for (int i = tid; i < ROWS * CH; i += 128) {
+    const int r = i / CH, c = i % CH;
+    const int gr = r0 + r;
+    const bool ok = gr < nrows;
+    const int t = ok ? gr / a.Hq : 0, h = ok ? gr % a.Hq : 0;
+    const bf16* src = qkv + ((long long)b * a.H + t) * a.ldq + h * DH + c * 8;
+    cp_async16(sQ + swz<DH>(r, c), src, ok);
+  }
+  if (k_begin < k_end) issue_kv(k_begin, 1);
+  cp_async_commit();
+
+  const float sl2 = rsqrtf((float)DH) * 1.4426950408889634f;  // 1/sqrt(d) * log2(e)
+  float o[DH / 8][4];
+#pragma unroll
+  for (int i = 0; i < DH / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  const int g = lane >> 2, tq = lane & 3;
+
+  for (int kt = k_begin; kt < k_end; kt += KT) {
+    if (kt != k_begin) {
+      __syncthreads();  // previous sub-tile fully consumed
+      issue_kv(kt, 2);
+      cp_async_commit();
+    }
     cp_async_wait_all();
     __syncthreads();
-
     // S = Q K^T for this warp's 16 rows x 64 keys
     float sacc[8][4];
 #pragma unroll
@@ -232,75 +242,106 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
   }
-  __syncthreads();  // tiles no longer read: reuse them for the partial
-  {
-    const int ra = warp * 16 + g, rb = ra + 8;
+  const int ra = warp * 16 + g, rb = ra + 8;
+  bf16* out = reinterpret_cast<bf16*>(a.out);
+
+  if (S == 1) {  // whole key range in this CTA: normalise and store
+    const float inva = lrow[0] > 0.f ? 1.f / lrow[0] : 0.f;
+    const float invb = lrow[1] > 0.f ? 1.f / lrow[1] : 0.f;
 #pragma unroll
-    for (int i = 0; i < DH / 8; ++i) {
-      const int col = i * 8 + tq * 2;
-      *reinterpret_cast<float2*>(sO + ra * DH + col) = make_float2(o[i][0], o[i][1]);
-      *reinterpret_cast<float2*>(sO + rb * DH + col) = make_float2(o[i][2], o[i][3]);
+    for (int hr = 0; hr < 2; ++hr) {
+      const int gr = r0 + (hr ? rb : ra);
+      if (gr >= nrows) continue;
+      const int t = gr / a.Hq, h = gr % a.Hq;
+      bf16* orow = out + ((long long)b * a.H + t) * a.ldo + h * DH;
+      const float inv = hr ? invb : inva;
+#pragma unroll
+      for (int i = 0; i < DH / 8; ++i)
+        *reinterpret_cast<__nv_bfloat162*>(orow + i * 8 + tq * 2) =
+            __floats2bfloat162_rn(o[i][2 * hr] * inv, o[i][2 * hr + 1] * inv);
     }
-    if (tq == 0) {
-      sM[ra] = mrow[0];
-      sM[rb] = mrow[1];
-      sL[ra] = lrow[0];
-      sL[rb] = lrow[1];
-    }
+    return;
+  }
+
+  // split keys: park (O, max, sum) in the L2-resident workspace, one cluster
+  // barrier, then this CTA combines rows [split*RP, split*RP + RP) in split order
+  const long long tile = (long long)b * gridDim.x + blockIdx.x;
+  constexpr int PART = ROWS * DH + 2 * ROWS;   // floats per split partial
+  float* my = a.ws + (tile * S + split) * PART;
+#pragma unroll
+  for (int i = 0; i < DH / 8; ++i) {
+    const int col = i * 8 + tq * 2;
+    *reinterpret_cast<float2*>(my + ra * DH + col) = make_float2(o[i][0], o[i][1]);
+    *reinterpret_cast<float2*>(my + rb * DH + col) = make_float2(o[i][2], o[i][3]);
+  }
+  if (tq == 0) {
+    my[ROWS * DH + ra] = mrow[0];
+    my[ROWS * DH + rb] = mrow[1];
+    my[ROWS * DH + ROWS + ra] = lrow[0];
+    my[ROWS * DH + ROWS + rb] = lrow[1];
   }
   cluster.sync();
 
-  // combine: this CTA finishes rows [split*RP, split*RP + RP) of the tile.
-  // (1) per row and split, the split's running max and sum -> weights
+  const float* base = a.ws + tile * S * PART;
   const int RP = ROWS / S;
-  float* sW = sL + ROWS;       // [S][RP]: split maxima, then weights exp2(m_s - max)  (local)
-  float* sLs = sW + ROWS;      // [S][RP]: split sums                                 (local)
-  float* sInv = sLs + ROWS;    // [RP]: 1 / sum_s w_s l_s                             (local)
-  if (tid < S * RP) {
-    const int s = tid / RP, rr = split * RP + tid % RP;
-    sW[tid] = cluster.map_shared_rank(sM, s)[rr];
-    sLs[tid] = cluster.map_shared_rank(sL, s)[rr];
+  if (tid < S * RP) {  // (1) per row and split: max and sum -> weights
+    const int sp = tid / RP, rr = split * RP + tid % RP;
+    sW[tid] = base[sp * PART + ROWS * DH + rr];
+    sLs[tid] = base[sp * PART + ROWS * DH + ROWS + rr];
   }
   __syncthreads();
   if (tid < RP) {
     float mx = -INFINITY;
-    for (int s = 0; s < S; ++s) mx = fmaxf(mx, sW[s * RP + tid]);
+    for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, sW[sp * RP + tid]);
     float lsum = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float ms = sW[s * RP + tid];
+    for (int sp = 0; sp < S; ++sp) {
+      const float ms = sW[sp * RP + tid];
       const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
-      lsum += w * sLs[s * RP + tid];
-      sW[s * RP + tid] = w;
+      lsum += w * sLs[sp * RP + tid];
+      sW[sp * RP + tid] = w;
     }
     sInv[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
   }
   __syncthreads();
-  // (2) weighted sum of the S partial O rows, loads issued together, summed in split order
-  bf16* out = reinterpret_cast<bf16*>(a.out);
-  for (int i = tid; i < RP * (DH / 2); i += 128) {
-    const int lr = i / (DH / 2);
-    const int rr = split * RP + lr;
-    const int col = (i % (DH / 2)) * 2;
-    const int gr = r0 + rr;
-    if (gr >= nrows) continue;
-    float2 v[16];
+  // (2) weighted sum of the S partial rows; U items per thread with their loads in flight together
+  constexpr int U = 4;
+  const int items = RP * (DH / 2);
+#pragma unroll 1
+  for (int it0 = tid; it0 < items; it0 += 128 * U) {
+    float2 acc[U];
+    int lr[U], col[U];
+    bool ok[U];
 #pragma unroll
-    for (int s = 0; s < 16; ++s)
-      if (s < S) v[s] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(sO, s) + rr * DH + col);
-    float acc0 = 0.f, acc1 = 0.f;
+    for (int u = 0; u < U; ++u) {
+      const int it = it0 + u * 128;
+      lr[u] = it / (DH / 2);
+      col[u] = (it % (DH / 2)) * 2;
+      ok[u] = it < items && r0 + split * RP + lr[u] < nrows;
+      acc[u] = make_float2(0.f, 0.f);
+    }
 #pragma unroll
-    for (int s = 0; s < 16; ++s)
-      if (s < S) {
-        const float w = sW[s * RP + lr];
-        acc0 += w * v[s].x;
-        acc1 += w * v[s].y;
+    for (int sp = 0; sp < 16; ++sp) {
+      if (sp < S) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (ok[u]) {
+            const float w = sW[sp * RP + lr[u]];
+            const float2 v = *reinterpret_cast<const float2*>(base + sp * PART + (split * RP + lr[u]) * DH + col[u]);
+            acc[u].x += w * v.x;
+            acc[u].y += w * v.y;
+          }
       }
-    const float inv = sInv[lr];
-    const int t = gr / a.Hq, h = gr % a.Hq;
-    *reinterpret_cast<__nv_bfloat162*>(out + ((long long)b * a.H + t) * a.ldo + h * DH + col) =
-        __floats2bfloat162_rn(acc0 * inv, acc1 * inv);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (ok[u]) {
+        const int gr = r0 + split * RP + lr[u];
+        const int t = gr / a.Hq, h = gr % a.Hq;
+        const float inv = sInv[lr[u]];
+        *reinterpret_cast<__nv_bfloat162*>(out + ((long long)b * a.H + t) * a.ldo + h * DH + col[u]) =
+            __floats2bfloat162_rn(acc[u].x * inv, acc[u].y * inv);
+      }
   }
-  cluster.sync();
 }
 
 template <int DH>
@@ -334,6 +375,12 @@ cudaError_t launch_fold(const AttnFoldArgs& a, int S, cudaStream_t s, bool pdl) 
 
 }  // namespace
 
+long long attn_fold_workspace_floats(const AttnFoldArgs& a, int S) {
+  if (S == 1) return 0;
+  const long long tiles = (long long)(a.Hq * a.H + ROWS - 1) / ROWS * a.B;
+  return tiles * S * (ROWS * (long long)a.Dh + 2 * ROWS);
+}
+
 int attn_fold_splits(const AttnFoldArgs& a, int sm_count) {
   const int tiles = (a.Hq * a.H + ROWS - 1) / ROWS * a.B;
   const int nkeys = a.P + a.H;
@@ -347,6 +394,7 @@ bool attn_fold_supported(int Dh) { return Dh == 64 || Dh == 128 || Dh == 256; }
 cudaError_t attention_fold(const AttnFoldArgs& a, int S, cudaStream_t s, bool pdl) {
   if (a.B <= 0 || a.Hq * a.H <= 0) return cudaSuccess;
   if (S < 1 || S > 16 || (S & (S - 1))) return cudaErrorInvalidValue;
+  if (attn_fold_workspace_floats(a, S) > a.ws_floats) return cudaErrorInvalidValue;
   switch (a.Dh) {
     case 64: return launch_fold<64>(a, S, s, pdl);
     case 128: return launch_fold<128>(a, S, s, pdl);

@@ -85,4 +85,37 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, f
   }
 }
 
+// Operands of an epilogue that do not depend on the accumulator (residual row
+// and gate), loaded ahead so their latency overlaps the partial-sum loads.
+struct EpiPre {
+  float2 h;
+  float2 g;
+};
+
+template <typename T>
+__device__ __forceinline__ EpiPre epi_prefetch(const Epi& e, int m, int n) {
+  EpiPre p;
+  p.h = make_float2(0.f, 0.f);
+  p.g = make_float2(1.f, 1.f);
+  if (e.kind == EPI_RESID_GATED || e.kind == EPI_RESID) {
+    p.h = *reinterpret_cast<const float2*>(e.resid + (long long)m * e.ldr + n);
+    if (e.kind == EPI_RESID_GATED) {
+      const T* g = (const T*)e.gate + (long long)(m / e.tok) * e.gate_bstride + n;
+      p.g = make_float2(to_f(g[0]), to_f(g[1]));
+    }
+  }
+  return p;
+}
+
+template <typename T>
+__device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, float a1, const EpiPre& p) {
+  if (e.kind == EPI_RESID_GATED || e.kind == EPI_RESID) {
+    *reinterpret_cast<float2*>(e.resid + (long long)m * e.ldr + n) =
+        make_float2(p.h.x + p.g.x * a0, p.h.y + p.g.y * a1);
+    return;
+  }
+  epi_pair<T>(e, m, n, a0, a1);
+}
+
+
 }  // namespace g3

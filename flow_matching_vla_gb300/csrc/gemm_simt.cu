@@ -5,6 +5,8 @@
 // the cross-check of the tensor-core path.  64x64 output tile, BK = 16,
 // 256 threads, 4x4 outputs per thread (two epilogue pairs per row).
 #include "epilogue.cuh"
+#include "launch.cuh"
+#include "tc_ptx.cuh"
 
 namespace g3 {
 
@@ -16,6 +18,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ A, int lda,
                                                         const T* __restrict__ W, int ldw, int M,
                                                         int N, int K, Epi e) {
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
   __shared__ float As[BK][BM + 4];
   __shared__ float Ws[BK][BN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -63,17 +67,15 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ A,
 
 }  // namespace
 
-cudaError_t gemm_simt(DType dt, const GemmArgs& a, cudaStream_t s) {
+cudaError_t gemm_simt(DType dt, const GemmArgs& a, cudaStream_t s, bool pdl) {
   if (a.M <= 0 || a.N <= 0) return cudaSuccess;
   if (a.N & 1) return cudaErrorInvalidValue;
   dim3 grid((a.N + BN - 1) / BN, (a.M + BM - 1) / BM);
   if (dt == DT_F32)
-    gemm_simt_kernel<float><<<grid, 256, 0, s>>>((const float*)a.A, a.lda, (const float*)a.W, a.ldw,
-                                                 a.M, a.N, a.K, a.epi);
-  else
-    gemm_simt_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)a.A, a.lda, (const bf16*)a.W, a.ldw,
-                                                a.M, a.N, a.K, a.epi);
-  return cudaGetLastError();
+    return launch_k(gemm_simt_kernel<float>, grid, 256, 0, s, pdl, (const float*)a.A, a.lda,
+                    (const float*)a.W, a.ldw, a.M, a.N, a.K, a.epi);
+  return launch_k(gemm_simt_kernel<bf16>, grid, 256, 0, s, pdl, (const bf16*)a.A, a.lda, (const bf16*)a.W,
+                  a.ldw, a.M, a.N, a.K, a.epi);
 }
 
 }  // namespace g3

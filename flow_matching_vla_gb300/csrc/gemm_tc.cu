@@ -9,10 +9,11 @@
 //    (L2 evict-first) and BNx64 activation tiles (L2 evict-last) through a
 //    STAGES-deep mbarrier ring; one thread issues loads, one issues MMAs.
 //  * Split-K across a thread-block cluster (1 x 1 x S, S <= 16): every CTA of
-//    the cluster accumulates a K slice, parks its fp32 partial in its own
-//    shared memory, and after a cluster barrier each CTA reduces 128/S rows
-//    over the S partials through distributed shared memory, in rank order
-//    (deterministic), and applies the epilogue to them.
+//    the cluster accumulates a K slice and parks its fp32 partial in an
+//    L2-resident workspace; after one cluster barrier each CTA sums 128/S rows
+//    over the S partials in rank order (deterministic) and applies the
+//    epilogue to them.  Without a split the epilogue runs straight from the
+//    TMEM registers (adjacent lanes swap one value to form output pairs).
 //  * Programmatic dependent launch: weight tiles (which no earlier kernel
 //    writes) are prefetched before griddepcontrol.wait; activations after.
 //  * Every mbarrier wait is bounded; on timeout the CTA records an error
@@ -39,16 +40,57 @@ struct TcSmem {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int PIPE = STAGES * STAGE_BYTES;
-  static constexpr int RED = BN * BM * 4;  // fp32 partial, reuses the pipeline buffers
-  static_assert(RED <= PIPE, "partial must fit in the pipeline buffers");
   static constexpr int BAR = (2 * STAGES + 1) * 8 + 16;
   static constexpr int TOTAL = PIPE + BAR + 1024;  // + alignment slack
 };
 
+// Rank ``rank`` of an S-way split sums rows [rank*128/S, (rank+1)*128/S) of the
+// tile over the S partials (layout [split][token][row]) in split order and
+// applies the epilogue.  U items per thread keep U*S loads in flight.
+template <int U>
+__device__ __forceinline__ void reduce_rows(const Epi& e, const float* __restrict__ base, int S, int rank,
+                                            int m0, int n0, int M, int N, int BN) {
+  const int R = BM / S, pairs = R / 2, items = pairs * BN;
+#pragma unroll 1
+  for (int it0 = threadIdx.x; it0 < items; it0 += 128 * U) {
+    int mm[U], nn[U], jj[U], rr[U];
+    bool ok[U];
+    EpiPre pre[U];
+    float2 acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int it = it0 + u * 128;
+      const int p = it % pairs, j = it / pairs;
+      rr[u] = rank * R + 2 * p;
+      jj[u] = j;
+      mm[u] = m0 + j;
+      nn[u] = n0 + rr[u];
+      ok[u] = it < items && mm[u] < M && nn[u] < N;
+      if (ok[u]) pre[u] = epi_prefetch<bf16>(e, mm[u], nn[u]);
+      acc[u] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int s = 0; s < 16 / U; ++s) {
+      if (s < S) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (ok[u]) {
+            const float2 v = *reinterpret_cast<const float2*>(base + ((long long)s * BN + jj[u]) * BM + rr[u]);
+            acc[u].x += v.x;
+            acc[u].y += v.y;
+          }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (ok[u]) epi_pair<bf16>(e, mm[u], nn[u], acc[u].x, acc[u].y, pre[u]);
+  }
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(128, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
-                   int N, int kb_per_split, Epi e, int* err, long long wait_limit) {
+                   int N, int kb_per_split, Epi e, float* __restrict__ ws, int* err, long long wait_limit) {
   using L = TcSmem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -59,11 +101,10 @@ __global__ void __launch_bounds__(128, 1)
   uint64_t* done = empty + STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  float* red = reinterpret_cast<float*>(smem);
 
   cg::cluster_group cluster = cg::this_cluster();
-  const int S = (int)cluster.num_blocks();
-  const int rank = (int)cluster.block_rank();
+  const int S = (int)gridDim.z;                 // split-K factor (the cluster size when reducing here)
+  const int rank = (int)blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
   const int kb0 = blockIdx.z * kb_per_split;
@@ -146,51 +187,83 @@ __global__ void __launch_bounds__(128, 1)
   // waits for the previous kernel before touching activation memory
   if (threadIdx.x != 0) ptx::pdl_wait();
 
-  // accumulator -> own shared memory, transposed to [token][row] (conflict-free)
   if (!ptx::mbar_wait(done, 0, wait_limit)) {
     atomicExch(abort_flag, 1);
     atomicExch(err, 1);
   }
   __syncthreads();
   ptx::tc_fence_after();
-  const int row = warp * 32 + lane;
-  if (!*abort_flag) {
+  const bool aborted = *abort_flag != 0;
+  const int row = warp * 32 + lane;         // TMEM lane = weight row n0 + row
+  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+
+  if (e.kind == EPI_PARTIAL) {
+    // split partial straight to the consumer's buffer: out[(split * M + m) * ldo + n]
+    float* part = reinterpret_cast<float*>(e.out) + (long long)blockIdx.z * M * e.ldo;
+    const int n = n0 + row;
+    if (!aborted) {  // CTA-uniform: every lane takes part in tcgen05.ld
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      float v[16];
-      ptx::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0, v);
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+        if (n < N) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) red[(c0 + j) * BM + row] = v[j];
+          for (int j = 0; j < 32; ++j)
+            if (m0 + c0 + j < M) part[(long long)(m0 + c0 + j) * e.ldo + n] = v[j];
+        }
+      }
+    }
+  } else if (S == 1) {
+    // direct epilogue from registers: lanes (2i, 2i+1) hold rows (n, n+1); swap
+    // one value per column pair so each lane finishes one (n, n+1) output pair
+    const int n_even = n0 + (row & ~1);
+    const bool odd = lane & 1;
+    if (!aborted) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float send = odd ? v[j] : v[j + 1];
+          const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+          const int m = m0 + c0 + j + (odd ? 1 : 0);
+          const float a0 = odd ? recv : v[j];
+          const float a1 = odd ? v[j + 1] : recv;
+          if (m < M && n_even < N) epi_pair<bf16>(e, m, n_even, a0, a1);
+        }
+      }
+    }
+  } else {
+    // split-K: park the fp32 partial in the L2-resident workspace, one cluster
+    // barrier (release/acquire orders the global writes), then each rank sums
+    // its 128/S rows over the S partials in rank order.
+    const long long tile = (long long)blockIdx.y * gridDim.x + blockIdx.x;
+    float* my = ws + ((tile * S + (long long)blockIdx.z) * BN) * BM;
+    if (!aborted) {
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) my[(c0 + j) * BM + row] = v[j];
+      }
+    }
+    cluster.sync();
+    const float* base = ws + (tile * S) * BN * BM;
+    if (!aborted) {
+      if (S <= 2)
+        reduce_rows<8>(e, base, S, rank, m0, n0, M, N, BN);
+      else if (S <= 4)
+        reduce_rows<4>(e, base, S, rank, m0, n0, M, N, BN);
+      else if (S <= 8)
+        reduce_rows<2>(e, base, S, rank, m0, n0, M, N, BN);
+      else
+        reduce_rows<1>(e, base, S, rank, m0, n0, M, N, BN);
     }
   }
   ptx::tc_fence_before();
-  cluster.sync();
-
-  // rank r reduces rows [r*R, r*R + R) over the S partials, in rank order
-  const bool aborted = *abort_flag != 0;
-  const int R = BM / S, pairs = R / 2;
-  if (!aborted) {
-    for (int it = threadIdx.x; it < pairs * BN; it += blockDim.x) {
-      const int p = it % pairs, j = it / pairs;
-      const int r0 = rank * R + 2 * p;
-      const int m = m0 + j, n = n0 + r0;
-      if (m >= M || n >= N) continue;
-      // issue the S partial loads together, then sum them in rank order
-      float2 v[16];
-#pragma unroll
-      for (int s = 0; s < 16; ++s)
-        if (s < S) v[s] = *reinterpret_cast<const float2*>(cluster.map_shared_rank(red, s) + j * BM + r0);
-      float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-      for (int s = 0; s < 16; ++s)
-        if (s < S) {
-          a0 += v[s].x;
-          a1 += v[s].y;
-        }
-      epi_pair<bf16>(e, m, n, a0, a1);
-    }
-  }
-  cluster.sync();  // peers finished reading this CTA's partial
+  __syncthreads();
   if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, BN);
@@ -200,8 +273,8 @@ __global__ void __launch_bounds__(128, 1)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 template <int BN, int STAGES>
-cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int S, int* err,
-                   long long lim, cudaStream_t s, bool pdl) {
+cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int S, float* ws,
+                   int* err, long long lim, cudaStream_t s, bool pdl) {
   using L = TcSmem<BN, STAGES>;
   auto kern = gemm_tc_kernel<BN, STAGES>;
   static bool configured = false;
@@ -221,13 +294,13 @@ cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs&
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = S;
+  attr[0].val.clusterDim.z = a.epi.kind == EPI_PARTIAL ? 1 : S;   // partials need no cluster
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const int KB = a.K / BK;
-  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, err, lim);
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim);
 }
 
 }  // namespace
@@ -251,25 +324,33 @@ cudaError_t tc_make_map(CUtensorMap* m, const void* ptr, long long rows, long lo
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-TcPlan tc_plan(int M, int N, int K, int sm_count) {
+TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split) {
   TcPlan p;
   p.BN = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
   const int KB = K / BK;
   const long long tiles = (long long)((N + BM - 1) / BM) * ((M + p.BN - 1) / p.BN);
   p.S = 1;
-  while (p.S < 16 && KB % (2 * p.S) == 0 && tiles * 2 * p.S <= sm_count + sm_count / 16) p.S *= 2;
+  while (p.S < 16 && 2 * p.S <= max_split && KB % (2 * p.S) == 0 && tiles * 2 * p.S <= sm_count + sm_count / 16)
+    p.S *= 2;
   return p;
 }
 
 bool tc_supported(int M, int N, int K) { return M > 0 && N > 0 && K > 0 && K % BK == 0 && N % 2 == 0; }
 
+long long tc_workspace_floats(const TcPlan& p, int M, int N) {
+  if (p.S == 1) return 0;
+  const long long tiles = (long long)((N + BM - 1) / BM) * ((M + p.BN - 1) / p.BN);
+  return tiles * p.S * p.BN * BM;
+}
+
 cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
-                    int* err, long long wait_limit, cudaStream_t s, bool pdl) {
+                    float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl) {
   if (!tc_supported(a.M, a.N, a.K) || (a.K / BK) % p.S) return cudaErrorInvalidValue;
+  if (a.epi.kind != EPI_PARTIAL && tc_workspace_floats(p, a.M, a.N) > ws_floats) return cudaErrorInvalidValue;
   switch (p.BN) {
-    case 64: return launch<64, 4>(tw, tx, a, p.S, err, wait_limit, s, pdl);
-    case 128: return launch<128, 4>(tw, tx, a, p.S, err, wait_limit, s, pdl);
-    case 256: return launch<256, 4>(tw, tx, a, p.S, err, wait_limit, s, pdl);
+    case 64: return launch<64, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
+    case 128: return launch<128, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
+    case 256: return launch<256, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

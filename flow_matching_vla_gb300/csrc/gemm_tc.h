@@ -18,9 +18,13 @@ struct TcPlan {
 cudaError_t tc_make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld,
                         int box_rows);
 bool tc_supported(int M, int N, int K);
-TcPlan tc_plan(int M, int N, int K, int sm_count);
+// Split-K factor: the largest power of two <= max_split that divides the
+// K blocks and keeps tiles * S within 17/16 of the SM count.
+TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split);
+// Split-K partials the plan needs (fp32 elements of the workspace).
+long long tc_workspace_floats(const TcPlan& p, int M, int N);
 // W map: box_rows 128 over [N][K]; X map: box_rows plan.BN over [M][K].
 cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
-                    int* err, long long wait_limit, cudaStream_t s, bool pdl);
+                    float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl);
 
 }  // namespace g3

@@ -17,6 +17,8 @@ enum EpiKind : int {
   EPI_RESID_GATED = 2,  // h[m][n] += gate[m / tok][n] * acc            (fp32 residual)
   EPI_RESID = 3,        // h[m][n] += acc
   EPI_GEGLU = 4,        // out[m][n/2] = gelu(acc[n]) * acc[n+1]          (interleaved gate/up rows)
+  EPI_PARTIAL = 5,      // split-K partial: out[(split * M + m) * ldo + n] = acc (fp32); the
+                        // consumer (norm / out_proj kernel) sums the splits into the residual
 };
 enum Act : int { ACT_NONE = 0, ACT_SWISH = 1, ACT_GELU = 2 };
 
@@ -51,11 +53,15 @@ struct GemmArgs {
 };
 
 // CUDA-core GEMM (any shape with N even).
-cudaError_t gemm_simt(DType dt, const GemmArgs& a, cudaStream_t s);
+cudaError_t gemm_simt(DType dt, const GemmArgs& a, cudaStream_t s, bool pdl);
 
 // ---- normalisation / projection kernels ------------------------------------
 enum NormKind : int { NORM_RMS = 0, NORM_LN = 1 };
 struct NormArgs {
+  // optional residual update first: h[m] += gate_b * sum_{s < S} part[s][m]   (rank order)
+  const float* part = nullptr;   // fp32 [S][M][D]
+  int part_S = 0, part_M = 0;
+  const void* gate = nullptr;    // activation dtype, per sample: gate + b * mod_bstride (nullable: 1)
   int kind = NORM_RMS;
   float eps = 1e-6f;
   const void* mod = nullptr;     // activation dtype; row for sample b: mod + b * mod_bstride
@@ -65,24 +71,25 @@ struct NormArgs {
 };
 
 // out[m] = norm(h[m]) * (1 + scale) + shift for m < M (mod == nullptr: plain norm)
-cudaError_t adanorm(DType dt, const float* h, int D, int M, void* out, NormArgs na, cudaStream_t s);
+// (with na.part: h[m] += gate * sum of the split-K partials first, written back)
+cudaError_t adanorm(DType dt, float* h, int D, int M, void* out, NormArgs na, cudaStream_t s, bool pdl);
 
 // EXPERT step head: h[m] = x[m] W_in^T + b_in (fp32), then out[m] = AdaRMS(h[m]).
 cudaError_t expert_in(DType dt, const float* x, int A, const void* w_in, const float* b_in, float* h,
-                      int D, int M, void* out, NormArgs na, cudaStream_t s);
+                      int D, int M, void* out, NormArgs na, cudaStream_t s, bool pdl);
 
 // Final norm + action_out_proj + Euler: rows m < M of the action tokens.
 // h row of action token m: (m / H) * tok + ro + m % H.  v = norm(h) W_out^T + b_out;
 // v_out[m] = v (nullable); if do_euler: x[m] += dt[k] * v.
-cudaError_t out_euler(DType dt, const float* h, int D, int M, int H, int ro, const void* w_out,
+cudaError_t out_euler(DType dt, float* h, int D, int M, int H, int ro, const void* w_out,
                       const float* b_out, int A, NormArgs na, float* x, const float* dts, int k,
-                      int do_euler, float* v_out, cudaStream_t s);
+                      int do_euler, float* v_out, cudaStream_t s, bool pdl);
 
 // DIT step head: a[m] = x[m] W1^T + b1 (activation dtype) for the M action rows, and the
 // state tokens copied into the residual rows (b * tok + j, j < ns) from state [B][ns][D].
 cudaError_t dit_in(DType dt, const float* x, int A, const void* w1, const float* b1, void* a_out,
                    int D, int M, const float* state, int ns, int tok, int B, float* h,
-                   cudaStream_t s);
+                   cudaStream_t s, bool pdl);
 
 // ---- attention ----------------------------------------------------------------
 struct AttnArgs {
@@ -99,7 +106,7 @@ struct AttnArgs {
   void* out = nullptr;      // output of (b, t, head): out + (b*Tq + t)*ldo + head*Dh
   int ldo = 0;
 };
-cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s);
+cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s, bool pdl);
 
 // Tensor-core attention of the expert family (one KV head, heads folded into rows).
 struct AttnFoldArgs {
@@ -110,8 +117,11 @@ struct AttnFoldArgs {
   int k_slot = 0, v_slot = 0;
   void* out = nullptr;         // bf16 [B*H][ldo], head h at column h*Dh
   int ldo = 0;
+  float* ws = nullptr;         // split partials (L2-resident scratch)
+  long long ws_floats = 0;
 };
 bool attn_fold_supported(int Dh);
+long long attn_fold_workspace_floats(const AttnFoldArgs& a, int S);
 int attn_fold_splits(const AttnFoldArgs& a, int sm_count);
 cudaError_t attention_fold(const AttnFoldArgs& a, int S, cudaStream_t s, bool pdl);
 

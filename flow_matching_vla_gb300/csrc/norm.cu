@@ -13,6 +13,8 @@
 // latency-bound, not bandwidth-bound.
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
+#include "tc_ptx.cuh"
 
 namespace g3 {
 
@@ -42,15 +44,62 @@ __device__ void norm_row(float* row, int D, int m, const NormArgs& na, float* re
   __syncthreads();
 }
 
+// Residual row m (optionally updated from split-K partials) into shared memory.
+// h[m] += gate * sum_s part[s][m]: the sum runs in split order, then one fma
+// per element -- the same arithmetic a single-pass epilogue would do.
 template <typename T>
-__global__ void adanorm_kernel(const float* __restrict__ h, int D, T* __restrict__ out,
-                               NormArgs na) {
+__device__ __forceinline__ void load_residual(float* __restrict__ h, int D, int m, const NormArgs& na,
+                                              float* row) {
+  float* hr = h + (long long)m * D;
+  if (!na.part) {
+    for (int i = threadIdx.x; i < D; i += blockDim.x) row[i] = hr[i];
+    __syncthreads();
+    return;
+  }
+  const T* g = na.gate ? (const T*)na.gate + (long long)(m / na.tok) * na.mod_bstride : nullptr;
+  // 4 elements per thread, the (<= 16) partial loads issued together, summed in split order
+  for (int i = threadIdx.x * 4; i < D; i += blockDim.x * 4) {
+    float4 v[16];
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      if (s < na.part_S) v[s] = *reinterpret_cast<const float4*>(na.part + ((long long)s * na.part_M + m) * D + i);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < 16; ++s)
+      if (s < na.part_S) {
+        acc.x += v[s].x;
+        acc.y += v[s].y;
+        acc.z += v[s].z;
+        acc.w += v[s].w;
+      }
+    float4 hv = *reinterpret_cast<const float4*>(hr + i);
+    float gg[4] = {1.f, 1.f, 1.f, 1.f};
+    if (g) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) gg[q] = to_f(g[i + q]);
+    }
+    hv.x += gg[0] * acc.x;
+    hv.y += gg[1] * acc.y;
+    hv.z += gg[2] * acc.z;
+    hv.w += gg[3] * acc.w;
+    *reinterpret_cast<float4*>(hr + i) = hv;
+    row[i] = hv.x;
+    row[i + 1] = hv.y;
+    row[i + 2] = hv.z;
+    row[i + 3] = hv.w;
+  }
+  __syncthreads();
+}
+
+template <typename T>
+__global__ void adanorm_kernel(float* __restrict__ h, int D, T* __restrict__ out, NormArgs na) {
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
   extern __shared__ float sm[];
   float* row = sm;
   float* red = sm + D;
   const int m = blockIdx.x;
-  const float* hr = h + (long long)m * D;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) row[i] = hr[i];
+  load_residual<T>(h, D, m, na, row);
   norm_row<T>(row, D, m, na, red);
   T* o = out + (long long)m * D;
   for (int i = threadIdx.x; i < D; i += blockDim.x) o[i] = from_f<T>(row[i]);
@@ -60,6 +109,8 @@ template <typename T>
 __global__ void expert_in_kernel(const float* __restrict__ x, int A, const T* __restrict__ w_in,
                                  const float* __restrict__ b_in, float* __restrict__ h, int D,
                                  T* __restrict__ out, NormArgs na) {
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
   extern __shared__ float sm[];
   float* row = sm;
   float* red = sm + D;
@@ -82,19 +133,20 @@ __global__ void expert_in_kernel(const float* __restrict__ x, int A, const T* __
 }
 
 template <typename T>
-__global__ void out_euler_kernel(const float* __restrict__ h, int D, int H, int ro, int tok,
+__global__ void out_euler_kernel(float* __restrict__ h, int D, int H, int ro, int tok,
                                  const T* __restrict__ w_out, const float* __restrict__ b_out,
                                  int A, NormArgs na, float* __restrict__ x,
                                  const float* __restrict__ dts, int k, int do_euler,
                                  float* __restrict__ v_out) {
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
   extern __shared__ float sm[];
   float* row = sm;
   float* red = sm + D;
   const int m = blockIdx.x;                       // action row b * H + j
   const long long hrow = (long long)(m / H) * tok + ro + m % H;
-  const float* hr = h + hrow * D;
-  for (int i = threadIdx.x; i < D; i += blockDim.x) row[i] = hr[i];
   // the modulation row is indexed per sample: pass the residual row so m / tok = b
+  load_residual<T>(h, D, (int)hrow, na, row);
   norm_row<T>(row, D, (int)hrow, na, red);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int a = warp; a < A; a += nw) {
@@ -115,6 +167,8 @@ __global__ void dit_in_kernel(const float* __restrict__ x, int A, const T* __res
                               const float* __restrict__ b1, T* __restrict__ a_out, int D, int M,
                               const float* __restrict__ state, int ns, int tok,
                               float* __restrict__ h) {
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
   extern __shared__ float xs[];
   const int blk = blockIdx.x;
   if (blk >= M) {  // state-token rows: copy the bound embedding into the residual stream
@@ -138,58 +192,49 @@ inline int threads_for(int D) { return D <= 512 ? 128 : 256; }
 
 }  // namespace
 
-cudaError_t adanorm(DType dt, const float* h, int D, int M, void* out, NormArgs na,
-                    cudaStream_t s) {
+cudaError_t adanorm(DType dt, float* h, int D, int M, void* out, NormArgs na, cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;
   const size_t smem = (D + 33) * sizeof(float);
   if (dt == DT_F32)
-    adanorm_kernel<float><<<M, threads_for(D), smem, s>>>(h, D, (float*)out, na);
-  else
-    adanorm_kernel<bf16><<<M, threads_for(D), smem, s>>>(h, D, (bf16*)out, na);
-  return cudaGetLastError();
+    return launch_k(adanorm_kernel<float>, M, threads_for(D), smem, s, pdl, h, D, (float*)out, na);
+  return launch_k(adanorm_kernel<bf16>, M, threads_for(D), smem, s, pdl, h, D, (bf16*)out, na);
 }
 
 cudaError_t expert_in(DType dt, const float* x, int A, const void* w_in, const float* b_in,
-                      float* h, int D, int M, void* out, NormArgs na, cudaStream_t s) {
+                      float* h, int D, int M, void* out, NormArgs na, cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;
   const size_t smem = (D + 33 + A) * sizeof(float);
   if (dt == DT_F32)
-    expert_in_kernel<float><<<M, threads_for(D), smem, s>>>(x, A, (const float*)w_in, b_in, h, D,
-                                                            (float*)out, na);
-  else
-    expert_in_kernel<bf16><<<M, threads_for(D), smem, s>>>(x, A, (const bf16*)w_in, b_in, h, D,
-                                                           (bf16*)out, na);
-  return cudaGetLastError();
+    return launch_k(expert_in_kernel<float>, M, threads_for(D), smem, s, pdl, x, A, (const float*)w_in,
+                    b_in, h, D, (float*)out, na);
+  return launch_k(expert_in_kernel<bf16>, M, threads_for(D), smem, s, pdl, x, A, (const bf16*)w_in, b_in,
+                  h, D, (bf16*)out, na);
 }
 
-cudaError_t out_euler(DType dt, const float* h, int D, int M, int H, int ro, const void* w_out,
+cudaError_t out_euler(DType dt, float* h, int D, int M, int H, int ro, const void* w_out,
                       const float* b_out, int A, NormArgs na, float* x, const float* dts, int k,
-                      int do_euler, float* v_out, cudaStream_t s) {
+                      int do_euler, float* v_out, cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;
   const size_t smem = (D + 33) * sizeof(float);
   const int tok = na.tok;
   if (dt == DT_F32)
-    out_euler_kernel<float><<<M, 256, smem, s>>>(h, D, H, ro, tok, (const float*)w_out, b_out, A,
-                                                 na, x, dts, k, do_euler, v_out);
-  else
-    out_euler_kernel<bf16><<<M, 256, smem, s>>>(h, D, H, ro, tok, (const bf16*)w_out, b_out, A,
-                                                na, x, dts, k, do_euler, v_out);
-  return cudaGetLastError();
+    return launch_k(out_euler_kernel<float>, M, 256, smem, s, pdl, h, D, H, ro, tok, (const float*)w_out,
+                    b_out, A, na, x, dts, k, do_euler, v_out);
+  return launch_k(out_euler_kernel<bf16>, M, 256, smem, s, pdl, h, D, H, ro, tok, (const bf16*)w_out, b_out,
+                  A, na, x, dts, k, do_euler, v_out);
 }
 
 cudaError_t dit_in(DType dt, const float* x, int A, const void* w1, const float* b1, void* a_out,
                    int D, int M, const float* state, int ns, int tok, int B, float* h,
-                   cudaStream_t s) {
+                   cudaStream_t s, bool pdl) {
   const int blocks = M + (state ? B * ns : 0);
   if (blocks <= 0) return cudaSuccess;
   const size_t smem = A * sizeof(float);
   if (dt == DT_F32)
-    dit_in_kernel<float><<<blocks, threads_for(D), smem, s>>>(x, A, (const float*)w1, b1,
-                                                              (float*)a_out, D, M, state, ns, tok, h);
-  else
-    dit_in_kernel<bf16><<<blocks, threads_for(D), smem, s>>>(x, A, (const bf16*)w1, b1,
-                                                             (bf16*)a_out, D, M, state, ns, tok, h);
-  return cudaGetLastError();
+    return launch_k(dit_in_kernel<float>, blocks, threads_for(D), smem, s, pdl, x, A, (const float*)w1, b1,
+                    (float*)a_out, D, M, state, ns, tok, h);
+  return launch_k(dit_in_kernel<bf16>, blocks, threads_for(D), smem, s, pdl, x, A, (const bf16*)w1, b1,
+                  (bf16*)a_out, D, M, state, ns, tok, h);
 }
 
 }  // namespace g3

@@ -74,8 +74,19 @@ struct gr00t_ctx {
 
   // tensor-core GEMM: SM count and a cache of TMA descriptors
   int sm_count = 148;
+  float* gemm_ws = nullptr;   // split-K partials (L2-resident scratch)
+  long long gemm_ws_floats = 0;
   std::map<std::tuple<const void*, long long, long long, long long, int>, CUtensorMap> tmaps;
   int opt_pdl = 1;
+  int split_cap = 8;        // GEMMs that reduce their split-K partials in-kernel
+  int resid_split_cap = 16; // residual GEMMs whose partials the next kernel folds in
+
+  // split-K partials a residual GEMM left for the next norm / out_proj kernel
+  struct Pending {
+    const float* part = nullptr;
+    int S = 0, M = 0;
+    const void* gate = nullptr;
+  } pending;
 
   // per-kernel timing: event pairs around every launch of one kernel class
   int time_class = 0;
@@ -231,6 +242,9 @@ void plan_buffers(gr00t_ctx* c, Plan& pl) {
   if (dit) pl.add((void**)&c->atb, (size_t)c->g.max_steps * D * 4);
   if (!dit) pl.add((void**)&c->rope_tab, (size_t)c->H * (c->Dh / 2) * sizeof(float2));
   pl.add((void**)&c->table, (size_t)(2 * L + 3) * sizeof(void*));
+  // split-K plans keep tiles * S <= 17/16 of the SM count; BN <= 256, 128 rows each
+  c->gemm_ws_floats = (long long)(c->sm_count + c->sm_count / 16 + 1) * 256 * 128;
+  pl.add((void**)&c->gemm_ws, (size_t)c->gemm_ws_floats * 4);
   pl.add((void**)&c->err_flag, 64);
 }
 
@@ -373,16 +387,46 @@ int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
   ++c->launches;
   tmark(c, cls);
   if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
-    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count);
+    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, a.epi.kind == EPI_PARTIAL ? c->resid_split_cap : c->split_cap);
     const CUtensorMap* tw = tmap(c, a.W, a.N, a.K, a.ldw, 128);
     const CUtensorMap* tx = tmap(c, a.A, a.M, a.K, a.lda, p.BN);
     if (!tw || !tx) return set_err(c, GR00T_ECUDA, "TMA descriptor encode failed (alignment?)");
-    CK(c, gemm_tc(*tw, *tx, a, p, c->err_flag, c->wait_limit, c->stream, c->opt_pdl != 0));
+    CK(c, gemm_tc(*tw, *tx, a, p, c->gemm_ws, c->gemm_ws_floats, c->err_flag, c->wait_limit, c->stream,
+                  c->opt_pdl != 0));
   } else {
-    CK(c, gemm_simt(c->dt, a, c->stream));
+    CK(c, gemm_simt(c->dt, a, c->stream, c->opt_pdl != 0));
   }
   tmark(c, cls);
   return GR00T_OK;
+}
+
+// Residual GEMM h += gate * (A W^T).  When the tensor-core plan splits K, the
+// S fp32 partials go to the scratch workspace and the next norm / out_proj
+// kernel folds them into h (pending), saving a reduction phase here.
+int gemm_resid(gr00t_ctx* c, GemmArgs a, int cls) {
+  if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
+    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, c->resid_split_cap);
+    if (p.S > 1 && (long long)p.S * a.M * a.N <= c->gemm_ws_floats) {
+      c->pending.part = c->gemm_ws;
+      c->pending.S = p.S;
+      c->pending.M = a.M;
+      c->pending.gate = a.epi.kind == EPI_RESID_GATED ? a.epi.gate : nullptr;
+      a.epi.kind = EPI_PARTIAL;
+      a.epi.out = c->gemm_ws;
+      a.epi.ldo = a.N;
+    }
+  }
+  return gemm(c, a, cls);
+}
+
+// Attach (and clear) pending partials to the next norm's arguments.
+NormArgs take_pending(gr00t_ctx* c, NormArgs na) {
+  na.part = c->pending.part;
+  na.part_S = c->pending.S;
+  na.part_M = c->pending.M;
+  na.gate = c->pending.gate;
+  c->pending = gr00t_ctx::Pending();
+  return na;
 }
 
 #define RC(x)                          \
@@ -421,7 +465,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     na.shift_off = D;
     ++c->launches;
     tmark(c, GR00T_KCLASS_NORM);
-    CK(c, expert_in(c->dt, x, c->A, c->w_in, c->b_in, c->h, D, M, c->n, na, s));
+    CK(c, expert_in(c->dt, x, c->A, c->w_in, c->b_in, c->h, D, M, c->n, na, s, c->opt_pdl != 0));
     tmark(c, GR00T_KCLASS_NORM);
     const int nq = c->nqkv[0];
     for (int l = 0; l < L; ++l) {
@@ -440,6 +484,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         af.B = B; af.H = H; af.Hq = c->Hq; af.Dh = c->Dh; af.P = P;
         af.table = c->table; af.k_slot = 2 * l; af.v_slot = 2 * l + 1;
         af.out = c->att; af.ldo = c->qd;
+        af.ws = c->gemm_ws; af.ws_floats = c->gemm_ws_floats;   // kernels run in order: one scratch
         CK(c, attention_fold(af, attn_fold_splits(af, c->sm_count), s, c->opt_pdl != 0));
       } else {
         AttnArgs at;
@@ -447,7 +492,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         at.table = c->table; at.k_slot = 2 * l; at.v_slot = 2 * l + 1; at.P = P;
         at.ks = ptr_at(c->qkv, (long long)c->qd, es); at.vs = ptr_at(c->qkv, (long long)c->qd + c->Dh, es);
         at.lds = nq; at.S = tok; at.out = c->att; at.ldo = c->qd;
-        CK(c, attention_simt(c->dt, at, s));
+        CK(c, attention_simt(c->dt, at, s, c->opt_pdl != 0));
       }
       tmark(c, GR00T_KCLASS_ATTENTION);
 
@@ -455,13 +500,13 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       go.A = c->att; go.lda = c->qd; go.W = c->w_o[l]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
       go.epi.kind = EPI_RESID_GATED; go.epi.resid = c->h; go.epi.ldr = D;
       go.epi.gate = ptr_at(site(2 * l), 2LL * D, es); go.epi.gate_bstride = bstride; go.epi.tok = tok;
-      RC(gemm(c, go, GR00T_KCLASS_O_GEMM));
+      RC(gemm_resid(c, go, GR00T_KCLASS_O_GEMM));
 
       NormArgs n2 = na;
       n2.mod = site(2 * l + 1);
       ++c->launches;
       tmark(c, GR00T_KCLASS_NORM);
-      CK(c, adanorm(c->dt, c->h, D, M, c->n, n2, s));
+      CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, n2), s, c->opt_pdl != 0));
       tmark(c, GR00T_KCLASS_NORM);
 
       GemmArgs gu;
@@ -478,14 +523,14 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       gd.A = c->u; gd.lda = c->F; gd.W = c->w_down[l]; gd.ldw = c->F; gd.M = M; gd.N = D; gd.K = c->F;
       gd.epi.kind = EPI_RESID_GATED; gd.epi.resid = c->h; gd.epi.ldr = D;
       gd.epi.gate = ptr_at(site(2 * l + 1), 2LL * D, es); gd.epi.gate_bstride = bstride; gd.epi.tok = tok;
-      RC(gemm(c, gd, GR00T_KCLASS_DOWN_GEMM));
+      RC(gemm_resid(c, gd, GR00T_KCLASS_DOWN_GEMM));
 
       if (l + 1 < L) {
         NormArgs n3 = na;
         n3.mod = site(2 * l + 2);
         ++c->launches;
         tmark(c, GR00T_KCLASS_NORM);
-        CK(c, adanorm(c->dt, c->h, D, M, c->n, n3, s));
+        CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, n3), s, c->opt_pdl != 0));
         tmark(c, GR00T_KCLASS_NORM);
       }
     }
@@ -493,8 +538,9 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     nf.mod = site(2 * L);
     ++c->launches;
     tmark(c, GR00T_KCLASS_NORM);
-    CK(c, out_euler(c->dt, c->h, D, MA, H, 0, c->w_out, c->b_out, c->A, nf, x, c->dts, k, do_euler,
-                    v_out, s));
+    CK(c, out_euler(c->dt, c->h, D, MA, H, 0, c->w_out, c->b_out, c->A, take_pending(c, nf), x, c->dts, k,
+                    do_euler,
+                    v_out, s, c->opt_pdl != 0));
     tmark(c, GR00T_KCLASS_NORM);
     return GR00T_OK;
   }
@@ -504,7 +550,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   ++c->launches;
   tmark(c, GR00T_KCLASS_NORM);
   CK(c, dit_in(c->dt, x, c->A, c->w_enc1, c->b_enc1, c->a_enc, D, MA, (const float*)c->host_table[2 * L + 2],
-               Ns, tok, B, c->h, s));
+               Ns, tok, B, c->h, s, c->opt_pdl != 0));
   tmark(c, GR00T_KCLASS_NORM);
   {
     GemmArgs g;  // e = swish(a W2[:, :D]^T + atb_k), atb_k holds W2's time half and b2
@@ -527,7 +573,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     n1.mod = site(i);
     ++c->launches;
     tmark(c, GR00T_KCLASS_NORM);
-    CK(c, adanorm(c->dt, c->h, D, M, c->n, n1, s));
+    CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, n1), s, c->opt_pdl != 0));
     tmark(c, GR00T_KCLASS_NORM);
     const int nq = c->nqkv[i];
     GemmArgs g;
@@ -548,17 +594,17 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     }
     ++c->launches;
     tmark(c, GR00T_KCLASS_ATTENTION);
-    CK(c, attention_simt(c->dt, at, s));
+    CK(c, attention_simt(c->dt, at, s, c->opt_pdl != 0));
     tmark(c, GR00T_KCLASS_ATTENTION);
     GemmArgs go;
     go.A = c->att; go.lda = c->qd; go.W = c->w_o[i]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
     go.epi.kind = EPI_RESID; go.epi.resid = c->h; go.epi.ldr = D;
-    RC(gemm(c, go, GR00T_KCLASS_O_GEMM));
+    RC(gemm_resid(c, go, GR00T_KCLASS_O_GEMM));
     NormArgs n3 = na;
     n3.mod = nullptr;
     ++c->launches;
     tmark(c, GR00T_KCLASS_NORM);
-    CK(c, adanorm(c->dt, c->h, D, M, c->n, n3, s));
+    CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, n3), s, c->opt_pdl != 0));
     tmark(c, GR00T_KCLASS_NORM);
     GemmArgs gu;
     gu.A = c->n; gu.lda = D; gu.W = c->w_up[i]; gu.ldw = D; gu.M = M; gu.N = c->F; gu.K = D;
@@ -567,7 +613,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     GemmArgs gd;
     gd.A = c->u; gd.lda = c->F; gd.W = c->w_down[i]; gd.ldw = c->F; gd.M = M; gd.N = D; gd.K = c->F;
     gd.epi.kind = EPI_RESID; gd.epi.resid = c->h; gd.epi.ldr = D;
-    RC(gemm(c, gd, GR00T_KCLASS_DOWN_GEMM));
+    RC(gemm_resid(c, gd, GR00T_KCLASS_DOWN_GEMM));
   }
   NormArgs nf = na;
   nf.mod = site(L);
@@ -575,8 +621,9 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   nf.shift_off = 0;
   ++c->launches;
   tmark(c, GR00T_KCLASS_NORM);
-  CK(c, out_euler(c->dt, c->h, D, MA, H, Ns, c->w_out, c->b_out, c->A, nf, x, c->dts, k, do_euler,
-                  v_out, s));
+  CK(c, out_euler(c->dt, c->h, D, MA, H, Ns, c->w_out, c->b_out, c->A, take_pending(c, nf), x, c->dts, k,
+                  do_euler,
+                  v_out, s, c->opt_pdl != 0));
   tmark(c, GR00T_KCLASS_NORM);
   return GR00T_OK;
 }
@@ -877,6 +924,11 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
     case GR00T_OPT_WAIT_LIMIT:
       if (value < 0) return set_err(c, GR00T_EINVAL, "wait limit must be >= 0");
       c->wait_limit = value;
+      break;
+    case GR00T_OPT_SPLIT_CAP:
+    case GR00T_OPT_RESID_SPLIT_CAP:
+      if (value < 1 || value > 16 || (value & (value - 1))) return set_err(c, GR00T_EINVAL, "split cap: 1, 2, 4, 8 or 16");
+      (option == GR00T_OPT_SPLIT_CAP ? c->split_cap : c->resid_split_cap) = (int)value;
       break;
     case GR00T_OPT_TIME_KERNEL: {
       if (value < 0 || value > GR00T_KCLASS_NORM) return set_err(c, GR00T_EINVAL, "unknown kernel class");

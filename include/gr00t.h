@@ -242,6 +242,8 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
 #define GR00T_OPT_ATTN_PATH 4     /* 0: tensor-core attention where supported (default), 1: CUDA-core */
 #define GR00T_OPT_TIME_KERNEL 5   /* bracket every launch of one kernel class with timing events
                                      (GR00T_KCLASS_*, 0 = off); read with gr00t_kernel_times */
+#define GR00T_OPT_SPLIT_CAP 6     /* largest split-K factor of GEMMs that reduce in-kernel (1..16, power of 2; default 8) */
+#define GR00T_OPT_RESID_SPLIT_CAP 7 /* same for residual GEMMs whose partials the next kernel folds in (default 16) */
 int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
 
 #define GR00T_INFO_KERNELS_PER_STEP 1   /* kernel launches of one denoise step            */
