@@ -229,6 +229,12 @@ class DenoiseLoop:
         self._check(self._lib.gr00t_denoise_step(self._ctx, int(k), _ptr(x_in), _ptr(self._chunk(v_out))))
         return v_out
 
+    def denoise_step_noalloc(self, k: int, x_in, v_out):
+        """gr00t_denoise_step_noalloc: the same step with scratch from the library's fixed array."""
+        self._check(self._lib.gr00t_denoise_step_noalloc(self._ctx, int(k), _ptr(self._chunk(x_in)),
+                                                         _ptr(self._chunk(v_out))))
+        return v_out
+
     def set_option(self, option: int, value: int):
         self._check(self._lib.gr00t_set_option(self._ctx, int(option), int(value)))
 

@@ -58,6 +58,7 @@ SIGNATURES = {
     "gr00t_denoise": (ctypes.c_int, [_VP, _VP, _VP]),
     "gr00t_denoise_host": (ctypes.c_int, [_VP, _VP, _VP]),
     "gr00t_denoise_step": (ctypes.c_int, [_VP, ctypes.c_int, _VP, _VP]),
+    "gr00t_denoise_step_noalloc": (ctypes.c_int, [_VP, ctypes.c_int, _VP, _VP]),
     "gr00t_destroy": (ctypes.c_int, [_VP]),
     "gr00t_last_error": (ctypes.c_char_p, [_VP]),
     "gr00t_set_option": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int64]),

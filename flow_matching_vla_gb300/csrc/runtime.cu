@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <map>
+#include <mutex>
 #include <string>
 #include <tuple>
 #include <vector>
@@ -73,6 +74,7 @@ struct gr00t_ctx {
   int launches = 0;  // kernel launches of the last enqueued step
 
   // tensor-core GEMM: SM count and a cache of TMA descriptors
+  int device = 0;
   int sm_count = 148;
   float* gemm_ws = nullptr;   // split-K partials (L2-resident scratch)
   long long gemm_ws_floats = 0;
@@ -716,6 +718,7 @@ extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, voi
   gr00t_ctx* c = new gr00t_ctx();
   c->g = *g;
   c->sm_count = prop.multiProcessorCount;
+  c->device = dev;
   c->dt = g->dtype == GR00T_DTYPE_BF16 ? DT_BF16 : DT_F32;
   c->esz = c->dt == DT_BF16 ? 2 : 4;
   c->D = g->hidden; c->L = g->layers; c->Hq = g->q_heads; c->Hkv = g->kv_heads; c->Dh = g->head_dim;
@@ -998,4 +1001,104 @@ extern "C" int gr00t_kernel_times(gr00t_ctx* c, float* ms, int max, int* count) 
   }
   *count = n;
   return GR00T_OK;
+}
+
+// ---- allocation-free step ------------------------------------------------------
+//
+// Scratch of gr00t_denoise_step_noalloc: a fixed array in the library's device
+// image, 8 MiB of fp32 on every GPU that loads the library, held until the
+// process exits.  Host code cannot use the symbol itself as a device address;
+// its device address is looked up once per device with that device current.
+#define G3_NOALLOC_SCRATCH_FLOATS (1 << 21)
+static __device__ __align__(256) float g_noalloc_scratch[G3_NOALLOC_SCRATCH_FLOATS];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+constexpr int kMaxDevices = 256;
+float* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the fixed scratch array on device ``dev`` (current).
+cudaError_t noalloc_scratch(int dev, float** out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return cudaSuccess;
+}
+
+// Scratch (fp32 elements) one GEMM of the step uses when the scratch holds ``cap``
+// elements; mirrors gemm() / gemm_resid().
+long long gemm_scratch(gr00t_ctx* c, int M, int N, int K, bool resid, long long cap) {
+  if (!(c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(M, N, K))) return 0;
+  if (resid) {
+    const TcPlan p = tc_plan(M, N, K, c->sm_count, c->resid_split_cap);
+    if (p.S > 1 && (long long)p.S * M * N <= cap) return (long long)p.S * M * N;
+  }
+  return tc_workspace_floats(tc_plan(M, N, K, c->sm_count, c->split_cap), M, N);
+}
+
+// Largest scratch any kernel of one denoise step needs at the bound (batch, prefix).
+long long step_scratch(gr00t_ctx* c, long long cap) {
+  const int B = c->bB, D = c->D, M = B * c->tok, MA = B * c->H;
+  long long need = 0;
+  auto take = [&](long long v) { need = v > need ? v : need; };
+  const int up_rows = (c->g.mlp_kind == GR00T_MLP_GEGLU ? 2 : 1) * c->F;
+  if (c->g.family == GR00T_FAMILY_DIT) {
+    take(gemm_scratch(c, MA, D, D, false, cap));
+    for (int l = 0; l < c->L; ++l) {
+      take(gemm_scratch(c, M, c->nqkv[l], D, false, cap));
+      take(gemm_scratch(c, M, D, c->qd, true, cap));
+      take(gemm_scratch(c, M, up_rows, D, false, cap));
+      take(gemm_scratch(c, M, D, c->F, true, cap));
+    }
+    return need;
+  }
+  take(gemm_scratch(c, M, c->nqkv[0], D, false, cap));
+  take(gemm_scratch(c, M, D, c->qd, true, cap));
+  take(gemm_scratch(c, M, up_rows, D, false, cap));
+  take(gemm_scratch(c, M, D, c->F, true, cap));
+  if (c->dt == DT_BF16 && c->opt_attn == 0 && attn_fold_supported(c->Dh)) {
+    AttnFoldArgs af;
+    af.B = B; af.H = c->H; af.Hq = c->Hq; af.Dh = c->Dh; af.P = c->bP;
+    take(attn_fold_workspace_floats(af, attn_fold_splits(af, c->sm_count)));
+  }
+  return need;
+}
+
+}  // namespace
+
+extern "C" int gr00t_denoise_step_noalloc(gr00t_ctx* c, int k, const float* x_in, float* v_out) {
+  if (!c) return GR00T_EINVAL;
+  if (!x_in || !v_out) return set_err(c, GR00T_EINVAL, "x_in/v_out is NULL");
+  RC(check_ready(c));
+  if (k < 0 || k >= c->sT) return set_err(c, GR00T_EINVAL, "step %d outside [0, %d)", k, c->sT);
+  int dev = -1;
+  CK(c, cudaGetDevice(&dev));
+  if (dev != c->device)
+    return set_err(c, GR00T_EINVAL, "device %d is current; the context lives on device %d", dev, c->device);
+  const long long cap = G3_NOALLOC_SCRATCH_FLOATS;
+  const long long need = step_scratch(c, cap);
+  if (need > cap)
+    return set_err(c, GR00T_EINVAL,
+                   "this step needs %lld floats of scratch at batch %d, prefix %d; the fixed array holds %lld "
+                   "(use gr00t_denoise_step)", need, c->bB, c->bP, cap);
+  float* scratch = nullptr;
+  CK(c, noalloc_scratch(dev, &scratch));
+  const size_t bytes = (size_t)c->bB * c->H * c->A * sizeof(float);
+  CK(c, cudaMemcpyAsync(c->xtmp, x_in, bytes, cudaMemcpyDeviceToDevice, c->stream));
+  // same launch sequence as gr00t_denoise_step, scratch taken from the fixed array
+  float* const own = c->gemm_ws;
+  const long long own_floats = c->gemm_ws_floats;
+  c->gemm_ws = scratch;
+  c->gemm_ws_floats = cap;
+  const int rc = enqueue_step(c, k, c->xtmp, v_out, 0);
+  c->gemm_ws = own;
+  c->gemm_ws_floats = own_floats;
+  return rc;
 }

@@ -228,6 +228,34 @@ int gr00t_denoise_host(gr00t_ctx* ctx, const float* x_noise_host, float* actions
  */
 int gr00t_denoise_step(gr00t_ctx* ctx, int k, const float* x_in, float* v_out);
 
+/*
+ * gr00t_denoise_step with no allocation of any kind and no use of the
+ * context's scratch workspace.  (No counterpart in the source pages: this is
+ * an interface addition of this library.)
+ *
+ * Who it is for: callers that are not allowed to allocate device memory at
+ * the point where they run a step -- e.g. a controller that fixed its device
+ * memory budget at start-up and treats any later allocation as an error, or a
+ * host program that lends this library a context and forbids it from taking
+ * memory of its own.  This call never calls cudaMalloc, cudaFree or any other
+ * allocating routine; the scratch that the tensor-core GEMMs (split-K
+ * partials) and the attention (per-split partials) need comes from a fixed
+ * array compiled into the library: 8 MiB of fp32 (2^21 floats) in the device
+ * image of every GPU that loads the library, held until the process exits.
+ *
+ * Same arguments, inputs, outputs and results as gr00t_denoise_step.
+ * Set-up: the first call on a device looks up the array's device address
+ * (with that device current -- it must be the context's device); make that
+ * first call before any stream capture.  A step whose scratch need at the
+ * bound (batch, prefix) exceeds the array returns GR00T_EINVAL with the need
+ * in gr00t_last_error, before anything is enqueued.  All calls in the process
+ * share the one array: calls that overlap on the GPU (other streams, other
+ * contexts) race on it.  The array keeps the last call's contents; every
+ * kernel writes the scratch it reads within the same step, so nothing in it
+ * has to start at zero.
+ */
+int gr00t_denoise_step_noalloc(gr00t_ctx* ctx, int k, const float* x_in, float* v_out);
+
 /* Free everything the context owns (synchronises its stream first). */
 int gr00t_destroy(gr00t_ctx* ctx);
 

@@ -1,0 +1,60 @@
+"""The allocation-free step entry point, checked against gr00t_denoise_step.
+
+Collected last on purpose (file name): a failure here comes after every other
+test has run.  The entry point exists for callers that may not allocate device
+memory when they run a step; it takes its scratch from a fixed array in the
+library image instead of the context's workspace, so its results must match
+the regular step's on the same inputs, call after call.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+VEL_REL = 1e-2     # bf16 per-step velocity gate used by the parity tests
+
+
+def _fmv():
+    import flow_matching_vla_gb300 as fmv
+    return fmv
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "pi05"])
+def test_noalloc_step_matches_regular_step_twice(name):
+    fmv = _fmv()
+    c = synth.make_case(name)
+    loop, held = fmv.from_case(c)
+    x = torch.from_numpy(c["x_noise"]).cuda()
+    for k in (0, c["geom"]["steps"] - 1):      # two calls in a row, different steps
+        ref = loop.denoise_step(k, x).clone()
+        got = torch.full_like(ref, float("nan"))
+        loop.denoise_step_noalloc(k, x, got)
+        torch.cuda.synchronize()
+        assert torch.isfinite(got).all()
+        e_inf, e_rel = oracle.error_metrics(got.cpu().numpy(), ref.cpu().numpy())
+        assert e_rel <= VEL_REL, (k, e_rel)
+    assert loop.info(fmv.INFO_ERROR_FLAG) == 0
+
+
+def test_noalloc_rejects_a_step_larger_than_its_scratch():
+    fmv = _fmv()
+    # 32 samples of a 1024-wide expert: the deferred residual partials alone are
+    # 2 x 1600 x 1024 floats, more than the fixed 2^21-float array
+    c = synth.make_case("small_bf16", hidden=1024, mlp_dim=1024, batch=32, layers=1, prefix=64,
+                        time_dim=256)
+    loop, held = fmv.from_case(c)
+    x = torch.from_numpy(c["x_noise"]).cuda()
+    out = torch.empty_like(x)
+    with pytest.raises(fmv.Gr00tError) as ei:
+        loop.denoise_step_noalloc(0, x, out)
+    assert ei.value.status == -1 and "fixed array" in str(ei.value)
+    # the regular entry point still runs the same step
+    loop.denoise_step(0, x, out)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
