@@ -62,9 +62,9 @@ extern "C" {
 
 /*
  * Geometry of one expert.  Validated by gr00t_create before anything is
- * allocated ("GR00T N1.7": a mismatch fails before a network is created;
- * "pi0.5 Design": a configuration the runtime does not implement is refused
- * at load rather than run).
+ * allocated ("GR00T N1.7", Checkpoint: a wrong architecture is rejected
+ * before anything is built; "pi0.5 Design", Runtime boundary: unsupported
+ * configurations are rejected when loading).
  *
  * EXPERT family: kv_heads must be 1 (the head fold is exact only with a
  * single KV head and an all-ones mask, "pi0.5 Design", Attention and the K/V
@@ -166,8 +166,8 @@ int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, void* stream, 
 
 /*
  * Bind the per-request prefix / VL-context K/V for the whole denoise loop
- * ("GR00T N1.7", Who runs what: runs once, its outputs stay bound for the
- * whole denoise loop; "pi0.5 Design": prefix K/V (bound once)).
+ * ("GR00T N1.7", Who runs what: the backbone's K/V is produced once per
+ * request and reused by every denoise step; "pi0.5 Design", sequence diagram).
  *
  * ``k``, ``v``: arrays of ``layers`` DEVICE pointers, each to a contiguous
  * [batch, prefix, kv_heads, head_dim] tensor in the geometry's dtype.  EXPERT:
@@ -192,8 +192,8 @@ int gr00t_bind_prefix_kv(gr00t_ctx* ctx, int batch, int prefix, const void* cons
 
 /*
  * Hoist the time conditioning for a step count and batch ("pi0.5 Design",
- * cond component: the time embedder and the AdaRMS Denses move out of the
- * per-step graph and re-run only when the step count or batch changes;
+ * cond component: the time embedder and the AdaRMS Denses leave the
+ * per-step graph and are evaluated again only for a new step count or batch;
  * "GR00T N1.7", Build-time constants).  Builds the modulation table
  * [steps * batch, sites, row] (rows [step][request]), the Euler step sizes
  * on the uniform grid of vla.cpp Eq. (1), and for DIT the action_time_bias

@@ -18,10 +18,11 @@ def _w(w, name, dtype):
 def action_time_bias(g, w, steps, dtype=np.float64):
     """Hoisted action_time_bias [steps, D] ("GR00T N1.7", Build-time constants).
 
-    The page hoists "the timestep half of the action encoder's W2, plus the
-    concatenation".  W2 acts on concat(W1 x + b1, temb(tau)); its time half
-    applied to the sinusoid of tau_k, plus W2's bias, is the bias row of step
-    k: atb_k = W2[:, D:] temb(tau_k) + b2 (reading S3 for temb).
+    The page moves the part of the encoder's second projection that only
+    sees the time embedding out of the step.  W2 acts on concat(W1 x + b1,
+    temb(tau)); its time columns applied to the sinusoid of tau_k, plus W2's
+    bias, form the bias row of step k: atb_k = W2[:, D:] temb(tau_k) + b2
+    (reading S3 for temb).
     """
     D = g["hidden"]
     taus, _ = schedule(g["direction"], steps)

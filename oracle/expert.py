@@ -31,7 +31,7 @@ def expert_velocity(g, w, x, mod_k, K, V, dtype=np.float64, trace=None):
 
     ``x``: [B, H, A]; ``mod_k``: [B, 2L+1, 3D] (this step's modulation rows,
     one per request); ``K``/``V``: per layer [B, P, 1, Dh] prefix K/V, bound
-    once ("pi0.5 Design", sequence diagram: prefix K/V (bound once)).
+    once per request and reused by every step ("pi0.5 Design", sequence diagram).
 
     Per layer l (rows of the hoisted table per the Component contract):
       n  = AdaRMS(h, row 2l)                         input_layernorm

@@ -195,7 +195,7 @@ def test_hoisted_table_equals_per_step_evaluation(name):
 
 
 def test_action_time_bias_is_time_half_of_w2():
-    # "the timestep half of the action encoder's W2, plus the concatenation"
+    # the hoisted bias is W2's time columns applied to the sinusoid, plus W2's bias
     c = synth.make_case("small_dit")
     g, w = c["geom"], c["weights"]
     D = g["hidden"]
