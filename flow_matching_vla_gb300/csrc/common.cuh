@@ -53,4 +53,21 @@ __device__ __forceinline__ float gelu_tanhf(float x) {
   return 0.5f * x * (1.f + tanhf(c * (x + 0.044715f * x * x * x)));
 }
 
+// The same GeLU with the hardware tanh.approx.f32 instruction (relative error
+// about 2^-11, below the bf16 rounding of its output); used on the bf16 path.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gelu_tanh_fast(float x) {
+  const float c = 0.7978845608028654f;
+  return 0.5f * x * (1.f + tanh_approx(c * (x + 0.044715f * x * x * x)));
+}
+
+// GeLU used by the epilogues: accurate tanh for fp32 activations, hardware tanh for bf16.
+template <typename T> __device__ __forceinline__ float gelu_act(float x);
+template <> __device__ __forceinline__ float gelu_act<float>(float x) { return gelu_tanhf(x); }
+template <> __device__ __forceinline__ float gelu_act<bf16>(float x) { return gelu_tanh_fast(x); }
+
 }  // namespace g3

@@ -36,8 +36,8 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, f
         a0 = swishf(a0);
         a1 = swishf(a1);
       } else if (e.act == ACT_GELU) {
-        a0 = gelu_tanhf(a0);
-        a1 = gelu_tanhf(a1);
+        a0 = gelu_act<T>(a0);
+        a1 = gelu_act<T>(a1);
       }
       const long long r = e.rg ? (long long)(m / e.rg) * e.rs + e.ro + m % e.rg : (long long)m;
       if (e.out_f32)
@@ -77,7 +77,7 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, f
     }
     case EPI_GEGLU: {
       T* o = (T*)e.out + (long long)m * e.ldo + (n >> 1);
-      *o = from_f<T>(gelu_tanhf(a0) * a1);
+      *o = from_f<T>(gelu_act<T>(a0) * a1);
       break;
     }
     default:

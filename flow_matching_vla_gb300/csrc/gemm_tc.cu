@@ -51,15 +51,16 @@ template <int U>
 __device__ __forceinline__ void reduce_rows(const Epi& e, const float* __restrict__ base, int S, int rank,
                                             int m0, int n0, int M, int N, int BN) {
   const int R = BM / S, pairs = R / 2, items = pairs * BN;
+  const int nt = blockDim.x;
 #pragma unroll 1
-  for (int it0 = threadIdx.x; it0 < items; it0 += 128 * U) {
+  for (int it0 = threadIdx.x; it0 < items; it0 += nt * U) {
     int mm[U], nn[U], jj[U], rr[U];
     bool ok[U];
     EpiPre pre[U];
     float2 acc[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      const int it = it0 + u * 128;
+      const int it = it0 + u * nt;
       const int p = it % pairs, j = it / pairs;
       rr[u] = rank * R + 2 * p;
       jj[u] = j;
@@ -87,8 +88,10 @@ __device__ __forceinline__ void reduce_rows(const Epi& e, const float* __restric
   }
 }
 
+constexpr int kThreads = 256;  // 8 warps: warp 0 TMA, warp 1 MMA, all 8 share the epilogue
+
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
                    int N, int kb_per_split, Epi e, float* __restrict__ ws, int* err, long long wait_limit) {
   using L = TcSmem<BN, STAGES>;
@@ -194,8 +197,12 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const bool aborted = *abort_flag != 0;
-  const int row = warp * 32 + lane;         // TMEM lane = weight row n0 + row
-  const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+  // TMEM lane quadrant q = warp % 4 holds weight rows 32q..32q+31; the two warps
+  // of a quadrant split the BN token columns
+  const int quad = warp & 3;
+  const int row = quad * 32 + lane;          // TMEM lane = weight row n0 + row
+  const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
+  const int c_begin = (warp >> 2) * (BN / 2), c_end = c_begin + BN / 2;
 
   if (e.kind == EPI_PARTIAL) {
     // split partial straight to the consumer's buffer: out[(split * M + m) * ldo + n]
@@ -203,7 +210,7 @@ __global__ void __launch_bounds__(128, 1)
     const int n = n0 + row;
     if (!aborted) {  // CTA-uniform: every lane takes part in tcgen05.ld
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         float v[32];
         ptx::tmem_ld32(taddr + (uint32_t)c0, v);
         if (n < N) {
@@ -220,7 +227,7 @@ __global__ void __launch_bounds__(128, 1)
     const bool odd = lane & 1;
     if (!aborted) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         float v[32];
         ptx::tmem_ld32(taddr + (uint32_t)c0, v);
 #pragma unroll
@@ -242,7 +249,7 @@ __global__ void __launch_bounds__(128, 1)
     float* my = ws + ((tile * S + (long long)blockIdx.z) * BN) * BM;
     if (!aborted) {
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         float v[32];
         ptx::tmem_ld32(taddr + (uint32_t)c0, v);
 #pragma unroll
@@ -287,7 +294,7 @@ cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs&
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.N + BM - 1) / BM, (a.M + BN - 1) / BN, S);
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = L::TOTAL;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
