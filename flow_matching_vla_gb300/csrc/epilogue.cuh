@@ -118,4 +118,86 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, f
 }
 
 
+
+// ---------------------------------------------------------------------------
+// Epilogue of one thread's output pairs for a run of token columns, with the
+// per-thread invariants hoisted (the thread's weight rows n, n+1 are fixed).
+// ``lo``/``hi`` give the pair (rows n, n+1) of column m0 + 2*jj + par, where
+// the thread handles every other column starting at parity ``par`` (the lane-
+// pair swap of the tensor-core epilogue).  Used by the tensor-core kernels.
+// ---------------------------------------------------------------------------
+template <int KIND>
+struct EpiRun {
+  // Called once per thread before the column loop.
+  __device__ __forceinline__ EpiRun(const Epi& e, int n) : e_(e), n_(n) {
+    if (KIND == EPI_STORE) {
+      b0_ = e.bias ? e.bias[n] : 0.f;
+      b1_ = e.bias ? e.bias[n + 1] : 0.f;
+    } else if (KIND == EPI_ROPE) {
+      rope_ = n < e.rope_cols;
+      if (rope_) {
+        const int head = n / e.hd, i = (n % e.hd) >> 1;
+        half_ = e.hd >> 1;
+        i_ = i;
+        col0_ = head * e.hd + i;
+      }
+    }
+  }
+  // Column m (token row of the output); j = m % tok_rope maintained by the caller for RoPE.
+  __device__ __forceinline__ void operator()(int m, int j, float a0, float a1) const {
+    if (KIND == EPI_STORE) {
+      a0 += b0_;
+      a1 += b1_;
+      if (e_.act == ACT_SWISH) {
+        a0 = swishf(a0);
+        a1 = swishf(a1);
+      } else if (e_.act == ACT_GELU) {
+        a0 = gelu_tanh_fast(a0);
+        a1 = gelu_tanh_fast(a1);
+      }
+      const long long r = e_.rg ? (long long)(m / e_.rg) * e_.rs + e_.ro + m % e_.rg : (long long)m;
+      if (e_.out_f32)
+        store_pair<float>((float*)e_.out + r * e_.ldo + n_, a0, a1);
+      else
+        store_pair<bf16>((bf16*)e_.out + r * e_.ldo + n_, a0, a1);
+    } else if (KIND == EPI_ROPE) {
+      bf16* o = (bf16*)e_.out + (long long)m * e_.ldo;
+      if (rope_) {
+        const float2 cs = e_.rope_tab[j * half_ + i_];
+        o[col0_] = __float2bfloat16_rn(a0 * cs.x - a1 * cs.y);
+        o[col0_ + half_] = __float2bfloat16_rn(a1 * cs.x + a0 * cs.y);
+      } else {
+        store_pair<bf16>(o + n_, a0, a1);
+      }
+    } else if (KIND == EPI_GEGLU) {
+      ((bf16*)e_.out)[(long long)m * e_.ldo + (n_ >> 1)] = __float2bfloat16_rn(gelu_tanh_fast(a0) * a1);
+    } else {  // residual kinds
+      const EpiPre p = epi_prefetch<bf16>(e_, m, n_);
+      epi_pair<bf16>(e_, m, n_, a0, a1, p);
+    }
+  }
+  const Epi& e_;
+  int n_;
+  float b0_ = 0.f, b1_ = 0.f;
+  bool rope_ = false;
+  int half_ = 0, i_ = 0, col0_ = 0;
+};
+
+// 32 accumulator columns c0..c0+31 of rows (n, n+1) held by a lane pair; this
+// lane finishes columns of parity ``odd``.
+template <int KIND>
+__device__ __forceinline__ void epi_columns(const EpiRun<KIND>& run, const float (&v)[32], bool odd, int m_first,
+                                            int M, int tok_rope) {
+  int j = m_first % tok_rope;  // token index within its sample, for the RoPE table
+  int m = m_first;
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const float send = odd ? v[c] : v[c + 1];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+    if (m < M) run(m, j, odd ? recv : v[c], odd ? v[c + 1] : recv);
+    m += 2;
+    j += 2;
+    if (j >= tok_rope) j -= tok_rope;
+  }
+}
 }  // namespace g3

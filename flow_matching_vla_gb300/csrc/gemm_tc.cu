@@ -88,6 +88,21 @@ __device__ __forceinline__ void reduce_rows(const Epi& e, const float* __restric
   }
 }
 
+// Epilogue of accumulator columns [c_begin, c_end) of this warp's TMEM lanes.
+template <int KIND>
+__device__ __forceinline__ void tile_epilogue(const Epi& e, uint32_t taddr, int c_begin, int c_end, int m0,
+                                              int n_even, int M, int N, bool odd) {
+  const EpiRun<KIND> run(e, n_even < N ? n_even : 0);
+  const bool live = n_even < N;
+  const int tok = KIND == EPI_ROPE ? e.tok_rope : 1;
+#pragma unroll 1
+  for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+    float v[32];
+    ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+    epi_columns<KIND>(run, v, odd, m0 + c0 + (odd ? 1 : 0), live ? M : 0, tok);
+  }
+}
+
 constexpr int kThreads = 256;  // 8 warps: warp 0 TMA, warp 1 MMA, all 8 share the epilogue
 
 template <int BN, int STAGES>
@@ -226,19 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_even = n0 + (row & ~1);
     const bool odd = lane & 1;
     if (!aborted) {
-#pragma unroll 1
-      for (int c0 = c_begin; c0 < c_end; c0 += 32) {
-        float v[32];
-        ptx::tmem_ld32(taddr + (uint32_t)c0, v);
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const float send = odd ? v[j] : v[j + 1];
-          const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-          const int m = m0 + c0 + j + (odd ? 1 : 0);
-          const float a0 = odd ? recv : v[j];
-          const float a1 = odd ? v[j + 1] : recv;
-          if (m < M && n_even < N) epi_pair<bf16>(e, m, n_even, a0, a1);
-        }
+      switch (e.kind) {
+        case EPI_STORE: tile_epilogue<EPI_STORE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        case EPI_ROPE: tile_epilogue<EPI_ROPE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        case EPI_GEGLU: tile_epilogue<EPI_GEGLU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        default: tile_epilogue<EPI_RESID>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
       }
     }
   } else {
@@ -275,6 +282,197 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, BN);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Persistent variant for many tiles (large token counts): one CTA per SM walks
+// the tiles; warp 0 streams TMA stages continuously across tiles, warp 1
+// issues the MMAs into one of two TMEM accumulators (2 x BN columns), and
+// warps 2..9 drain the other accumulator through the epilogue, so the
+// epilogue of tile i overlaps the main loop of tile i + 1.  Tiles are ordered
+// token-tile fastest: concurrently running CTAs share weight tiles in L2.
+// ---------------------------------------------------------------------------
+constexpr int kPersThreads = 320;
+
+template <int BN, int STAGES>
+struct PersSmem {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int PIPE = STAGES * STAGE_BYTES;
+  static constexpr int BAR = (2 * STAGES + 4) * 8 + 16;
+  static constexpr int TOTAL = PIPE + BAR + 1024;
+};
+
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kPersThreads, 1)
+    gemm_tc_persistent(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
+                       int N, int KB, Epi e, int* err, long long wait_limit) {
+  using L = PersSmem<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::PIPE);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;   // accumulator b ready for the epilogue
+  uint64_t* tempty = tfull + 2;       // accumulator b drained by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = (M + BN - 1) / BN;
+  const int tiles = ((N + BM - 1) / BM) * mt;
+  constexpr int kEpiWarps = kPersThreads / 32 - 2;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&tfull[b], 1);
+      ptx::mbar_init(&tempty[b], kEpiWarps);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmW);
+    ptx::prefetch_tmap(&tmX);
+  }
+  if (warp == 2) ptx::tmem_alloc(tmem_slot, 2 * BN);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  ptx::pdl_launch_dependents();
+
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicExch(err, 1);
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pw = ptx::policy_evict_first(), px = ptx::policy_evict_last();
+      const int t0 = blockIdx.x;
+      const int pre = (t0 < tiles) ? (KB < STAGES ? KB : STAGES) : 0;
+      for (int i = 0; i < pre; ++i) {  // first tile's weights before the dependency wait
+        ptx::mbar_arrive_expect_tx(&full[i], L::STAGE_BYTES);
+        ptx::tma_load_2d(sA + i * A_BYTES, &tmW, &full[i], i * BK, (t0 / mt) * BM, pw);
+      }
+      ptx::pdl_wait();
+      long long it = 0, issued = pre;
+      for (int t = t0; t < tiles && !*abort_flag; t += gridDim.x) {
+        const int n0 = (t / mt) * BM, m0 = (t % mt) * BN;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          if (!(t == t0 && kb < pre)) {
+            if (it >= STAGES && !ptx::mbar_wait(&empty[s], (uint32_t)(((it / STAGES) & 1) ^ 1), wait_limit)) {
+              fail();
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
+            ptx::tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], kb * BK, n0, pw);
+            issued = it + 1;
+          }
+          ptx::tma_load_2d(sB + s * L::B_BYTES, &tmX, &full[s], kb * BK, m0, px);
+        }
+      }
+      if (*abort_flag)  // drain this thread's in-flight copies (bounded)
+        for (long long i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
+          ptx::mbar_wait(&full[i % STAGES], (uint32_t)((i / STAGES) & 1), wait_limit);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN);
+      long long it = 0;
+      int lt = 0;
+      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++lt) {
+        const int b = lt & 1;
+        if (lt >= 2 && !ptx::mbar_wait(&tempty[b], (uint32_t)(((lt >> 1) & 1) ^ 1), wait_limit)) {
+          fail();
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(b * BN);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++it) {
+          const int s = (int)(it % STAGES);
+          if (!ptx::mbar_wait(&full[s], (uint32_t)((it / STAGES) & 1), wait_limit)) {
+            fail();
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint64_t ad = ptx::sdesc_sw128(ptx::smem_u32(sA + s * A_BYTES));
+          const uint64_t bd = ptx::sdesc_sw128(ptx::smem_u32(sB + s * L::B_BYTES));
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) ptx::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
+          ptx::mma_commit(&empty[s]);
+        }
+        ptx::mma_commit(&tfull[b]);
+        if (!ok) break;
+      }
+    }
+  } else {
+    ptx::pdl_wait();
+    const int ew = warp - 2;
+    const int quad = warp & 3;
+    const int c_begin = (ew >> 2) * (BN / 2), c_end = c_begin + BN / 2;
+    const bool odd = lane & 1;
+    int lt = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+      const int b = lt & 1;
+      if (!ptx::mbar_wait(&tfull[b], (uint32_t)((lt >> 1) & 1), wait_limit)) {
+        fail();
+        break;
+      }
+      ptx::tc_fence_after();
+      if (*abort_flag) break;
+      const int n0 = (t / mt) * BM, m0 = (t % mt) * BN;
+      const int n_even = n0 + quad * 32 + (lane & ~1);
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN);
+      switch (e.kind) {
+        case EPI_STORE: tile_epilogue<EPI_STORE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        case EPI_ROPE: tile_epilogue<EPI_ROPE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        case EPI_GEGLU: tile_epilogue<EPI_GEGLU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        default: tile_epilogue<EPI_RESID>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[b]);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 2 * BN);
+  }
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_persistent(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int sm_count,
+                              int* err, long long lim, cudaStream_t s, bool pdl) {
+  using L = PersSmem<BN, STAGES>;
+  auto kern = gemm_tc_persistent<BN, STAGES>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e1 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e1 != cudaSuccess) return e1;
+    configured = true;
+  }
+  const int tiles = ((a.N + BM - 1) / BM) * ((a.M + BN - 1) / BN);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles < sm_count ? tiles : sm_count);
+  cfg.blockDim = dim3(kPersThreads);
+  cfg.dynamicSmemBytes = L::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, a.K / BK, a.epi, err, lim);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -358,6 +556,23 @@ cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs
     case 64: return launch<64, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
     case 128: return launch<128, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
     case 256: return launch<256, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace g3
+
+namespace g3 {
+
+bool tc_use_persistent(const TcPlan& p, int M) { return p.S == 1 && M > 64; }
+
+cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a,
+                                      const TcPlan& p, int sm_count, int* err, long long wait_limit,
+                                      cudaStream_t s, bool pdl) {
+  if (!tc_supported(a.M, a.N, a.K) || p.S != 1) return cudaErrorInvalidValue;
+  switch (p.BN) {
+    case 128: return launch_persistent<128, 6>(tw, tx, a, sm_count, err, wait_limit, s, pdl);
+    case 256: return launch_persistent<256, 4>(tw, tx, a, sm_count, err, wait_limit, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

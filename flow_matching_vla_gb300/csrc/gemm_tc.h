@@ -27,4 +27,11 @@ long long tc_workspace_floats(const TcPlan& p, int M, int N);
 cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
                     float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl);
 
+// Large token counts (no split, M > 64): persistent CTAs with a double-buffered
+// TMEM accumulator so each tile's epilogue overlaps the next tile's MMAs.
+bool tc_use_persistent(const TcPlan& p, int M);
+cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a,
+                                      const TcPlan& p, int sm_count, int* err, long long wait_limit,
+                                      cudaStream_t s, bool pdl);
+
 }  // namespace g3

@@ -108,6 +108,10 @@ struct AttnArgs {
 };
 cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s, bool pdl);
 
+// Tensor-core attention of the DiT head (bf16, Dh 48 or 64, <= 32 query tokens, masks).
+bool attn_dit_supported(const AttnArgs& a);
+cudaError_t attention_dit(const AttnArgs& a, cudaStream_t s, bool pdl);
+
 // Tensor-core attention of the expert family (one KV head, heads folded into rows).
 struct AttnFoldArgs {
   const void* qkv = nullptr;   // bf16 [B*H][ldq]: q heads at 0, suffix k at k_off, v at v_off

@@ -188,12 +188,94 @@ __global__ void dit_in_kernel(const float* __restrict__ x, int A, const T* __res
   }
 }
 
+// Warp per row, for many rows: the row lives in registers (D/64 float2 per
+// lane), reductions are warp shuffles, no block barriers; 8 rows per CTA.
+constexpr int kRowsPerCta = 8;
+constexpr int kMaxPairsPerLane = 32;  // D <= 2048
+
+template <typename T>
+__global__ void __launch_bounds__(256) adanorm_rows_kernel(float* __restrict__ h, int D, int M,
+                                                           T* __restrict__ out, NormArgs na) {
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const int np = D / 64;  // float2 per lane
+  float* hr = h + (long long)m * D;
+  float2 x[kMaxPairsPerLane];
+#pragma unroll
+  for (int k = 0; k < kMaxPairsPerLane; ++k)
+    if (k < np) x[k] = *reinterpret_cast<const float2*>(hr + (k * 32 + lane) * 2);
+  if (na.part) {  // h += gate * sum_s part[s] (split order), written back
+    const T* g = na.gate ? (const T*)na.gate + (long long)(m / na.tok) * na.mod_bstride : nullptr;
+    float2 acc[kMaxPairsPerLane];
+#pragma unroll
+    for (int k = 0; k < kMaxPairsPerLane; ++k) acc[k] = make_float2(0.f, 0.f);
+    for (int sp = 0; sp < na.part_S; ++sp) {
+      const float* pr = na.part + ((long long)sp * na.part_M + m) * D;
+#pragma unroll
+      for (int k = 0; k < kMaxPairsPerLane; ++k)
+        if (k < np) {
+          const float2 v = *reinterpret_cast<const float2*>(pr + (k * 32 + lane) * 2);
+          acc[k].x += v.x;
+          acc[k].y += v.y;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kMaxPairsPerLane; ++k)
+      if (k < np) {
+        const int i = (k * 32 + lane) * 2;
+        const float g0 = g ? to_f(g[i]) : 1.f, g1 = g ? to_f(g[i + 1]) : 1.f;
+        x[k].x += g0 * acc[k].x;
+        x[k].y += g1 * acc[k].y;
+        *reinterpret_cast<float2*>(hr + i) = x[k];
+      }
+  }
+  float mean = 0.f;
+  if (na.kind == NORM_LN) {
+    float sacc = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMaxPairsPerLane; ++k)
+      if (k < np) sacc += x[k].x + x[k].y;
+    mean = warp_sum(sacc) / (float)D;
+  }
+  float q = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMaxPairsPerLane; ++k)
+    if (k < np) {
+      const float a = x[k].x - mean, b = x[k].y - mean;
+      q += a * a + b * b;
+    }
+  const float r = rsqrtf(warp_sum(q) / (float)D + na.eps);
+  const T* mod = na.mod ? (const T*)na.mod + (long long)(m / na.tok) * na.mod_bstride : nullptr;
+  T* o = out + (long long)m * D;
+#pragma unroll
+  for (int k = 0; k < kMaxPairsPerLane; ++k)
+    if (k < np) {
+      const int i = (k * 32 + lane) * 2;
+      float y0 = (x[k].x - mean) * r, y1 = (x[k].y - mean) * r;
+      if (mod) {
+        y0 = y0 * (1.f + to_f(mod[na.scale_off + i])) + to_f(mod[na.shift_off + i]);
+        y1 = y1 * (1.f + to_f(mod[na.scale_off + i + 1])) + to_f(mod[na.shift_off + i + 1]);
+      }
+      o[i] = from_f<T>(y0);
+      o[i + 1] = from_f<T>(y1);
+    }
+}
+
 inline int threads_for(int D) { return D <= 512 ? 128 : 256; }
 
 }  // namespace
 
 cudaError_t adanorm(DType dt, float* h, int D, int M, void* out, NormArgs na, cudaStream_t s, bool pdl) {
   if (M <= 0) return cudaSuccess;
+  if (M > 1024 && D <= 64 * kMaxPairsPerLane) {  // many rows: warp per row
+    const int blocks = (M + kRowsPerCta - 1) / kRowsPerCta;
+    if (dt == DT_F32)
+      return launch_k(adanorm_rows_kernel<float>, blocks, 32 * kRowsPerCta, 0, s, pdl, h, D, M, (float*)out, na);
+    return launch_k(adanorm_rows_kernel<bf16>, blocks, 32 * kRowsPerCta, 0, s, pdl, h, D, M, (bf16*)out, na);
+  }
   const size_t smem = (D + 33) * sizeof(float);
   if (dt == DT_F32)
     return launch_k(adanorm_kernel<float>, M, threads_for(D), smem, s, pdl, h, D, (float*)out, na);

@@ -80,6 +80,7 @@ struct gr00t_ctx {
   long long gemm_ws_floats = 0;
   std::map<std::tuple<const void*, long long, long long, long long, int>, CUtensorMap> tmaps;
   int opt_pdl = 1;
+  int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
   int split_cap = 8;        // GEMMs that reduce their split-K partials in-kernel
   int resid_split_cap = 16; // residual GEMMs whose partials the next kernel folds in
 
@@ -393,8 +394,12 @@ int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
     const CUtensorMap* tw = tmap(c, a.W, a.N, a.K, a.ldw, 128);
     const CUtensorMap* tx = tmap(c, a.A, a.M, a.K, a.lda, p.BN);
     if (!tw || !tx) return set_err(c, GR00T_ECUDA, "TMA descriptor encode failed (alignment?)");
-    CK(c, gemm_tc(*tw, *tx, a, p, c->gemm_ws, c->gemm_ws_floats, c->err_flag, c->wait_limit, c->stream,
-                  c->opt_pdl != 0));
+    if (c->opt_persistent && tc_use_persistent(p, a.M))
+      CK(c, gemm_tc_persistent_launch(*tw, *tx, a, p, c->sm_count, c->err_flag, c->wait_limit, c->stream,
+                                      c->opt_pdl != 0));
+    else
+      CK(c, gemm_tc(*tw, *tx, a, p, c->gemm_ws, c->gemm_ws_floats, c->err_flag, c->wait_limit, c->stream,
+                    c->opt_pdl != 0));
   } else {
     CK(c, gemm_simt(c->dt, a, c->stream, c->opt_pdl != 0));
   }
@@ -596,7 +601,10 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     }
     ++c->launches;
     tmark(c, GR00T_KCLASS_ATTENTION);
-    CK(c, attention_simt(c->dt, at, s, c->opt_pdl != 0));
+    if (c->dt == DT_BF16 && c->opt_attn == 0 && attn_dit_supported(at))
+      CK(c, attention_dit(at, s, c->opt_pdl != 0));
+    else
+      CK(c, attention_simt(c->dt, at, s, c->opt_pdl != 0));
     tmark(c, GR00T_KCLASS_ATTENTION);
     GemmArgs go;
     go.A = c->att; go.lda = c->qd; go.W = c->w_o[i]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
@@ -927,6 +935,9 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
     case GR00T_OPT_WAIT_LIMIT:
       if (value < 0) return set_err(c, GR00T_EINVAL, "wait limit must be >= 0");
       c->wait_limit = value;
+      break;
+    case GR00T_OPT_PERSISTENT_GEMM:
+      c->opt_persistent = value ? 1 : 0;
       break;
     case GR00T_OPT_SPLIT_CAP:
     case GR00T_OPT_RESID_SPLIT_CAP:

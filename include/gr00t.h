@@ -272,6 +272,7 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
                                      (GR00T_KCLASS_*, 0 = off); read with gr00t_kernel_times */
 #define GR00T_OPT_SPLIT_CAP 6     /* largest split-K factor of GEMMs that reduce in-kernel (1..16, power of 2; default 8) */
 #define GR00T_OPT_RESID_SPLIT_CAP 7 /* same for residual GEMMs whose partials the next kernel folds in (default 16) */
+#define GR00T_OPT_PERSISTENT_GEMM 8 /* 1 (default): persistent tensor-core GEMM for unsplit shapes with > 64 tokens */
 int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
 
 #define GR00T_INFO_KERNELS_PER_STEP 1   /* kernel launches of one denoise step            */
