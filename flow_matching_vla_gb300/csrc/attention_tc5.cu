@@ -1,0 +1,554 @@
+// tcgen05 / TMEM attention of the action expert over prefix ++ own K/V.
+//
+// Same computation as the head-folded attention ("pi0.5 Design", Attention
+// and the K/V pool: one KV head, the Hq query heads folded into rows, all-ones
+// mask; vla.cpp Eq. (2) per row), on the 5th-generation tensor cores:
+//
+//  * a CTA owns 128 folded rows (r = t * Hq + h) and a range of 64-key tiles;
+//    the prefix tiles come from the bound per-layer K/V, the suffix tiles from
+//    this step's QKV projection;
+//  * warp 0 issues TMA: Q once through a 3-D map over [tokens][heads][Dh]
+//    whose box lands exactly in folded-row order, K and V tiles through a
+//    2-stage ring (128-byte swizzle, 64-element boxes);
+//  * warp 1 issues tcgen05.mma: S = Q K^T into one of two TMEM buffers
+//    (kind::f16, K-major operands), and O += P V into a TMEM accumulator with
+//    V read MN-major straight from its [key][dim] tile;
+//  * warps 2..5 (one thread per row, the TMEM lane) run the softmax in
+//    registers: exp2 of scaled scores against a running maximum that is only
+//    raised -- and O rescaled in TMEM -- when a tile's maximum exceeds it by
+//    more than 8 (2^8 headroom, exact arithmetic otherwise), write P (bf16)
+//    into shared memory in the MMA's swizzled K-major layout and hand it to
+//    the MMA warp;
+//  * key splits of one row tile form a cluster; partial (O, max, sum) go to
+//    the workspace and are combined after one cluster barrier in split order.
+// All mbarrier waits are bounded (error flag, drained copies, freed TMEM).
+#include <cooperative_groups.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace g3 {
+
+namespace cg = cooperative_groups;
+
+namespace {
+
+constexpr int ROWS = 128;   // folded query rows per CTA (MMA M)
+constexpr int KT = 64;      // keys per tile (MMA N of S, K of PV)
+constexpr int kThreads = 192;
+
+template <int DH>
+struct T5Smem {
+  static constexpr int BOXES = DH / 64;          // 64-element column boxes per row block
+  static constexpr int Q_BYTES = ROWS * DH * 2;
+  static constexpr int KV_BYTES = KT * DH * 2;   // one K (or V) tile
+  static constexpr int STAGE = 2 * KV_BYTES;
+  static constexpr int P_BYTES = ROWS * KT * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = Q_BYTES;
+  static constexpr int OFF_P = OFF_KV + 2 * STAGE;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int TOTAL = OFF_BAR + NBAR * 8 + 16 + 3 * ROWS * 4 + 1024;
+};
+
+// MN-major (V) descriptor: 64-element rows of 128 bytes along N in groups of 8 K-rows
+// (1024 bytes); consecutive 64-element N blocks ``lbo`` bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+      "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
+      "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
+      "[%2];" ::"r"(ptx::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Key tile i of sample b: prefix tiles first (64-key steps over [0, P)), then suffix tiles over [P, P + H).
+struct KeyTile {
+  bool prefix;
+  int row;    // first row in the prefix map ([B*P]) or the suffix map ([B*H])
+  int valid;  // keys of the tile in range
+};
+__device__ __forceinline__ KeyTile key_tile(int i, int b, int P, int H) {
+  const int np = (P + KT - 1) / KT;
+  KeyTile t;
+  if (i < np) {
+    t.prefix = true;
+    t.row = b * P + i * KT;
+    t.valid = min(KT, P - i * KT);
+  } else {
+    const int j = (i - np) * KT;
+    t.prefix = false;
+    t.row = b * H + j;
+    t.valid = min(KT, H - j);
+  }
+  return t;
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_t5_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKp,
+                   const __grid_constant__ CUtensorMap tmVp, const __grid_constant__ CUtensorMap tmKs,
+                   const __grid_constant__ CUtensorMap tmVs, AttnT5Args a) {
+  using L = T5Smem<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem + L::OFF_Q;
+  uint8_t* sKV = smem + L::OFF_KV;
+  uint8_t* sP = smem + L::OFF_P;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;    // [2]
+  uint64_t* s_empty = bars + 7;   // [2]
+  uint64_t* p_full = bars + 9;
+  uint64_t* pv_done = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sW = reinterpret_cast<float*>(tmem_slot + 4);   // combine scratch [S][RP]
+  float* sLs = sW + ROWS;
+  float* sInv = sLs + ROWS;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int S = (int)gridDim.y;
+  const int split = (int)blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  const int r0 = blockIdx.x * ROWS;
+  const int nrows = a.Hq * a.H;
+  const int ntiles = (a.P + KT - 1) / KT + (a.H + KT - 1) / KT;
+  const int tps = (ntiles + S - 1) / S;
+  const int t_begin = split * tps;
+  const int t_end = min(ntiles, t_begin + tps);
+  const int nt = t_end > t_begin ? t_end - t_begin : 0;
+  const long long lim = a.wait_limit;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&kv_full[i], 1);
+      ptx::mbar_init(&kv_empty[i], 1);
+      ptx::mbar_init(&s_full[i], 1);
+      ptx::mbar_init(&s_empty[i], 4);
+    }
+    ptx::mbar_init(p_full, 4);
+    ptx::mbar_init(pv_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmKp);
+    ptx::prefetch_tmap(&tmVp);
+    ptx::prefetch_tmap(&tmKs);
+    ptx::prefetch_tmap(&tmVs);
+  }
+  if (warp == 2) ptx::tmem_alloc(tmem_slot, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tO = tmem;              // O: DH columns
+  const uint32_t tS = tmem + 256;        // S buffers: 2 x 64 columns
+  ptx::pdl_launch_dependents();
+  auto fail = [&]() {
+    *abort_flag = 1;
+    atomicExch(a.err, 1);
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      auto load_kv = [&](int i, int st) {
+        const KeyTile kt = key_tile(t_begin + i, b, a.P, a.H);
+        uint8_t* k = sKV + st * L::STAGE;
+        uint8_t* v = k + L::KV_BYTES;
+        ptx::mbar_arrive_expect_tx(&kv_full[st], L::STAGE);
+        for (int x = 0; x < L::BOXES; ++x) {
+          if (kt.prefix) {
+            ptx::tma_load_2d(k + x * KT * 128, &tmKp, &kv_full[st], x * 64, kt.row, ptx::policy_evict_first());
+            ptx::tma_load_2d(v + x * KT * 128, &tmVp, &kv_full[st], x * 64, kt.row, ptx::policy_evict_first());
+          } else {
+            ptx::tma_load_2d(k + x * KT * 128, &tmKs, &kv_full[st], a.k_off + x * 64, kt.row, ptx::policy_evict_last());
+            ptx::tma_load_2d(v + x * KT * 128, &tmVs, &kv_full[st], a.v_off + x * 64, kt.row, ptx::policy_evict_last());
+          }
+        }
+      };
+      // bound prefix tiles do not depend on the previous kernel: stage them first
+      int pre = 0;
+      for (; pre < 2 && pre < nt; ++pre)
+        if (!key_tile(t_begin + pre, b, a.P, a.H).prefix) break;
+      for (int i = 0; i < pre; ++i) load_kv(i, i);
+      ptx::pdl_wait();
+      ptx::mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+      const int tokens_per_tile = ROWS / a.Hq;
+      for (int x = 0; x < L::BOXES; ++x)
+        tma_load_3d(sQ + x * ROWS * 128, &tmQ, q_full, x * 64, 0, b * a.H + blockIdx.x * tokens_per_tile);
+      int loaded = pre;
+      for (int i = pre; i < nt && !*abort_flag; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !ptx::mbar_wait(&kv_empty[st], ((i >> 1) & 1) ^ 1, lim)) {
+          fail();
+          break;
+        }
+        load_kv(i, st);
+        loaded = i + 1;
+      }
+      if (*abort_flag) {  // drain this thread's in-flight copies (bounded) before the CTA can exit
+        ptx::mbar_wait(q_full, 0, lim);
+        for (int i = loaded - 1; i >= 0 && i >= loaded - 2; --i) ptx::mbar_wait(&kv_full[i & 1], (i >> 1) & 1, lim);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idS = ptx::idesc_bf16(ROWS, KT);
+      constexpr uint32_t idO = ptx::idesc_bf16(ROWS, DH) | (1u << 16);   // B (V) MN-major
+      bool ok = ptx::mbar_wait(q_full, 0, lim);
+      if (!ok) fail();
+      for (int j = 0; ok && j <= nt; ++j) {
+        if (j < nt) {  // S(j) = Q K(j)^T
+          const int st = j & 1, sb = j & 1;
+          if (!ptx::mbar_wait(&kv_full[st], (j >> 1) & 1, lim)) { fail(); break; }
+          if (j >= 2 && !ptx::mbar_wait(&s_empty[sb], ((j >> 1) & 1) ^ 1, lim)) { fail(); break; }
+          ptx::tc_fence_after();
+          const uint32_t q0 = ptx::smem_u32(sQ), k0 = ptx::smem_u32(sKV + st * L::STAGE);
+#pragma unroll
+          for (int x = 0; x < L::BOXES; ++x)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              ptx::mma_bf16(tS + sb * KT, ptx::sdesc_sw128(q0 + x * ROWS * 128) + 2 * k,
+                            ptx::sdesc_sw128(k0 + x * KT * 128) + 2 * k, idS, (x | k) != 0);
+          ptx::mma_commit(&s_full[sb]);
+        }
+        if (j >= 1) {  // O += P(j-1) V(j-1)
+          const int st = (j - 1) & 1;
+          if (!ptx::mbar_wait(p_full, (j - 1) & 1, lim)) { fail(); break; }
+          ptx::tc_fence_after();
+          const uint32_t p0 = ptx::smem_u32(sP), v0 = ptx::smem_u32(sKV + st * L::STAGE + L::KV_BYTES);
+#pragma unroll
+          for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 2 K-row groups of 1024 bytes of V
+            ptx::mma_bf16(tO, ptx::sdesc_sw128(p0) + 2 * k, sdesc_sw128_mn(v0 + k * 2048, KT * 128), idO,
+                          (j - 1) > 0 || k > 0);
+          ptx::mma_commit(pv_done);
+          ptx::mma_commit(&kv_empty[st]);
+        }
+      }
+    }
+  } else {
+    // ---------------- softmax (warps 2..5: TMEM lane quadrant = warp % 4) ----------------
+    ptx::pdl_wait();
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const float sl2 = rsqrtf((float)DH) * 1.4426950408889634f;
+    float m_used = -INFINITY, l = 0.f;
+    for (int j = 0; j < nt; ++j) {
+      const int sb = j & 1;
+      if (!ptx::mbar_wait(&s_full[sb], (j >> 1) & 1, lim)) { fail(); break; }
+      ptx::tc_fence_after();
+      float sv[64];
+      {
+        float v0[32], v1[32];
+        ptx::tmem_ld32(tS + sb * KT + lane_off, v0);
+        ptx::tmem_ld32(tS + sb * KT + 32 + lane_off, v1);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sv[c] = v0[c];
+          sv[32 + c] = v1[c];
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s_empty[sb]);
+      const int valid = key_tile(t_begin + j, b, a.P, a.H).valid;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        sv[c] = c < valid ? sv[c] * sl2 : -INFINITY;
+        mt = fmaxf(mt, sv[c]);
+      }
+      // raise the running maximum only when this tile exceeds it by more than 2^8
+      const bool raise = mt > m_used + 8.f;
+      const float m_new = raise ? mt : m_used;
+      const float corr = raise ? exp2f(m_used - m_new) : 1.f;   // 0 on the first tile
+      float ps = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = exp2f(sv[c] - m_new), p1 = exp2f(sv[c + 1] - m_new);
+        ps += p0 + p1;
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      l = l * corr + ps;
+      // P and O are in use by the previous PV until it completes
+      if (j >= 1 && !ptx::mbar_wait(pv_done, (j - 1) & 1, lim)) { fail(); break; }
+      ptx::tc_fence_after();
+      if (j >= 1 && __any_sync(0xffffffffu, raise)) {  // rescale this warp's O rows in TMEM
+#pragma unroll 1
+        for (int c0 = 0; c0 < DH; c0 += 32) {
+          float o[32];
+          ptx::tmem_ld32(tO + c0 + lane_off, o);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] *= corr;
+          tmem_st32(tO + c0 + lane_off, o);
+        }
+      }
+      m_used = m_new;
+      // P row -> shared memory, K-major 128-byte swizzled (16-byte chunk c at c ^ (row % 8))
+      uint4* prow = reinterpret_cast<uint4*>(sP + row * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        prow[c ^ (row & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(p_full);
+    }
+    // the last PV
+    if (nt > 0 && !*abort_flag && !ptx::mbar_wait(pv_done, (nt - 1) & 1, lim)) fail();
+    ptx::tc_fence_after();
+    // l over the row is complete in-thread (one thread per row)
+    const int gr = r0 + row;
+    const bool aborted = *abort_flag != 0;
+    if (S == 1) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const int t = gr / a.Hq, h = gr % a.Hq;
+      bf16* orow = (bf16*)a.out + ((long long)b * a.H + t) * a.ldo + h * DH;
+#pragma unroll 1
+      for (int c0 = 0; c0 < DH; c0 += 32) {
+        float o[32];
+        if (nt > 0 && !aborted) {
+          ptx::tmem_ld32(tO + c0 + lane_off, o);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0.f;
+        }
+        if (gr < nrows) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 8) {
+            uint4 w;
+            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(o[c + 2 * q] * inv, o[c + 2 * q + 1] * inv);
+              wp[q] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(orow + c0 + c) = w;
+          }
+        }
+      }
+    } else {
+      // partial (O unnormalised, running max, sum) of this split -> workspace
+      const long long tile = (long long)b * gridDim.x + blockIdx.x;
+      constexpr int PART = ROWS * DH + 2 * ROWS;
+      float* my = a.ws + (tile * S + split) * PART;
+#pragma unroll 1
+      for (int c0 = 0; c0 < DH; c0 += 32) {
+        float o[32];
+        if (nt > 0 && !aborted) {
+          ptx::tmem_ld32(tO + c0 + lane_off, o);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0.f;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+          *reinterpret_cast<float4*>(my + row * DH + c0 + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+      }
+      my[ROWS * DH + row] = nt > 0 ? m_used : -INFINITY;
+      my[ROWS * DH + ROWS + row] = l;
+    }
+  }
+
+  // ---------------- combine the key splits ----------------
+  if (S > 1) {
+    cluster.sync();
+    const long long tile = (long long)b * gridDim.x + blockIdx.x;
+    constexpr int PART = ROWS * DH + 2 * ROWS;
+    const float* base = a.ws + tile * S * PART;
+    const int RP = ROWS / S;
+    const int tid = threadIdx.x;
+    if (tid < S * RP) {
+      const int sp = tid / RP, rr = split * RP + tid % RP;
+      sW[tid] = base[sp * PART + ROWS * DH + rr];
+      sLs[tid] = base[sp * PART + ROWS * DH + ROWS + rr];
+    }
+    __syncthreads();
+    if (tid < RP) {
+      float mx = -INFINITY;
+      for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, sW[sp * RP + tid]);
+      float lsum = 0.f;
+      for (int sp = 0; sp < S; ++sp) {
+        const float ms = sW[sp * RP + tid];
+        const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
+        lsum += w * sLs[sp * RP + tid];
+        sW[sp * RP + tid] = w;
+      }
+      sInv[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
+    }
+    __syncthreads();
+    const int items = RP * (DH / 4);
+    for (int it = tid; it < items; it += kThreads) {
+      const int lr = it / (DH / 4), col = (it % (DH / 4)) * 4;
+      const int gr = r0 + split * RP + lr;
+      if (gr >= nrows) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 v[16];
+#pragma unroll
+      for (int sp = 0; sp < 16; ++sp)
+        if (sp < S) v[sp] = *reinterpret_cast<const float4*>(base + sp * PART + (split * RP + lr) * DH + col);
+#pragma unroll
+      for (int sp = 0; sp < 16; ++sp)
+        if (sp < S) {
+          const float w = sW[sp * RP + lr];
+          acc.x += w * v[sp].x;
+          acc.y += w * v[sp].y;
+          acc.z += w * v[sp].z;
+          acc.w += w * v[sp].w;
+        }
+      const float inv = sInv[lr];
+      const int t = gr / a.Hq, h = gr % a.Hq;
+      bf16* o = (bf16*)a.out + ((long long)b * a.H + t) * a.ldo + h * DH + col;
+      *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DH>
+cudaError_t launch_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl) {
+  using L = T5Smem<DH>;
+  auto kern = attn_t5_kernel<DH>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.Hq * a.H + ROWS - 1) / ROWS, S, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = S;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode5 = nullptr;
+
+cudaError_t encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                   const cuuint32_t* box) {
+  if (!g_encode5) {
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&g_encode5, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode5) return cudaErrorNotSupported;
+  }
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode5(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool attn_t5_supported(int Dh, int Hq) { return (Dh == 64 || Dh == 128 || Dh == 256) && Hq > 0 && ROWS % Hq == 0; }
+
+int attn_t5_splits(const AttnT5Args& a, int sm_count) {
+  const int tiles = (a.Hq * a.H + ROWS - 1) / ROWS * a.B;
+  const int ntiles = (a.P + KT - 1) / KT + (a.H + KT - 1) / KT;
+  int S = 1;
+  while (S < 16 && tiles * S * 2 <= sm_count && ntiles >= 2 * S) S *= 2;
+  return S;
+}
+
+long long attn_t5_workspace_floats(const AttnT5Args& a, int S) {
+  if (S == 1) return 0;
+  const long long tiles = (long long)(a.Hq * a.H + ROWS - 1) / ROWS * a.B;
+  return tiles * S * ((long long)ROWS * a.Dh + 2 * ROWS);
+}
+
+// maps: [0] Q (3-D over [B*H tokens][Hq][Dh] inside qkv), [1] prefix K, [2] prefix V ([B*P][Dh]),
+//       [3] suffix K, [4] suffix V (2-D over qkv [B*H][ldq]; x offsets k_off / v_off)
+cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, CUtensorMap* maps) {
+  const int D = a.Dh;
+  const cuuint64_t qd[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.H};
+  const cuuint64_t qs[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.ldq * 2};
+  const cuuint32_t qb[3] = {64, (cuuint32_t)a.Hq, (cuuint32_t)(ROWS / a.Hq)};
+  cudaError_t e = encode(&maps[0], a.qkv, 3, qd, qs, qb);
+  if (e != cudaSuccess) return e;
+  const cuuint32_t kb[2] = {64, KT};
+  const long long prow = (long long)a.B * (a.P > 0 ? a.P : 1);
+  const cuuint64_t pd[2] = {(cuuint64_t)D, (cuuint64_t)prow};
+  const cuuint64_t ps[1] = {(cuuint64_t)D * 2};
+  // with no prefix the prefix maps are never used: point them at the suffix rows
+  e = encode(&maps[1], a.P > 0 ? kp : a.qkv, 2, pd, ps, kb);
+  if (e != cudaSuccess) return e;
+  e = encode(&maps[2], a.P > 0 ? vp : a.qkv, 2, pd, ps, kb);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t sd[2] = {(cuuint64_t)a.ldq, (cuuint64_t)a.B * a.H};
+  const cuuint64_t ss[1] = {(cuuint64_t)a.ldq * 2};
+  e = encode(&maps[3], a.qkv, 2, sd, ss, kb);
+  if (e != cudaSuccess) return e;
+  return encode(&maps[4], a.qkv, 2, sd, ss, kb);
+}
+
+cudaError_t attention_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl) {
+  if (a.B <= 0 || a.Hq * a.H <= 0) return cudaSuccess;
+  if (!attn_t5_supported(a.Dh, a.Hq) || S < 1 || S > 16 || (S & (S - 1))) return cudaErrorInvalidValue;
+  if (attn_t5_workspace_floats(a, S) > a.ws_floats) return cudaErrorInvalidValue;
+  switch (a.Dh) {
+    case 64: return launch_t5<64>(a, maps, S, s, pdl);
+    case 128: return launch_t5<128>(a, maps, S, s, pdl);
+    case 256: return launch_t5<256>(a, maps, S, s, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace g3

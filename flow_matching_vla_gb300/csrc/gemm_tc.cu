@@ -105,10 +105,25 @@ __device__ __forceinline__ void tile_epilogue(const Epi& e, uint32_t taddr, int 
 
 constexpr int kThreads = 256;  // 8 warps: warp 0 TMA, warp 1 MMA, all 8 share the epilogue
 
+// Memory later kernels read, to be pulled into L2 while this kernel runs.
+struct L2Ahead {
+  const void* p[3];
+  long long bytes[3];
+};
+inline L2Ahead l2_ahead(const GemmArgs& a) {
+  L2Ahead r;
+  for (int i = 0; i < 3; ++i) {
+    r.p[i] = a.l2[i].p;
+    r.bytes[i] = a.l2[i].bytes;
+  }
+  return r;
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
-                   int N, int kb_per_split, Epi e, float* __restrict__ ws, int* err, long long wait_limit) {
+                   int N, int kb_per_split, Epi e, float* __restrict__ ws, int* err, long long wait_limit,
+                   L2Ahead ahead) {
   using L = TcSmem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -139,6 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmW);
     ptx::prefetch_tmap(&tmX);
   }
+  if (threadIdx.x == 32)
+    for (int i = 0; i < 3; ++i) ptx::prefetch_l2_slice(ahead.p[i], ahead.bytes[i]);
   if (warp == 2) ptx::tmem_alloc(tmem_slot, BN);
   ptx::tc_fence_before();
   __syncthreads();
@@ -505,7 +522,7 @@ cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs&
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const int KB = a.K / BK;
-  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim);
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim, l2_ahead(a));
 }
 
 }  // namespace

@@ -50,6 +50,12 @@ struct GemmArgs {
   int ldw = 0;
   int M = 0, N = 0, K = 0;
   Epi epi;
+  // optional L2 prefetch of memory later kernels read (e.g. the next layer's
+  // weights), spread over the CTAs and issued before the dependency wait
+  struct Prefetch {
+    const void* p = nullptr;
+    long long bytes = 0;
+  } l2[3];
 };
 
 // CUDA-core GEMM (any shape with N even).
@@ -128,6 +134,28 @@ bool attn_fold_supported(int Dh);
 long long attn_fold_workspace_floats(const AttnFoldArgs& a, int S);
 int attn_fold_splits(const AttnFoldArgs& a, int sm_count);
 cudaError_t attention_fold(const AttnFoldArgs& a, int S, cudaStream_t s, bool pdl);
+
+// tcgen05 / TMEM attention of the expert family (same computation as attention_fold).
+struct AttnT5Args {
+  const void* qkv = nullptr;  // bf16 [B*H][ldq]
+  int ldq = 0, k_off = 0, v_off = 0;
+  int B = 0, H = 0, Hq = 0, Dh = 0, P = 0;
+  void* out = nullptr;        // bf16 [B*H][ldo]
+  int ldo = 0;
+  float* ws = nullptr;        // split partials (L2-resident scratch)
+  long long ws_floats = 0;
+  int* err = nullptr;         // device error word (bounded waits)
+  long long wait_limit = 0;
+};
+}  // namespace g3
+#include <cuda.h>
+namespace g3 {
+bool attn_t5_supported(int Dh, int Hq);
+int attn_t5_splits(const AttnT5Args& a, int sm_count);
+long long attn_t5_workspace_floats(const AttnT5Args& a, int S);
+// maps[5]: Q, prefix K, prefix V, suffix K, suffix V
+cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, CUtensorMap* maps);
+cudaError_t attention_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl);
 
 // ---- schedule / bind / create helpers --------------------------------------------
 // temb[k*B + b][E] (activation dtype) of tau_k; dts[k] = tau_{k+1} - tau_k.

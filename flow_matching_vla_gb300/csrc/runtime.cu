@@ -81,6 +81,7 @@ struct gr00t_ctx {
   std::map<std::tuple<const void*, long long, long long, long long, int>, CUtensorMap> tmaps;
   int opt_pdl = 1;
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
+  int opt_l2_ahead = 0;     // each layer's first GEMM prefetches the next layer into L2 (off: measured slower)
   int split_cap = 8;        // GEMMs that reduce their split-K partials in-kernel
   int resid_split_cap = 16; // residual GEMMs whose partials the next kernel folds in
 
@@ -481,11 +482,35 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       g.epi.kind = EPI_ROPE; g.epi.out = c->qkv; g.epi.ldo = nq;
       g.epi.rope_cols = (c->Hq + 1) * c->Dh; g.epi.hd = c->Dh; g.epi.rope_tab = c->rope_tab;
       g.epi.tok_rope = tok;
+      if (c->opt_l2_ahead) {  // pull the next layer's weights and prefix K/V into L2 meanwhile
+        const int ln = (l + 1) % L;
+        g.l2[0].p = c->w_qkv[ln];
+        g.l2[0].bytes = ((const char*)c->w_down[ln] + (size_t)D * c->F * es) - (const char*)c->w_qkv[ln];
+        if (P > 0) {
+          g.l2[1].p = c->host_table[2 * ln];
+          g.l2[1].bytes = (long long)B * P * c->Dh * es;
+          g.l2[2].p = c->host_table[2 * ln + 1];
+          g.l2[2].bytes = g.l2[1].bytes;
+        }
+      }
       RC(gemm(c, g, GR00T_KCLASS_QKV_GEMM));
 
       ++c->launches;
       tmark(c, GR00T_KCLASS_ATTENTION);
-      if (c->dt == DT_BF16 && c->opt_attn == 0 && attn_fold_supported(c->Dh)) {
+      // tcgen05 attention once there are enough 128-row tiles; below that the
+      // 64-row mma.sync kernel spreads the work over more SMs
+      const bool big_attn = (long long)B * ((c->Hq * H + 127) / 128) >= 8;
+      if (c->dt == DT_BF16 && c->opt_attn == 0 && big_attn && attn_t5_supported(c->Dh, c->Hq)) {
+        AttnT5Args a5;
+        a5.qkv = c->qkv; a5.ldq = nq; a5.k_off = c->qd; a5.v_off = c->qd + c->Dh;
+        a5.B = B; a5.H = H; a5.Hq = c->Hq; a5.Dh = c->Dh; a5.P = P;
+        a5.out = c->att; a5.ldo = c->qd;
+        a5.ws = c->gemm_ws; a5.ws_floats = c->gemm_ws_floats;
+        a5.err = c->err_flag; a5.wait_limit = c->wait_limit;
+        CUtensorMap maps[5];
+        CK(c, attn_t5_maps(a5, c->host_table[2 * l], c->host_table[2 * l + 1], maps));
+        CK(c, attention_t5(a5, maps, attn_t5_splits(a5, c->sm_count), s, c->opt_pdl != 0));
+      } else if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 2) && attn_fold_supported(c->Dh)) {
         AttnFoldArgs af;
         af.qkv = c->qkv; af.ldq = nq; af.k_off = c->qd; af.v_off = c->qd + c->Dh;
         af.B = B; af.H = H; af.Hq = c->Hq; af.Dh = c->Dh; af.P = P;
@@ -816,7 +841,7 @@ extern "C" int gr00t_bind_prefix_kv(gr00t_ctx* c, int batch, int prefix, const v
   CK(c, cudaMemcpyAsync(c->table, t.data(), t.size() * sizeof(void*), cudaMemcpyHostToDevice, c->stream));
   if (!dit) CK(c, rope_table(prefix, c->H, c->Dh, c->g.rope_theta, c->rope_tab, c->stream));
   // masks / state are read through host_table at capture (slot presence, state pointer)
-  const bool layout_change = c->bB != batch || c->bP != prefix ||
+  const bool layout_change = c->bB != batch || c->bP != prefix || t != c->host_table ||
                              (c->host_table[2 * c->L] == nullptr) != (text_mask == nullptr) ||
                              (c->host_table[2 * c->L + 1] == nullptr) != (image_mask == nullptr) ||
                              c->host_table[2 * c->L + 2] != state_tokens;
@@ -929,7 +954,7 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
       c->opt_gemm = (int)value;
       break;
     case GR00T_OPT_ATTN_PATH:
-      if (value != 0 && value != 1) return set_err(c, GR00T_EINVAL, "attention path must be 0 or 1");
+      if (value < 0 || value > 2) return set_err(c, GR00T_EINVAL, "attention path must be 0, 1 or 2");
       c->opt_attn = (int)value;
       break;
     case GR00T_OPT_WAIT_LIMIT:
@@ -938,6 +963,9 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
       break;
     case GR00T_OPT_PERSISTENT_GEMM:
       c->opt_persistent = value ? 1 : 0;
+      break;
+    case GR00T_OPT_L2_PREFETCH:
+      c->opt_l2_ahead = value ? 1 : 0;
       break;
     case GR00T_OPT_SPLIT_CAP:
     case GR00T_OPT_RESID_SPLIT_CAP:
@@ -1017,10 +1045,10 @@ extern "C" int gr00t_kernel_times(gr00t_ctx* c, float* ms, int max, int* count) 
 // ---- allocation-free step ------------------------------------------------------
 //
 // Scratch of gr00t_denoise_step_noalloc: a fixed array in the library's device
-// image, 8 MiB of fp32 on every GPU that loads the library, held until the
+// image, 12 MiB of fp32 on every GPU that loads the library, held until the
 // process exits.  Host code cannot use the symbol itself as a device address;
 // its device address is looked up once per device with that device current.
-#define G3_NOALLOC_SCRATCH_FLOATS (1 << 21)
+#define G3_NOALLOC_SCRATCH_FLOATS (3 << 20)
 static __device__ __align__(256) float g_noalloc_scratch[G3_NOALLOC_SCRATCH_FLOATS];
 
 namespace {
@@ -1074,7 +1102,12 @@ long long step_scratch(gr00t_ctx* c, long long cap) {
   take(gemm_scratch(c, M, D, c->qd, true, cap));
   take(gemm_scratch(c, M, up_rows, D, false, cap));
   take(gemm_scratch(c, M, D, c->F, true, cap));
-  if (c->dt == DT_BF16 && c->opt_attn == 0 && attn_fold_supported(c->Dh)) {
+  if (c->dt == DT_BF16 && c->opt_attn == 0 && (long long)B * ((c->Hq * c->H + 127) / 128) >= 8 &&
+      attn_t5_supported(c->Dh, c->Hq)) {
+    AttnT5Args a5;
+    a5.B = B; a5.H = c->H; a5.Hq = c->Hq; a5.Dh = c->Dh; a5.P = c->bP;
+    take(attn_t5_workspace_floats(a5, attn_t5_splits(a5, c->sm_count)));
+  } else if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 2) && attn_fold_supported(c->Dh)) {
     AttnFoldArgs af;
     af.B = B; af.H = c->H; af.Hq = c->Hq; af.Dh = c->Dh; af.P = c->bP;
     take(attn_fold_workspace_floats(af, attn_fold_splits(af, c->sm_count)));

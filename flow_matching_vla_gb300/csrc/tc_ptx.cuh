@@ -69,6 +69,27 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// Hint the L2 to fetch [p, p + bytes) (bytes a multiple of 16, p 16-byte aligned); no completion.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
+// Spread an L2 prefetch of [p, p + bytes) over the CTAs of the grid (one thread per CTA calls it).
+__device__ __forceinline__ void prefetch_l2_slice(const void* p, long long bytes) {
+  if (!p || bytes <= 0) return;
+  const long long ctas = (long long)gridDim.x * gridDim.y * gridDim.z;
+  const long long cta = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+  long long per = (bytes + ctas - 1) / ctas;
+  per = (per + 15) & ~15LL;
+  long long b0 = cta * per, b1 = b0 + per;
+  if (b1 > bytes) b1 = bytes & ~15LL;
+  for (long long o = b0; o < b1; o += 65536) {
+    const long long n = (b1 - o) < 65536 ? (b1 - o) : 65536;
+    prefetch_l2(static_cast<const char*>(p) + o, (uint32_t)n);
+  }
+}
+
 // ---- tensor memory and tcgen05 -----------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),

@@ -174,8 +174,8 @@ int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, void* stream, 
  * every layer, keys already rotated by RoPE at positions 0..prefix-1.  DIT:
  * even layers only (odd entries ignored, may be NULL).  The memory is
  * BORROWED: the caller keeps it alive and unchanged until the next bind or
- * gr00t_destroy.  The pointers land in a device-side table, so a rebind at
- * the same (batch, prefix) reuses the captured graph.
+ * gr00t_destroy.  Rebinding new pointers re-captures the loop's CUDA graph on
+ * the next gr00t_denoise (its TMA descriptors embed the K/V addresses).
  *
  * ``text_mask``/``image_mask``: DIT only, DEVICE uint8 [batch, prefix],
  * 1 = visible; block i reads the text mask when i % 4 == 0 and the image
@@ -240,7 +240,7 @@ int gr00t_denoise_step(gr00t_ctx* ctx, int k, const float* x_in, float* v_out);
  * memory of its own.  This call never calls cudaMalloc, cudaFree or any other
  * allocating routine; the scratch that the tensor-core GEMMs (split-K
  * partials) and the attention (per-split partials) need comes from a fixed
- * array compiled into the library: 8 MiB of fp32 (2^21 floats) in the device
+ * array compiled into the library: 12 MiB of fp32 (3 * 2^20 floats) in the device
  * image of every GPU that loads the library, held until the process exits.
  *
  * Same arguments, inputs, outputs and results as gr00t_denoise_step.
@@ -267,12 +267,15 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
 #define GR00T_OPT_USE_GRAPH 1     /* 1 (default): replay the loop as a CUDA graph */
 #define GR00T_OPT_GEMM_PATH 2     /* 0: tensor-core path where supported (default), 1: CUDA-core path */
 #define GR00T_OPT_WAIT_LIMIT 3    /* spin-wait iteration limit of bounded device waits (>= 0) */
-#define GR00T_OPT_ATTN_PATH 4     /* 0: tensor-core attention where supported (default), 1: CUDA-core */
+#define GR00T_OPT_ATTN_PATH 4     /* 0: fastest tensor-core attention (default), 1: CUDA-core,
+                                     2: mma.sync head-folded kernel (expert family) */
 #define GR00T_OPT_TIME_KERNEL 5   /* bracket every launch of one kernel class with timing events
                                      (GR00T_KCLASS_*, 0 = off); read with gr00t_kernel_times */
 #define GR00T_OPT_SPLIT_CAP 6     /* largest split-K factor of GEMMs that reduce in-kernel (1..16, power of 2; default 8) */
 #define GR00T_OPT_RESID_SPLIT_CAP 7 /* same for residual GEMMs whose partials the next kernel folds in (default 16) */
 #define GR00T_OPT_PERSISTENT_GEMM 8 /* 1 (default): persistent tensor-core GEMM for unsplit shapes with > 64 tokens */
+#define GR00T_OPT_L2_PREFETCH 9   /* 1: each layer's first GEMM prefetches the next layer's weights (default 0)
+                                     and prefix K/V into L2 */
 int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
 
 #define GR00T_INFO_KERNELS_PER_STEP 1   /* kernel launches of one denoise step            */
