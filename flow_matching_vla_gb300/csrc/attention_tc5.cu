@@ -7,9 +7,10 @@
 //  * a CTA owns 128 folded rows (r = t * Hq + h) and a range of 64-key tiles;
 //    the prefix tiles come from the bound per-layer K/V, the suffix tiles from
 //    this step's QKV projection;
-//  * warp 0 issues TMA: Q once through a 3-D map over [tokens][heads][Dh]
-//    whose box lands exactly in folded-row order, K and V tiles through a
-//    2-stage ring (128-byte swizzle, 64-element boxes);
+//  * warps 0 and 6 issue TMA: Q once through a 3-D map over [tokens][heads][Dh]
+//    whose box lands exactly in folded-row order; K and V tiles through
+//    separate 2-slot rings (128-byte swizzle, 64-element boxes), a K slot
+//    freed as soon as S = QK^T read it, a V slot when P V did;
 //  * warp 1 issues tcgen05.mma: S = Q K^T into one of two TMEM buffers
 //    (kind::f16, K-major operands), and O += P V into a TMEM accumulator with
 //    V read MN-major straight from its [key][dim] tile;
@@ -38,20 +39,20 @@ namespace {
 
 constexpr int ROWS = 128;   // folded query rows per CTA (MMA M)
 constexpr int KT = 64;      // keys per tile (MMA N of S, K of PV)
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;   // warp 0: K loads, 1: MMA, 2..5: softmax, 6: V loads
 
 template <int DH>
 struct T5Smem {
   static constexpr int BOXES = DH / 64;          // 64-element column boxes per row block
   static constexpr int Q_BYTES = ROWS * DH * 2;
   static constexpr int KV_BYTES = KT * DH * 2;   // one K (or V) tile
-  static constexpr int STAGE = 2 * KV_BYTES;
-  static constexpr int P_BYTES = ROWS * KT * 2;
+  static constexpr int STAGE = 2 * KV_BYTES;     // K tile then V tile of one ring slot
+  static constexpr int P_BYTES = ROWS * KT * 2;   // one of two P buffers
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = Q_BYTES;
   static constexpr int OFF_P = OFF_KV + 2 * STAGE;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 1 + 1;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2;
   static constexpr int TOTAL = OFF_BAR + NBAR * 8 + 16 + 3 * ROWS * 4 + 1024;
 };
 
@@ -126,12 +127,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sP = smem + L::OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* k_full = bars + 1;    // [2] K tile of ring slot landed
+  uint64_t* k_empty = bars + 3;   // [2] S = QK^T read it
   uint64_t* s_full = bars + 5;    // [2]
   uint64_t* s_empty = bars + 7;   // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* pv_done = bars + 10;
+  uint64_t* p_full = bars + 9;    // [2] P buffer b written
+  uint64_t* pv_done = bars + 11;  // [2] the PV reading P buffer b completed
+  uint64_t* v_full = bars + 13;   // [2] V tile of ring slot landed
+  uint64_t* v_empty = bars + 15;  // [2] PV read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sW = reinterpret_cast<float*>(tmem_slot + 4);   // combine scratch [S][RP]
@@ -155,13 +158,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&kv_full[i], 1);
-      ptx::mbar_init(&kv_empty[i], 1);
+      ptx::mbar_init(&k_full[i], 1);
+      ptx::mbar_init(&k_empty[i], 1);
+      ptx::mbar_init(&v_full[i], 1);
+      ptx::mbar_init(&v_empty[i], 1);
       ptx::mbar_init(&s_full[i], 1);
       ptx::mbar_init(&s_empty[i], 4);
     }
-    ptx::mbar_init(p_full, 4);
-    ptx::mbar_init(pv_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&p_full[i], 4);
+      ptx::mbar_init(&pv_done[i], 1);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmQ);
@@ -183,47 +190,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicExch(a.err, 1);
   };
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == 6) {
+    // ---------------- TMA producers: warp 0 streams K tiles, warp 6 V tiles ----------------
     if (lane == 0) {
-      auto load_kv = [&](int i, int st) {
+      const bool is_k = warp == 0;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      auto load = [&](int i, int st) {
         const KeyTile kt = key_tile(t_begin + i, b, a.P, a.H);
-        uint8_t* k = sKV + st * L::STAGE;
-        uint8_t* v = k + L::KV_BYTES;
-        ptx::mbar_arrive_expect_tx(&kv_full[st], L::STAGE);
+        uint8_t* dst = sKV + st * L::STAGE + (is_k ? 0 : L::KV_BYTES);
+        ptx::mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
         for (int x = 0; x < L::BOXES; ++x) {
-          if (kt.prefix) {
-            ptx::tma_load_2d(k + x * KT * 128, &tmKp, &kv_full[st], x * 64, kt.row, ptx::policy_evict_first());
-            ptx::tma_load_2d(v + x * KT * 128, &tmVp, &kv_full[st], x * 64, kt.row, ptx::policy_evict_first());
-          } else {
-            ptx::tma_load_2d(k + x * KT * 128, &tmKs, &kv_full[st], a.k_off + x * 64, kt.row, ptx::policy_evict_last());
-            ptx::tma_load_2d(v + x * KT * 128, &tmVs, &kv_full[st], a.v_off + x * 64, kt.row, ptx::policy_evict_last());
-          }
+          if (kt.prefix)
+            ptx::tma_load_2d(dst + x * KT * 128, is_k ? &tmKp : &tmVp, &full[st], x * 64, kt.row,
+                             ptx::policy_evict_first());
+          else
+            ptx::tma_load_2d(dst + x * KT * 128, is_k ? &tmKs : &tmVs, &full[st], (is_k ? a.k_off : a.v_off) + x * 64,
+                             kt.row, ptx::policy_evict_last());
         }
       };
       // bound prefix tiles do not depend on the previous kernel: stage them first
       int pre = 0;
       for (; pre < 2 && pre < nt; ++pre)
         if (!key_tile(t_begin + pre, b, a.P, a.H).prefix) break;
-      for (int i = 0; i < pre; ++i) load_kv(i, i);
+      for (int i = 0; i < pre; ++i) load(i, i);
       ptx::pdl_wait();
-      ptx::mbar_arrive_expect_tx(q_full, L::Q_BYTES);
-      const int tokens_per_tile = ROWS / a.Hq;
-      for (int x = 0; x < L::BOXES; ++x)
-        tma_load_3d(sQ + x * ROWS * 128, &tmQ, q_full, x * 64, 0, b * a.H + blockIdx.x * tokens_per_tile);
+      if (is_k) {
+        ptx::mbar_arrive_expect_tx(q_full, L::Q_BYTES);
+        const int tokens_per_tile = ROWS / a.Hq;
+        for (int x = 0; x < L::BOXES; ++x)
+          tma_load_3d(sQ + x * ROWS * 128, &tmQ, q_full, x * 64, 0, b * a.H + blockIdx.x * tokens_per_tile);
+      }
       int loaded = pre;
       for (int i = pre; i < nt && !*abort_flag; ++i) {
         const int st = i & 1;
-        if (i >= 2 && !ptx::mbar_wait(&kv_empty[st], ((i >> 1) & 1) ^ 1, lim)) {
+        if (i >= 2 && !ptx::mbar_wait(&empty[st], ((i >> 1) & 1) ^ 1, lim)) {
           fail();
           break;
         }
-        load_kv(i, st);
+        load(i, st);
         loaded = i + 1;
       }
       if (*abort_flag) {  // drain this thread's in-flight copies (bounded) before the CTA can exit
-        ptx::mbar_wait(q_full, 0, lim);
-        for (int i = loaded - 1; i >= 0 && i >= loaded - 2; --i) ptx::mbar_wait(&kv_full[i & 1], (i >> 1) & 1, lim);
+        if (is_k) ptx::mbar_wait(q_full, 0, lim);
+        for (int i = loaded - 1; i >= 0 && i >= loaded - 2; --i) ptx::mbar_wait(&full[i & 1], (i >> 1) & 1, lim);
       }
     }
   } else if (warp == 1) {
@@ -236,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j <= nt; ++j) {
         if (j < nt) {  // S(j) = Q K(j)^T
           const int st = j & 1, sb = j & 1;
-          if (!ptx::mbar_wait(&kv_full[st], (j >> 1) & 1, lim)) { fail(); break; }
+          if (!ptx::mbar_wait(&k_full[st], (j >> 1) & 1, lim)) { fail(); break; }
           if (j >= 2 && !ptx::mbar_wait(&s_empty[sb], ((j >> 1) & 1) ^ 1, lim)) { fail(); break; }
           ptx::tc_fence_after();
           const uint32_t q0 = ptx::smem_u32(sQ), k0 = ptx::smem_u32(sKV + st * L::STAGE);
@@ -247,18 +257,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::mma_bf16(tS + sb * KT, ptx::sdesc_sw128(q0 + x * ROWS * 128) + 2 * k,
                             ptx::sdesc_sw128(k0 + x * KT * 128) + 2 * k, idS, (x | k) != 0);
           ptx::mma_commit(&s_full[sb]);
+          ptx::mma_commit(&k_empty[st]);
         }
         if (j >= 1) {  // O += P(j-1) V(j-1)
-          const int st = (j - 1) & 1;
-          if (!ptx::mbar_wait(p_full, (j - 1) & 1, lim)) { fail(); break; }
+          const int st = (j - 1) & 1, pb = (j - 1) & 1;
+          if (!ptx::mbar_wait(&p_full[pb], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
+          if (!ptx::mbar_wait(&v_full[st], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
           ptx::tc_fence_after();
-          const uint32_t p0 = ptx::smem_u32(sP), v0 = ptx::smem_u32(sKV + st * L::STAGE + L::KV_BYTES);
+          const uint32_t p0 = ptx::smem_u32(sP + pb * L::P_BYTES);
+          const uint32_t v0 = ptx::smem_u32(sKV + st * L::STAGE + L::KV_BYTES);
 #pragma unroll
           for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 2 K-row groups of 1024 bytes of V
             ptx::mma_bf16(tO, ptx::sdesc_sw128(p0) + 2 * k, sdesc_sw128_mn(v0 + k * 2048, KT * 128), idO,
                           (j - 1) > 0 || k > 0);
-          ptx::mma_commit(pv_done);
-          ptx::mma_commit(&kv_empty[st]);
+          ptx::mma_commit(&pv_done[pb]);
+          ptx::mma_commit(&v_empty[st]);
         }
       }
     }
@@ -289,30 +302,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s_empty[sb]);
       const int valid = key_tile(t_begin + j, b, a.P, a.H).valid;
-      float mt = -INFINITY;
+      // tile maximum of the raw scores (4 independent chains); keys past the tile end masked
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        sv[c] = c < valid ? sv[c] * sl2 : -INFINITY;
-        mt = fmaxf(mt, sv[c]);
+        if (c >= valid) sv[c] = -INFINITY;
+        mq[c & 3] = fmaxf(mq[c & 3], sv[c]);
       }
+      const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
       // raise the running maximum only when this tile exceeds it by more than 2^8
       const bool raise = mt > m_used + 8.f;
       const float m_new = raise ? mt : m_used;
-      const float corr = raise ? exp2f(m_used - m_new) : 1.f;   // 0 on the first tile
-      float ps = 0.f;
+      const float corr = raise ? ex2_approx(m_used - m_new) : 1.f;   // 0 on the first tile
+      float pq[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float p0 = exp2f(sv[c] - m_new), p1 = exp2f(sv[c + 1] - m_new);
-        ps += p0 + p1;
+        // p = 2^(s * log2e / sqrt(d) - m): the scale folded into one fma
+        const float p0 = ex2_approx(fmaf(sv[c], sl2, -m_new));
+        const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, -m_new));
+        pq[(c >> 1) & 3] += p0 + p1;
         __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
         pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h2);
       }
+      const float ps = (pq[0] + pq[1]) + (pq[2] + pq[3]);
       l = l * corr + ps;
-      // P and O are in use by the previous PV until it completes
-      if (j >= 1 && !ptx::mbar_wait(pv_done, (j - 1) & 1, lim)) { fail(); break; }
+      const int pb = j & 1;
+      // P buffer pb is free once PV(j-2) has completed
+      if (j >= 2 && !ptx::mbar_wait(&pv_done[pb], ((j - 2) >> 1) & 1, lim)) { fail(); break; }
+      const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
+      // O is stable once PV(j-1) has completed: needed only to rescale it
+      if (rescale && !ptx::mbar_wait(&pv_done[pb ^ 1], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
       ptx::tc_fence_after();
-      if (j >= 1 && __any_sync(0xffffffffu, raise)) {  // rescale this warp's O rows in TMEM
+      if (rescale) {  // rescale this warp's O rows in TMEM
 #pragma unroll 1
         for (int c0 = 0; c0 < DH; c0 += 32) {
           float o[32];
@@ -324,17 +346,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       m_used = m_new;
       // P row -> shared memory, K-major 128-byte swizzled (16-byte chunk c at c ^ (row % 8))
-      uint4* prow = reinterpret_cast<uint4*>(sP + row * 128);
+      uint4* prow = reinterpret_cast<uint4*>(sP + pb * L::P_BYTES + row * 128);
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         prow[c ^ (row & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(p_full);
+      if (lane == 0) ptx::mbar_arrive(&p_full[pb]);
     }
-    // the last PV
-    if (nt > 0 && !*abort_flag && !ptx::mbar_wait(pv_done, (nt - 1) & 1, lim)) fail();
+    // the last PV (it follows every earlier one on the tensor pipe)
+    if (nt > 0 && !*abort_flag && !ptx::mbar_wait(&pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, lim)) fail();
     ptx::tc_fence_after();
     // l over the row is complete in-thread (one thread per row)
     const int gr = r0 + row;

@@ -65,6 +65,13 @@ __device__ __forceinline__ float gelu_tanh_fast(float x) {
   return 0.5f * x * (1.f + tanh_approx(c * (x + 0.044715f * x * x * x)));
 }
 
+// 2^x with the hardware ex2.approx instruction (relative error about 2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // GeLU used by the epilogues: accurate tanh for fp32 activations, hardware tanh for bf16.
 template <typename T> __device__ __forceinline__ float gelu_act(float x);
 template <> __device__ __forceinline__ float gelu_act<float>(float x) { return gelu_tanhf(x); }

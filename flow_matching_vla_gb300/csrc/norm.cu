@@ -191,10 +191,10 @@ __global__ void dit_in_kernel(const float* __restrict__ x, int A, const T* __res
 // Warp per row, for many rows: the row lives in registers (D/64 float2 per
 // lane), reductions are warp shuffles, no block barriers; 8 rows per CTA.
 constexpr int kRowsPerCta = 8;
-constexpr int kMaxPairsPerLane = 32;  // D <= 2048
+constexpr int kMaxPairsPerLane = 16;  // D <= 1024
 
 template <typename T>
-__global__ void __launch_bounds__(256) adanorm_rows_kernel(float* __restrict__ h, int D, int M,
+__global__ void __launch_bounds__(256, 2) adanorm_rows_kernel(float* __restrict__ h, int D, int M,
                                                            T* __restrict__ out, NormArgs na) {
   ptx::pdl_launch_dependents();
   ptx::pdl_wait();

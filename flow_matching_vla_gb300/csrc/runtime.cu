@@ -500,7 +500,8 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       // tcgen05 attention once there are enough 128-row tiles; below that the
       // 64-row mma.sync kernel spreads the work over more SMs
       const bool big_attn = (long long)B * ((c->Hq * H + 127) / 128) >= 8;
-      if (c->dt == DT_BF16 && c->opt_attn == 0 && big_attn && attn_t5_supported(c->Dh, c->Hq)) {
+      if (c->dt == DT_BF16 && ((c->opt_attn == 0 && big_attn) || c->opt_attn == 3) &&
+          attn_t5_supported(c->Dh, c->Hq)) {
         AttnT5Args a5;
         a5.qkv = c->qkv; a5.ldq = nq; a5.k_off = c->qd; a5.v_off = c->qd + c->Dh;
         a5.B = B; a5.H = H; a5.Hq = c->Hq; a5.Dh = c->Dh; a5.P = P;
@@ -954,7 +955,7 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
       c->opt_gemm = (int)value;
       break;
     case GR00T_OPT_ATTN_PATH:
-      if (value < 0 || value > 2) return set_err(c, GR00T_EINVAL, "attention path must be 0, 1 or 2");
+      if (value < 0 || value > 3) return set_err(c, GR00T_EINVAL, "attention path must be 0, 1, 2 or 3");
       c->opt_attn = (int)value;
       break;
     case GR00T_OPT_WAIT_LIMIT:
@@ -1102,7 +1103,8 @@ long long step_scratch(gr00t_ctx* c, long long cap) {
   take(gemm_scratch(c, M, D, c->qd, true, cap));
   take(gemm_scratch(c, M, up_rows, D, false, cap));
   take(gemm_scratch(c, M, D, c->F, true, cap));
-  if (c->dt == DT_BF16 && c->opt_attn == 0 && (long long)B * ((c->Hq * c->H + 127) / 128) >= 8 &&
+  if (c->dt == DT_BF16 &&
+      ((c->opt_attn == 0 && (long long)B * ((c->Hq * c->H + 127) / 128) >= 8) || c->opt_attn == 3) &&
       attn_t5_supported(c->Dh, c->Hq)) {
     AttnT5Args a5;
     a5.B = B; a5.H = c->H; a5.Hq = c->Hq; a5.Dh = c->Dh; a5.P = c->bP;

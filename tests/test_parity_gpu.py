@@ -41,7 +41,7 @@ def _gates(case):
     return (BF16_VEL_REL, None) if bf16 else (FP32_REL, FP32_REL)
 
 
-def check_case(case, steps=None, samples=None):
+def check_case(case, steps=None, samples=None, options=()):
     """Run the GPU loop on ``case`` and compare with the oracle.
 
     ``samples``: only compare these batch entries (the oracle runs them as
@@ -51,6 +51,8 @@ def check_case(case, steps=None, samples=None):
     g = case["geom"]
     T = steps or g["steps"]
     loop, held = fmv.from_case(case, steps=T)
+    for opt, val in options:
+        loop.set_option(opt, val)
     x0 = torch.from_numpy(case["x_noise"]).cuda()
     out = loop.denoise(x0)
     # teacher-forced velocities need the oracle trajectory of the compared samples
@@ -132,3 +134,19 @@ def test_pi05_batch32_sampled():
 
 def test_pi05_long_prefix_sampled():
     check_case(synth.make_case("pi05_long"), samples=[0, 7])
+
+
+# every attention kernel of the expert family on the same small cases: 1 = CUDA
+# cores, 2 = mma.sync head-folded, 3 = tcgen05/TMEM (several 128-row tiles,
+# ragged key tiles, key splits combined across a cluster)
+@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("kw", [dict(), dict(prefix=0, batch=1), dict(prefix=700, batch=2, horizon=30)])
+def test_expert_attention_paths(path, kw):
+    fmv = _fmv()
+    check_case(synth.make_case("small_bf16", **kw), options=[(fmv.OPT_ATTN_PATH, path)])
+
+
+def test_tcgen05_attention_head_dim_64():
+    fmv = _fmv()
+    c = synth.make_case("small_bf16", q_heads=4, head_dim=64, batch=4, prefix=150)
+    check_case(c, options=[(fmv.OPT_ATTN_PATH, 3)])
