@@ -143,8 +143,10 @@ struct EpiRun {
       }
     }
   }
-  // Column m (token row of the output); j = m % tok_rope maintained by the caller for RoPE.
-  __device__ __forceinline__ void operator()(int m, int j, float a0, float a1) const {
+  // RoPE (cos, sin) of token index j (j < tok_rope) for this thread's frequency.
+  __device__ __forceinline__ float2 rope_cs(int j) const { return e_.rope_tab[j * half_ + i_]; }
+  // Column m (token row of the output); cs = rope_cs(m % tok_rope), loaded ahead by the caller.
+  __device__ __forceinline__ void operator()(int m, float2 cs, float a0, float a1) const {
     if (KIND == EPI_STORE) {
       a0 += b0_;
       a1 += b1_;
@@ -163,7 +165,6 @@ struct EpiRun {
     } else if (KIND == EPI_ROPE) {
       bf16* o = (bf16*)e_.out + (long long)m * e_.ldo;
       if (rope_) {
-        const float2 cs = e_.rope_tab[j * half_ + i_];
         o[col0_] = __float2bfloat16_rn(a0 * cs.x - a1 * cs.y);
         o[col0_ + half_] = __float2bfloat16_rn(a1 * cs.x + a0 * cs.y);
       } else {
@@ -184,20 +185,30 @@ struct EpiRun {
 };
 
 // 32 accumulator columns c0..c0+31 of rows (n, n+1) held by a lane pair; this
-// lane finishes columns of parity ``odd``.
+// lane finishes columns of parity ``odd``.  For RoPE the 16 (cos, sin) pairs
+// are loaded together up front (token index kept in [0, tok_rope), so every
+// load is in bounds even past M), not one dependent load per column.
 template <int KIND>
 __device__ __forceinline__ void epi_columns(const EpiRun<KIND>& run, const float (&v)[32], bool odd, int m_first,
                                             int M, int tok_rope) {
-  int j = m_first % tok_rope;  // token index within its sample, for the RoPE table
+  float2 cs[16];
+  if (KIND == EPI_ROPE) {
+    int j = m_first % tok_rope;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      cs[q] = run.rope_ ? run.rope_cs(j) : make_float2(1.f, 0.f);
+      j += 2;  // next column of this parity; tok_rope may be 1
+      if (j >= tok_rope) j -= tok_rope;
+      if (j >= tok_rope) j -= tok_rope;
+    }
+  }
   int m = m_first;
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
     const float send = odd ? v[c] : v[c + 1];
     const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-    if (m < M) run(m, j, odd ? recv : v[c], odd ? v[c + 1] : recv);
+    if (m < M) run(m, KIND == EPI_ROPE ? cs[c >> 1] : make_float2(1.f, 0.f), odd ? recv : v[c], odd ? v[c + 1] : recv);
     m += 2;
-    j += 2;
-    if (j >= tok_rope) j -= tok_rope;
   }
 }
 }  // namespace g3

@@ -460,6 +460,11 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   cudaStream_t s = c->stream;
 
   auto site = [&](int si) { return (const void*)(mod_k + (long long)si * R * es); };
+  // Kernels read the modulation table before their programmatic-launch wait.
+  // The table is written when the schedule is set, so the head of step 0 is
+  // launched without the early-launch attribute: it (and so every later
+  // kernel) starts only once that write has completed.
+  const bool pdl_head = c->opt_pdl != 0 && k > 0;
   NormArgs base;
   base.eps = c->g.norm_eps;
   base.mod_bstride = bstride;
@@ -473,7 +478,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     na.shift_off = D;
     ++c->launches;
     tmark(c, GR00T_KCLASS_NORM);
-    CK(c, expert_in(c->dt, x, c->A, c->w_in, c->b_in, c->h, D, M, c->n, na, s, c->opt_pdl != 0));
+    CK(c, expert_in(c->dt, x, c->A, c->w_in, c->b_in, c->h, D, M, c->n, na, s, pdl_head));
     tmark(c, GR00T_KCLASS_NORM);
     const int nq = c->nqkv[0];
     for (int l = 0; l < L; ++l) {
@@ -583,7 +588,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   ++c->launches;
   tmark(c, GR00T_KCLASS_NORM);
   CK(c, dit_in(c->dt, x, c->A, c->w_enc1, c->b_enc1, c->a_enc, D, MA, (const float*)c->host_table[2 * L + 2],
-               Ns, tok, B, c->h, s, c->opt_pdl != 0));
+               Ns, tok, B, c->h, s, pdl_head));
   tmark(c, GR00T_KCLASS_NORM);
   {
     GemmArgs g;  // e = swish(a W2[:, :D]^T + atb_k), atb_k holds W2's time half and b2

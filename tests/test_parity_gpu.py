@@ -150,3 +150,28 @@ def test_tcgen05_attention_head_dim_64():
     fmv = _fmv()
     c = synth.make_case("small_bf16", q_heads=4, head_dim=64, batch=4, prefix=150)
     check_case(c, options=[(fmv.OPT_ATTN_PATH, 3)])
+
+
+# many token rows (>= 256): the warp-per-row norms, the multi-row step head and
+# the step tail; the residual split cap selects how many split-K partials the
+# norms fold (1: none, 2: the unrolled pair, 16: the general loop)
+@pytest.mark.parametrize("cap", [1, 2, 16])
+def test_many_rows_expert_bf16(cap):
+    fmv = _fmv()
+    check_case(synth.make_case("small_bf16", batch=8), options=[(fmv.OPT_RESID_SPLIT_CAP, cap)])
+
+
+def test_many_rows_expert_fp32():
+    check_case(synth.make_case("small_fp32", batch=6))
+
+
+def test_many_rows_dit_layer_norm():
+    check_case(synth.make_case("small_dit", batch=16, prefix=120))
+
+
+def test_single_token_horizon_unsplit_epilogue():
+    # one token per sample and no split-K: the RoPE epilogue walks several
+    # samples' rows per thread with a token index that wraps every column
+    fmv = _fmv()
+    check_case(synth.make_case("small_bf16", prefix=0, horizon=1, batch=5),
+               options=[(fmv.OPT_SPLIT_CAP, 1)])
