@@ -67,21 +67,33 @@ __device__ __forceinline__ int swz(int r, int c) {
   return r * DH + ((c ^ (r & 7)) << 3);
 }
 
+constexpr int RING = 3;    // resident K/V sub-tile buffers
+
 template <int DH>
 struct AttnSmem {
   static constexpr int TILE = ROWS * DH * 2;   // Q, K or V tile (64 rows)
-  // Q, K, V tiles | combine scratch (weights, sums, 1/sum)
-  static constexpr int TOTAL = 3 * TILE + 3 * ROWS * 4 + 16;
+  // Q | RING x (K, V) | combine scratch (weights, sums, 1/sum)
+  static constexpr int TOTAL = (1 + 2 * RING) * TILE + 3 * ROWS * 4 + 16;
 };
+
+__device__ __forceinline__ void cp_async_wait_upto(int n) {  // at most n newer groups pending
+  if (n <= 0)
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+  else if (n == 1)
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else
+    asm volatile("cp.async.wait_group 2;" ::: "memory");
+}
 
 template <int DH>
 __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
   using L = AttnSmem<DH>;
   extern __shared__ __align__(128) uint8_t smem[];
   bf16* sQ = reinterpret_cast<bf16*>(smem);
-  bf16* sK = reinterpret_cast<bf16*>(smem + L::TILE);
-  bf16* sV = reinterpret_cast<bf16*>(smem + 2 * L::TILE);
-  float* sW = reinterpret_cast<float*>(smem + 3 * L::TILE);   // combine scratch [S][RP]
+  // K/V sub-tile buffer i: K at smem + (1 + 2i) TILE, V right after it
+  auto sK = [&](int i) { return reinterpret_cast<bf16*>(smem + (1 + 2 * i) * L::TILE); };
+  auto sV = [&](int i) { return reinterpret_cast<bf16*>(smem + (2 + 2 * i) * L::TILE); };
+  float* sW = reinterpret_cast<float*>(smem + (1 + 2 * RING) * L::TILE);   // combine scratch [S][RP]
   float* sLs = sW + ROWS;
   float* sInv = sLs + ROWS;
 
@@ -100,13 +112,13 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
 
   ptx::pdl_launch_dependents();
   // The bound prefix K/V and the pointer table are never written inside the
-  // loop: stage the first sub-tile's prefix rows before waiting on the kernel
-  // that produces this step's Q and suffix K/V.
+  // loop: stage the prefix rows of the first RING sub-tiles before waiting on
+  // the kernel that produces this step's Q and suffix K/V.
   const bf16* Kp = reinterpret_cast<const bf16*>(a.table[a.k_slot]);
   const bf16* Vp = reinterpret_cast<const bf16*>(a.table[a.v_slot]);
   const bf16* qkv = reinterpret_cast<const bf16*>(a.qkv);
   // phase 0: prefix rows only, 1: suffix and out-of-range rows only, 2: all rows
-  auto issue_kv = [&](int kt, int phase) {
+  auto issue_kv = [&](int kt, int phase, int buf) {
     for (int i = tid; i < KT * CH; i += 128) {
       const int r = i / CH, c = i % CH;
       const int s = kt + r;
@@ -122,11 +134,13 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
         ks = qkv + row * a.ldq + a.k_off;
         vs = qkv + row * a.ldq + a.v_off;
       }
-      cp_async16(sK + swz<DH>(r, c), ok ? (const void*)(ks + c * 8) : (const void*)qkv, ok);
-      cp_async16(sV + swz<DH>(r, c), ok ? (const void*)(vs + c * 8) : (const void*)qkv, ok);
+      cp_async16(sK(buf) + swz<DH>(r, c), ok ? (const void*)(ks + c * 8) : (const void*)qkv, ok);
+      cp_async16(sV(buf) + swz<DH>(r, c), ok ? (const void*)(vs + c * 8) : (const void*)qkv, ok);
     }
   };
-  if (k_begin < k_end) issue_kv(k_begin, 0);
+  const int nsub = (k_end - k_begin + KT - 1) / KT;   // 0 when the split is empty
+  const int first = nsub < RING ? nsub : RING;
+  for (int i = 0; i < first; ++i) issue_kv(k_begin + i * KT, 0, i);
   ptx::pdl_wait();
 
   // Q tile: folded row r = t * Hq + h -> qkv[(b*H + t) * ldq + h * DH]
@@ -138,7 +152,7 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
     const bf16* src = qkv + ((long long)b * a.H + t) * a.ldq + h * DH + c * 8;
     cp_async16(sQ + swz<DH>(r, c), src, ok);
   }
-  if (k_begin < k_end) issue_kv(k_begin, 1);
+  for (int i = 0; i < first; ++i) issue_kv(k_begin + i * KT, 1, i);
   cp_async_commit();
 
   const float sl2 = rsqrtf((float)DH) * 1.4426950408889634f;  // 1/sqrt(d) * log2(e)
@@ -148,14 +162,18 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   const int g = lane >> 2, tq = lane & 3;
 
-  for (int kt = k_begin; kt < k_end; kt += KT) {
-    if (kt != k_begin) {
-      __syncthreads();  // previous sub-tile fully consumed
-      issue_kv(kt, 2);
-      cp_async_commit();
-    }
-    cp_async_wait_all();
+  for (int it = 0; it < nsub; ++it) {
+    const int kt = k_begin + it * KT;
+    const int buf = it % RING;
+    // sub-tile `it` landed: the first RING arrived with Q; a later one was the
+    // refill group issued RING iterations ago, newer refills may stay pending
+    if (it == 0)
+      cp_async_wait_all();
+    else if (it >= RING)
+      cp_async_wait_upto(min(RING - 1, nsub - 1 - it));
     __syncthreads();
+    const bf16* cK = sK(buf);
+    const bf16* cV = sV(buf);
     // S = Q K^T for this warp's 16 rows x 64 keys
     float sacc[8][4];
 #pragma unroll
@@ -173,7 +191,7 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
         uint32_t kb[4];
         const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
         const int c = ks * 2 + ((lane >> 3) & 1);
-        ldsm_x4(kb, sK + swz<DH>(r, c));
+        ldsm_x4(kb, cK + swz<DH>(r, c));
         mma16816(sacc[2 * np], qa, kb[0], kb[1]);
         mma16816(sacc[2 * np + 1], qa, kb[2], kb[3]);
       }
@@ -231,10 +249,15 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
         uint32_t vb[4];
         const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
         const int c = dn * 2 + (lane >> 4);
-        ldsm_x4_t(vb, sV + swz<DH>(r, c));
+        ldsm_x4_t(vb, cV + swz<DH>(r, c));
         mma16816(o[2 * dn], pa, vb[0], vb[1]);
         mma16816(o[2 * dn + 1], pa, vb[2], vb[3]);
       }
+    }
+    if (it + RING < nsub) {  // buffer `buf` fully consumed by every warp: refill it
+      __syncthreads();
+      issue_kv(k_begin + (it + RING) * KT, 2, buf);
+      cp_async_commit();
     }
   }
 #pragma unroll

@@ -20,20 +20,21 @@
 //    more than 8 (2^8 headroom, exact arithmetic otherwise), write P (bf16)
 //    into shared memory in the MMA's swizzled K-major layout and hand it to
 //    the MMA warp;
-//  * key splits of one row tile form a cluster; partial (O, max, sum) go to
-//    the workspace and are combined after one cluster barrier in split order.
+//  * with S key splits each split CTA writes its partial (O / sum as bf16, and
+//    (max, sum)) to the workspace; a warp-per-row kernel merges the S splits.
 // All mbarrier waits are bounded (error flag, drained copies, freed TMEM).
-#include <cooperative_groups.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
 #include "tc_ptx.cuh"
 
 namespace g3 {
 
-namespace cg = cooperative_groups;
 
 namespace {
 
@@ -53,7 +54,7 @@ struct T5Smem {
   static constexpr int OFF_P = OFF_KV + 2 * STAGE;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
   static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2;
-  static constexpr int TOTAL = OFF_BAR + NBAR * 8 + 16 + 3 * ROWS * 4 + 1024;
+  static constexpr int TOTAL = OFF_BAR + NBAR * 8 + 16 + 1024;
 };
 
 // MN-major (V) descriptor: 64-element rows of 128 bytes along N in groups of 8 K-rows
@@ -137,11 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_empty = bars + 15;  // [2] PV read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* sW = reinterpret_cast<float*>(tmem_slot + 4);   // combine scratch [S][RP]
-  float* sLs = sW + ROWS;
-  float* sInv = sLs + ROWS;
 
-  cg::cluster_group cluster = cg::this_cluster();
   const int S = (int)gridDim.y;
   const int split = (int)blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -389,10 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      // partial (O unnormalised, running max, sum) of this split -> workspace
-      const long long tile = (long long)b * gridDim.x + blockIdx.x;
-      constexpr int PART = ROWS * DH + 2 * ROWS;
-      float* my = a.ws + (tile * S + split) * PART;
+      // this split's partial -> workspace: O / l as bf16 and (max, sum);
+      // attn_t5_combine merges the S splits of every row
+      const long long tiles = (long long)gridDim.x * gridDim.z;
+      const long long slot = ((long long)b * gridDim.x + blockIdx.x) * S + split;
+      bf16* wrow = reinterpret_cast<bf16*>(a.ws) + (slot * ROWS + row) * DH;
+      float2* wml = reinterpret_cast<float2*>(reinterpret_cast<bf16*>(a.ws) + tiles * S * ROWS * DH);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c0 = 0; c0 < DH; c0 += 32) {
         float o[32];
@@ -403,73 +403,85 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) o[c] = 0.f;
         }
 #pragma unroll
-        for (int c = 0; c < 32; c += 4)
-          *reinterpret_cast<float4*>(my + row * DH + c0 + c) = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+        for (int c = 0; c < 32; c += 8) {
+          uint4 w;
+          uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[c + 2 * q] * inv, o[c + 2 * q + 1] * inv);
+            wp[q] = *reinterpret_cast<uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(wrow + c0 + c) = w;
+        }
       }
-      my[ROWS * DH + row] = nt > 0 ? m_used : -INFINITY;
-      my[ROWS * DH + ROWS + row] = l;
+      wml[slot * ROWS + row] = make_float2(nt > 0 ? m_used : -INFINITY, l);
     }
   }
 
-  // ---------------- combine the key splits ----------------
-  if (S > 1) {
-    cluster.sync();
-    const long long tile = (long long)b * gridDim.x + blockIdx.x;
-    constexpr int PART = ROWS * DH + 2 * ROWS;
-    const float* base = a.ws + tile * S * PART;
-    const int RP = ROWS / S;
-    const int tid = threadIdx.x;
-    if (tid < S * RP) {
-      const int sp = tid / RP, rr = split * RP + tid % RP;
-      sW[tid] = base[sp * PART + ROWS * DH + rr];
-      sLs[tid] = base[sp * PART + ROWS * DH + ROWS + rr];
-    }
-    __syncthreads();
-    if (tid < RP) {
-      float mx = -INFINITY;
-      for (int sp = 0; sp < S; ++sp) mx = fmaxf(mx, sW[sp * RP + tid]);
-      float lsum = 0.f;
-      for (int sp = 0; sp < S; ++sp) {
-        const float ms = sW[sp * RP + tid];
-        const float w = ms == -INFINITY ? 0.f : exp2f(ms - mx);
-        lsum += w * sLs[sp * RP + tid];
-        sW[sp * RP + tid] = w;
-      }
-      sInv[tid] = lsum > 0.f ? 1.f / lsum : 0.f;
-    }
-    __syncthreads();
-    const int items = RP * (DH / 4);
-    for (int it = tid; it < items; it += kThreads) {
-      const int lr = it / (DH / 4), col = (it % (DH / 4)) * 4;
-      const int gr = r0 + split * RP + lr;
-      if (gr >= nrows) continue;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      float4 v[16];
-#pragma unroll
-      for (int sp = 0; sp < 16; ++sp)
-        if (sp < S) v[sp] = *reinterpret_cast<const float4*>(base + sp * PART + (split * RP + lr) * DH + col);
-#pragma unroll
-      for (int sp = 0; sp < 16; ++sp)
-        if (sp < S) {
-          const float w = sW[sp * RP + lr];
-          acc.x += w * v[sp].x;
-          acc.y += w * v[sp].y;
-          acc.z += w * v[sp].z;
-          acc.w += w * v[sp].w;
-        }
-      const float inv = sInv[lr];
-      const int t = gr / a.Hq, h = gr % a.Hq;
-      bf16* o = (bf16*)a.out + ((long long)b * a.H + t) * a.ldo + h * DH + col;
-      *reinterpret_cast<__nv_bfloat162*>(o) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      *reinterpret_cast<__nv_bfloat162*>(o + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    }
-  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
+}
+
+// Merge of the S key splits: a warp per folded query row.  Lane s < S reads
+// split s's (max, sum); the weights l_s 2^(m_s - M) / sum_s l_s 2^(m_s - M) are
+// shared by shuffles; each lane then sums its DH / 32 columns of the S
+// normalised partials (all S loads issued together) and stores the row.
+template <int DH>
+__global__ void __launch_bounds__(256) attn_t5_combine_kernel(AttnT5Args a, int S) {
+  ptx::pdl_launch_dependents();
+  constexpr int PER = DH / 32;   // columns per lane: 8, 4 or 2
+  const int lane = threadIdx.x & 31;
+  const int nrows = a.Hq * a.H;
+  const int tiles_x = (nrows + ROWS - 1) / ROWS;
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // b * nrows + gr
+  ptx::pdl_wait();
+  if (gw >= (long long)a.B * nrows) return;
+  const int b = (int)(gw / nrows), gr = (int)(gw % nrows);
+  const long long tiles = (long long)tiles_x * a.B;
+  const long long slot0 = ((long long)b * tiles_x + gr / ROWS) * S;
+  const int row = gr % ROWS;
+  const bf16* part = reinterpret_cast<const bf16*>(a.ws);
+  const float2* wml = reinterpret_cast<const float2*>(part + tiles * S * ROWS * DH);
+  typedef typename std::conditional<PER == 8, uint4, typename std::conditional<PER == 4, uint2, uint32_t>::type>::type V;
+  V v[16];   // the partial rows, loaded together with the (max, sum) pairs
+#pragma unroll
+  for (int sp = 0; sp < 16; ++sp)
+    if (sp < S) v[sp] = *reinterpret_cast<const V*>(part + ((slot0 + sp) * ROWS + row) * DH + lane * PER);
+  const float2 ml = lane < S ? wml[(slot0 + lane) * ROWS + row] : make_float2(-INFINITY, 0.f);
+  float mx = ml.x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float e = ml.x == -INFINITY ? 0.f : ml.y * exp2f(ml.x - mx);
+  const float tot = warp_sum(e);
+  const float w = tot > 0.f ? e / tot : 0.f;
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < 16; ++sp) {
+    if (sp >= S) break;
+    const float ws = __shfl_sync(0xffffffffu, w, sp);
+    const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[sp]);
+#pragma unroll
+    for (int q = 0; q < PER / 2; ++q) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[q]));
+      acc[2 * q] += ws * f.x;
+      acc[2 * q + 1] += ws * f.y;
+    }
+  }
+  V outv;
+  uint32_t* op = reinterpret_cast<uint32_t*>(&outv);
+#pragma unroll
+  for (int q = 0; q < PER / 2; ++q) {
+    __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    op[q] = *reinterpret_cast<uint32_t*>(&h2);
+  }
+  const int t = gr / a.Hq, h = gr % a.Hq;
+  *reinterpret_cast<V*>((bf16*)a.out + ((long long)b * a.H + t) * a.ldo + h * DH + lane * PER) = outv;
 }
 
 template <int DH>
@@ -480,25 +492,13 @@ cudaError_t launch_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaS
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
     configured = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((a.Hq * a.H + ROWS - 1) / ROWS, S, a.B);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L::TOTAL;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = S;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], a);
+  cudaError_t e = launch_k(kern, dim3((a.Hq * a.H + ROWS - 1) / ROWS, S, a.B), dim3(kThreads), L::TOTAL, s, pdl,
+                           maps[0], maps[1], maps[2], maps[3], maps[4], a);
+  if (e != cudaSuccess || S == 1) return e;
+  const long long warps = (long long)a.B * a.Hq * a.H;
+  return launch_k(attn_t5_combine_kernel<DH>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, pdl, a, S);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode5 = nullptr;
@@ -533,7 +533,8 @@ int attn_t5_splits(const AttnT5Args& a, int sm_count) {
 long long attn_t5_workspace_floats(const AttnT5Args& a, int S) {
   if (S == 1) return 0;
   const long long tiles = (long long)(a.Hq * a.H + ROWS - 1) / ROWS * a.B;
-  return tiles * S * ((long long)ROWS * a.Dh + 2 * ROWS);
+  const long long bytes = tiles * S * ROWS * ((long long)a.Dh * 2 + 8);
+  return (bytes + 3) / 4;
 }
 
 // maps: [0] Q (3-D over [B*H tokens][Hq][Dh] inside qkv), [1] prefix K, [2] prefix V ([B*P][Dh]),

@@ -502,11 +502,10 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
 
       ++c->launches;
       tmark(c, GR00T_KCLASS_ATTENTION);
-      // tcgen05 attention once there are enough 128-row tiles; below that the
-      // 64-row mma.sync kernel spreads the work over more SMs
-      const bool big_attn = (long long)B * ((c->Hq * H + 127) / 128) >= 8;
-      if (c->dt == DT_BF16 && ((c->opt_attn == 0 && big_attn) || c->opt_attn == 3) &&
-          attn_t5_supported(c->Dh, c->Hq)) {
+      // bf16: the tcgen05 kernel (key splits merged by a second kernel when the
+      // row tiles alone do not fill the GPU); the mma.sync and CUDA-core
+      // kernels remain selectable
+      if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 3) && attn_t5_supported(c->Dh, c->Hq)) {
         AttnT5Args a5;
         a5.qkv = c->qkv; a5.ldq = nq; a5.k_off = c->qd; a5.v_off = c->qd + c->Dh;
         a5.B = B; a5.H = H; a5.Hq = c->Hq; a5.Dh = c->Dh; a5.P = P;
@@ -515,7 +514,9 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         a5.err = c->err_flag; a5.wait_limit = c->wait_limit;
         CUtensorMap maps[5];
         CK(c, attn_t5_maps(a5, c->host_table[2 * l], c->host_table[2 * l + 1], maps));
-        CK(c, attention_t5(a5, maps, attn_t5_splits(a5, c->sm_count), s, c->opt_pdl != 0));
+        const int splits = attn_t5_splits(a5, c->sm_count);
+        if (splits > 1) ++c->launches;   // the split merge is a second kernel
+        CK(c, attention_t5(a5, maps, splits, s, c->opt_pdl != 0));
       } else if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 2) && attn_fold_supported(c->Dh)) {
         AttnFoldArgs af;
         af.qkv = c->qkv; af.ldq = nq; af.k_off = c->qd; af.v_off = c->qd + c->Dh;

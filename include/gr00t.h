@@ -267,8 +267,9 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
 #define GR00T_OPT_USE_GRAPH 1     /* 1 (default): replay the loop as a CUDA graph */
 #define GR00T_OPT_GEMM_PATH 2     /* 0: tensor-core path where supported (default), 1: CUDA-core path */
 #define GR00T_OPT_WAIT_LIMIT 3    /* spin-wait iteration limit of bounded device waits (>= 0) */
-#define GR00T_OPT_ATTN_PATH 4     /* 0: tensor-core attention chosen by size (default), 1: CUDA-core,
-                                     2: mma.sync head-folded kernel, 3: tcgen05/TMEM kernel (expert family) */
+#define GR00T_OPT_ATTN_PATH 4     /* expert family: 0 (default): tcgen05/TMEM kernel for bf16 (its key splits
+                                     merged by a second kernel), else CUDA cores; 1: CUDA-core kernel;
+                                     2: mma.sync head-folded kernel; 3: tcgen05/TMEM kernel */
 #define GR00T_OPT_TIME_KERNEL 5   /* bracket every launch of one kernel class with timing events
                                      (GR00T_KCLASS_*, 0 = off); read with gr00t_kernel_times */
 #define GR00T_OPT_SPLIT_CAP 6     /* largest split-K factor of GEMMs that reduce in-kernel (1..16, power of 2; default 8) */
