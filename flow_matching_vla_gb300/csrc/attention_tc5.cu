@@ -523,11 +523,15 @@ cudaError_t encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* 
 bool attn_t5_supported(int Dh, int Hq) { return (Dh == 64 || Dh == 128 || Dh == 256) && Hq > 0 && ROWS % Hq == 0; }
 
 int attn_t5_splits(const AttnT5Args& a, int sm_count) {
+  // at most one CTA per SM and 16 splits; then as few splits as keep that many
+  // key tiles per split, so no split is left empty
   const int tiles = (a.Hq * a.H + ROWS - 1) / ROWS * a.B;
   const int ntiles = (a.P + KT - 1) / KT + (a.H + KT - 1) / KT;
-  int S = 1;
-  while (S < 16 && tiles * S * 2 <= sm_count && ntiles >= 2 * S) S *= 2;
-  return S;
+  int S = sm_count / (tiles > 0 ? tiles : 1);
+  S = S < 1 ? 1 : (S > 16 ? 16 : S);
+  if (S > ntiles) S = ntiles > 0 ? ntiles : 1;
+  const int tps = (ntiles + S - 1) / S;
+  return tps > 0 ? (ntiles + tps - 1) / tps : 1;
 }
 
 long long attn_t5_workspace_floats(const AttnT5Args& a, int S) {
@@ -564,7 +568,7 @@ cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, CU
 
 cudaError_t attention_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl) {
   if (a.B <= 0 || a.Hq * a.H <= 0) return cudaSuccess;
-  if (!attn_t5_supported(a.Dh, a.Hq) || S < 1 || S > 16 || (S & (S - 1))) return cudaErrorInvalidValue;
+  if (!attn_t5_supported(a.Dh, a.Hq) || S < 1 || S > 16) return cudaErrorInvalidValue;
   if (attn_t5_workspace_floats(a, S) > a.ws_floats) return cudaErrorInvalidValue;
   switch (a.Dh) {
     case 64: return launch_t5<64>(a, maps, S, s, pdl);

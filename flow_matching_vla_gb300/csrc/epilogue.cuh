@@ -90,6 +90,7 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, f
 struct EpiPre {
   float2 h;
   float2 g;
+  float2 cs;   // RoPE (cos, sin) of the pair
 };
 
 template <typename T>
@@ -97,7 +98,11 @@ __device__ __forceinline__ EpiPre epi_prefetch(const Epi& e, int m, int n) {
   EpiPre p;
   p.h = make_float2(0.f, 0.f);
   p.g = make_float2(1.f, 1.f);
-  if (e.kind == EPI_RESID_GATED || e.kind == EPI_RESID) {
+  p.cs = make_float2(1.f, 0.f);
+  if (e.kind == EPI_ROPE && n < e.rope_cols) {
+    const int i = (n % e.hd) >> 1, half = e.hd >> 1;
+    p.cs = e.rope_tab[(m % e.tok_rope) * half + i];
+  } else if (e.kind == EPI_RESID_GATED || e.kind == EPI_RESID) {
     p.h = *reinterpret_cast<const float2*>(e.resid + (long long)m * e.ldr + n);
     if (e.kind == EPI_RESID_GATED) {
       const T* g = (const T*)e.gate + (long long)(m / e.tok) * e.gate_bstride + n;
@@ -112,6 +117,13 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, f
   if (e.kind == EPI_RESID_GATED || e.kind == EPI_RESID) {
     *reinterpret_cast<float2*>(e.resid + (long long)m * e.ldr + n) =
         make_float2(p.h.x + p.g.x * a0, p.h.y + p.g.y * a1);
+    return;
+  }
+  if (e.kind == EPI_ROPE && n < e.rope_cols) {   // rotation with the prefetched (cos, sin)
+    T* o = (T*)e.out + (long long)m * e.ldo;
+    const int head = n / e.hd, i = (n % e.hd) >> 1, half = e.hd >> 1;
+    o[head * e.hd + i] = from_f<T>(a0 * p.cs.x - a1 * p.cs.y);
+    o[head * e.hd + i + half] = from_f<T>(a1 * p.cs.x + a0 * p.cs.y);
     return;
   }
   epi_pair<T>(e, m, n, a0, a1);

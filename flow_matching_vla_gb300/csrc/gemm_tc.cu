@@ -40,9 +40,81 @@ struct TcSmem {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int PIPE = STAGES * STAGE_BYTES;
-  static constexpr int BAR = (2 * STAGES + 1) * 8 + 16;
+  static constexpr int BAR = (2 * STAGES + 2) * 8 + 16;
   static constexpr int TOTAL = PIPE + BAR + 1024;  // + alignment slack
+  // split-K reduced on chip: the idle pipeline holds this CTA's fp32 partial
+  // tile and the row slices its peers send it (one tile's worth)
+  static constexpr int PART_BYTES = BN * BM * 4;
+  static constexpr bool ONCHIP = 2 * PART_BYTES <= PIPE;
 };
+
+// Bulk copy of ``bytes`` (multiple of 16, 16-byte aligned) from this CTA's shared
+// memory into a peer's (cluster addresses), completing on the peer's mbarrier.
+__device__ __forceinline__ uint32_t mapa_u32(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void bulk_to_peer(uint32_t rdst, uint32_t src, uint32_t bytes, uint32_t rbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(rdst),
+      "r"(src), "r"(bytes), "r"(rbar)
+      : "memory");
+}
+
+// Element (r, c) of an fp32 [BM rows][BN] tile in shared memory: 16-byte chunk
+// c / 4 of row r stored at chunk (c / 4) ^ ((r / 2) % 8), so both the
+// row-per-lane writes from TMEM and the row-pair-per-lane reads of the
+// reduction spread over the banks.
+template <int BN>
+__device__ __forceinline__ int part_idx(int r, int c) {
+  return r * BN + ((((c >> 2) ^ ((r >> 1) & 7)) << 2) | (c & 3));
+}
+
+// On-chip split-K reduction, rank ``rank`` of S: rows [rank*R, rank*R + R) of
+// the tile summed over the S partials in rank order -- this CTA's from
+// ``part``, peer p's slice of those rows from ``recv`` slot p ([R][BN] each,
+// chunks swizzled by tile row) -- then the KIND epilogue.  One item is a row
+// pair and 4 consecutive tokens; the loops are kept rolled because this code
+// runs once per CTA on a cold instruction cache.
+template <int BN, int KIND>
+__device__ __forceinline__ void reduce_onchip(const Epi& e, const float* part, const float* recv, int S, int rank,
+                                           int m0, int n0, int M, int N) {
+  const int R = BM / S, pairs = R / 2, items = pairs * (BN / 4);
+  const int tok = KIND == EPI_ROPE ? e.tok_rope : 1;
+#pragma unroll 1
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    const int p = it % pairs, q = it / pairs;
+    const int rr = rank * R + 2 * p, j0 = 4 * q;
+    const int n = n0 + rr;
+    if (n >= N || m0 + j0 >= M) continue;
+    const EpiRun<KIND> run(e, n);
+    float2 cs[4];
+    if (KIND == EPI_ROPE) {
+      int j = (m0 + j0) % tok;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        cs[t] = run.rope_ ? run.rope_cs(j) : make_float2(1.f, 0.f);
+        j = j + 1 == tok ? 0 : j + 1;
+      }
+    }
+    const int ch = (q ^ ((rr >> 1) & 7)) << 2;   // rows rr and rr + 1 share the swizzle phase
+    const int lr = rr - rank * R;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+#pragma unroll 1
+    for (int sp = 0; sp < S; ++sp) {
+      const float* b = sp == rank ? part + rr * BN : recv + (sp * R + lr) * BN;
+      const float4 u0 = *reinterpret_cast<const float4*>(b + ch);
+      const float4 u1 = *reinterpret_cast<const float4*>(b + BN + ch);
+      s0.x += u0.x; s0.y += u0.y; s0.z += u0.z; s0.w += u0.w;
+      s1.x += u1.x; s1.y += u1.y; s1.z += u1.z; s1.w += u1.w;
+    }
+    const float a0[4] = {s0.x, s0.y, s0.z, s0.w}, a1[4] = {s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (m0 + j0 + t < M) run(m0 + j0 + t, KIND == EPI_ROPE ? cs[t] : make_float2(1.f, 0.f), a0[t], a1[t]);
+  }
+}
 
 // Rank ``rank`` of an S-way split sums rows [rank*128/S, (rank+1)*128/S) of the
 // tile over the S partials (layout [split][token][row]) in split order and
@@ -132,11 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::PIPE);
   uint64_t* empty = full + STAGES;
   uint64_t* done = empty + STAGES;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* recv_bar = done + 1;                // split-K: the peers' row slices landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   cg::cluster_group cluster = cg::this_cluster();
   const int S = (int)gridDim.z;                 // split-K factor (the cluster size when reducing here)
+  const bool onchip = L::ONCHIP && S > 1 && e.kind != EPI_PARTIAL;
   const int rank = (int)blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * BM, m0 = blockIdx.y * BN;
@@ -149,8 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&empty[s], 1);
     }
     ptx::mbar_init(done, 1);
+    ptx::mbar_init(recv_bar, 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
+    if (onchip) ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((S - 1) * (BM / S) * BN * 4));
     ptx::prefetch_tmap(&tmW);
     ptx::prefetch_tmap(&tmX);
   }
@@ -265,6 +341,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         default: tile_epilogue<EPI_RESID>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
       }
     }
+  } else if (onchip) {
+    // split-K on chip: park this CTA's fp32 partial in its idle pipeline memory,
+    // one cluster barrier, then one bulk copy per peer hands it the R = 128/S
+    // rows it reduces; the epilogue operands are fetched meanwhile
+    float* part = reinterpret_cast<float*>(smem);
+    float* recv = part + BN * BM;   // [S][R][BN]: slot p = rows of peer p (own slot unused)
+    const int R = BM / S;
+    if (!aborted) {
+#pragma unroll 1
+      for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+        float v[32];
+        ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(part + part_idx<BN>(row, c0 + j)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the bulk copies read these writes
+    cluster.sync();
+    if (threadIdx.x == 0) {
+      for (int q = 0; q < S; ++q) {
+        if (q == rank) continue;
+        bulk_to_peer(mapa_u32(ptx::smem_u32(recv + (long long)rank * R * BN), (uint32_t)q),
+                     ptx::smem_u32(part + (long long)q * R * BN), (uint32_t)(R * BN * 4),
+                     mapa_u32(ptx::smem_u32(recv_bar), (uint32_t)q));
+      }
+    }
+    if (!ptx::mbar_wait(recv_bar, 0, wait_limit)) {
+      atomicExch(abort_flag, 1);
+      atomicExch(err, 1);
+    }
+    if (!aborted && !*abort_flag) {
+      switch (e.kind) {
+        case EPI_STORE: reduce_onchip<BN, EPI_STORE>(e, part, recv, S, rank, m0, n0, M, N); break;
+        case EPI_ROPE: reduce_onchip<BN, EPI_ROPE>(e, part, recv, S, rank, m0, n0, M, N); break;
+        case EPI_GEGLU: reduce_onchip<BN, EPI_GEGLU>(e, part, recv, S, rank, m0, n0, M, N); break;
+        default: reduce_onchip<BN, EPI_RESID>(e, part, recv, S, rank, m0, n0, M, N); break;
+      }
+    }
+    cluster.sync();   // every copy out of this CTA has landed before it exits
   } else {
     // split-K: park the fp32 partial in the L2-resident workspace, one cluster
     // barrier (release/acquire orders the global writes), then each rank sums
@@ -546,14 +662,17 @@ cudaError_t tc_make_map(CUtensorMap* m, const void* ptr, long long rows, long lo
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split) {
+TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split, bool partial) {
   TcPlan p;
   p.BN = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
   const int KB = K / BK;
   const long long tiles = (long long)((N + BM - 1) / BM) * ((M + p.BN - 1) / p.BN);
+  // a CTA fills an SM's shared memory: the split stays within one wave.  A
+  // 256-token tile cannot reduce its split on chip, so it only splits when the
+  // partials go to the next kernel.
+  if (p.BN == 256 && !partial) max_split = 1;
   p.S = 1;
-  while (p.S < 16 && 2 * p.S <= max_split && KB % (2 * p.S) == 0 && tiles * 2 * p.S <= sm_count + sm_count / 16)
-    p.S *= 2;
+  while (p.S < 16 && 2 * p.S <= max_split && KB % (2 * p.S) == 0 && tiles * 2 * p.S <= sm_count) p.S *= 2;
   return p;
 }
 
@@ -570,8 +689,8 @@ cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs
   if (!tc_supported(a.M, a.N, a.K) || (a.K / BK) % p.S) return cudaErrorInvalidValue;
   if (a.epi.kind != EPI_PARTIAL && tc_workspace_floats(p, a.M, a.N) > ws_floats) return cudaErrorInvalidValue;
   switch (p.BN) {
-    case 64: return launch<64, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
-    case 128: return launch<128, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
+    case 64: return launch<64, 8>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);    // 8 x 24 KB stages
+    case 128: return launch<128, 6>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);   // 6 x 32 KB stages
     case 256: return launch<256, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
     default: return cudaErrorInvalidValue;
   }

@@ -18,9 +18,10 @@ struct TcPlan {
 cudaError_t tc_make_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld,
                         int box_rows);
 bool tc_supported(int M, int N, int K);
-// Split-K factor: the largest power of two <= max_split that divides the
-// K blocks and keeps tiles * S within 17/16 of the SM count.
-TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split);
+// Split-K factor: the largest power of two <= max_split that divides the K
+// blocks and keeps tiles * S within the SM count (one wave); ``partial``: the
+// split partials go to the next kernel instead of being reduced in-kernel.
+TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split, bool partial);
 // Split-K partials the plan needs (fp32 elements of the workspace).
 long long tc_workspace_floats(const TcPlan& p, int M, int N);
 // W map: box_rows 128 over [N][K]; X map: box_rows plan.BN over [M][K].

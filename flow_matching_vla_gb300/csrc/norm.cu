@@ -366,6 +366,59 @@ __global__ void __launch_bounds__(32 * kNormRowsPerCta) adanorm_rows_kernel(floa
     if (k < nq) st4(o + (k * 32 + lane) * 4, x[k]);
 }
 
+// Few rows: a CTA per row, D / 4 threads, one quad of the row per thread kept
+// in registers.  The modulation (and gate) quads are fetched before the
+// programmatic-launch wait; the residual quad and all S split-K partial quads
+// after it, in one round trip.
+template <typename T>
+__global__ void __launch_bounds__(512) adanorm_cta_kernel(float* __restrict__ h, int D, T* __restrict__ out,
+                                                          NormArgs na) {
+  ptx::pdl_launch_dependents();
+  __shared__ float red[33];
+  typedef RawQuad<T> RQ;
+  const int m = blockIdx.x;
+  const int i = threadIdx.x * 4;
+  typename RQ::type sc, sh, gq;
+  const long long mrow = (long long)(m / na.tok) * na.mod_bstride;
+  if (na.mod) {
+    sc = RQ::load((const T*)na.mod + mrow + na.scale_off + i);
+    sh = RQ::load((const T*)na.mod + mrow + na.shift_off + i);
+  }
+  if (na.part && na.gate) gq = RQ::load((const T*)na.gate + mrow + i);
+  ptx::pdl_wait();
+  float* hr = h + (long long)m * D + i;
+  float4 x = ld4(hr);
+  if (na.part) {
+    float4 v[16];
+#pragma unroll
+    for (int sp = 0; sp < 16; ++sp)
+      if (sp < na.part_S) v[sp] = ld4(na.part + ((long long)sp * na.part_M + m) * D + i);
+    float4 acc = v[0];
+#pragma unroll
+    for (int sp = 1; sp < 16; ++sp)
+      if (sp < na.part_S) add4(acc, v[sp]);
+    const float4 g = na.gate ? RQ::f(gq) : make_float4(1.f, 1.f, 1.f, 1.f);
+    x.x = fmaf(g.x, acc.x, x.x);
+    x.y = fmaf(g.y, acc.y, x.y);
+    x.z = fmaf(g.z, acc.z, x.z);
+    x.w = fmaf(g.w, acc.w, x.w);
+    st4(hr, x);
+  }
+  float mean = 0.f;
+  if (na.kind == NORM_LN) mean = block_sum((x.x + x.y) + (x.z + x.w), red) / (float)D;
+  const float a = x.x - mean, b = x.y - mean, c = x.z - mean, d = x.w - mean;
+  const float r = rsqrtf(block_sum((a * a + b * b) + (c * c + d * d), red) / (float)D + na.eps);
+  float4 y = make_float4(a * r, b * r, c * r, d * r);
+  if (na.mod) {
+    const float4 s4 = RQ::f(sc), t4 = RQ::f(sh);
+    y.x = y.x * (1.f + s4.x) + t4.x;
+    y.y = y.y * (1.f + s4.y) + t4.y;
+    y.z = y.z * (1.f + s4.z) + t4.z;
+    y.w = y.w * (1.f + s4.w) + t4.w;
+  }
+  st4(out + (long long)m * D + i, y);
+}
+
 // Eight values per call: w[0..7] = p[0..7] (p 16-byte aligned).
 __device__ __forceinline__ void ld8(const bf16* p, float (&w)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -579,6 +632,11 @@ cudaError_t adanorm(DType dt, float* h, int D, int M, void* out, NormArgs na, cu
       return launch_rows<float, AdanormRows>(D, blocks, na.part_S, na.part != nullptr, s, pdl, h, D, M, (float*)out,
                                              na);
     return launch_rows<bf16, AdanormRows>(D, blocks, na.part_S, na.part != nullptr, s, pdl, h, D, M, (bf16*)out, na);
+  }
+  if (D % 128 == 0 && D <= 2048 && (!na.part || na.part_S <= 16) && rows_ok(D, h, out, na.part) &&
+      mod_ok(na, dt == DT_F32 ? 4 : 2)) {  // few rows: a CTA per row, the row in registers
+    if (dt == DT_F32) return launch_k(adanorm_cta_kernel<float>, M, D / 4, 0, s, pdl, h, D, (float*)out, na);
+    return launch_k(adanorm_cta_kernel<bf16>, M, D / 4, 0, s, pdl, h, D, (bf16*)out, na);
   }
   const size_t smem = (D + 33) * sizeof(float);
   if (dt == DT_F32)

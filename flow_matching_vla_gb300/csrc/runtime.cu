@@ -82,8 +82,8 @@ struct gr00t_ctx {
   int opt_pdl = 1;
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
   int opt_l2_ahead = 0;     // each layer's first GEMM prefetches the next layer into L2 (off: measured slower)
-  int split_cap = 8;        // GEMMs that reduce their split-K partials in-kernel
-  int resid_split_cap = 16; // residual GEMMs whose partials the next kernel folds in
+  int split_cap = 4;        // GEMMs that reduce their split-K partials in-kernel
+  int resid_split_cap = 8;  // residual GEMMs whose partials the next kernel folds in
 
   // split-K partials a residual GEMM left for the next norm / out_proj kernel
   struct Pending {
@@ -391,7 +391,8 @@ int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
   ++c->launches;
   tmark(c, cls);
   if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
-    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, a.epi.kind == EPI_PARTIAL ? c->resid_split_cap : c->split_cap);
+    const bool partial = a.epi.kind == EPI_PARTIAL;
+    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, partial ? c->resid_split_cap : c->split_cap, partial);
     const CUtensorMap* tw = tmap(c, a.W, a.N, a.K, a.ldw, 128);
     const CUtensorMap* tx = tmap(c, a.A, a.M, a.K, a.lda, p.BN);
     if (!tw || !tx) return set_err(c, GR00T_ECUDA, "TMA descriptor encode failed (alignment?)");
@@ -413,7 +414,7 @@ int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
 // kernel folds them into h (pending), saving a reduction phase here.
 int gemm_resid(gr00t_ctx* c, GemmArgs a, int cls) {
   if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
-    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, c->resid_split_cap);
+    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, c->resid_split_cap, true);
     if (p.S > 1 && (long long)p.S * a.M * a.N <= c->gemm_ws_floats) {
       c->pending.part = c->gemm_ws;
       c->pending.S = p.S;
@@ -1083,10 +1084,10 @@ cudaError_t noalloc_scratch(int dev, float** out) {
 long long gemm_scratch(gr00t_ctx* c, int M, int N, int K, bool resid, long long cap) {
   if (!(c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(M, N, K))) return 0;
   if (resid) {
-    const TcPlan p = tc_plan(M, N, K, c->sm_count, c->resid_split_cap);
+    const TcPlan p = tc_plan(M, N, K, c->sm_count, c->resid_split_cap, true);
     if (p.S > 1 && (long long)p.S * M * N <= cap) return (long long)p.S * M * N;
   }
-  return tc_workspace_floats(tc_plan(M, N, K, c->sm_count, c->split_cap), M, N);
+  return tc_workspace_floats(tc_plan(M, N, K, c->sm_count, c->split_cap, false), M, N);
 }
 
 // Largest scratch any kernel of one denoise step needs at the bound (batch, prefix).
@@ -1109,9 +1110,7 @@ long long step_scratch(gr00t_ctx* c, long long cap) {
   take(gemm_scratch(c, M, D, c->qd, true, cap));
   take(gemm_scratch(c, M, up_rows, D, false, cap));
   take(gemm_scratch(c, M, D, c->F, true, cap));
-  if (c->dt == DT_BF16 &&
-      ((c->opt_attn == 0 && (long long)B * ((c->Hq * c->H + 127) / 128) >= 8) || c->opt_attn == 3) &&
-      attn_t5_supported(c->Dh, c->Hq)) {
+  if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 3) && attn_t5_supported(c->Dh, c->Hq)) {
     AttnT5Args a5;
     a5.B = B; a5.H = c->H; a5.Hq = c->Hq; a5.Dh = c->Dh; a5.P = c->bP;
     take(attn_t5_workspace_floats(a5, attn_t5_splits(a5, c->sm_count)));
@@ -1134,8 +1133,10 @@ extern "C" int gr00t_denoise_step_noalloc(gr00t_ctx* c, int k, const float* x_in
   CK(c, cudaGetDevice(&dev));
   if (dev != c->device)
     return set_err(c, GR00T_EINVAL, "device %d is current; the context lives on device %d", dev, c->device);
+  // the step's launch sequence is the regular entry point's (planned against the
+  // context's own scratch); it runs here only if its scratch fits the fixed array
   const long long cap = G3_NOALLOC_SCRATCH_FLOATS;
-  const long long need = step_scratch(c, cap);
+  const long long need = step_scratch(c, c->gemm_ws_floats);
   if (need > cap)
     return set_err(c, GR00T_EINVAL,
                    "this step needs %lld floats of scratch at batch %d, prefix %d; the fixed array holds %lld "

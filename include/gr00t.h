@@ -246,8 +246,9 @@ int gr00t_denoise_step(gr00t_ctx* ctx, int k, const float* x_in, float* v_out);
  * Same arguments, inputs, outputs and results as gr00t_denoise_step.
  * Set-up: the first call on a device looks up the array's device address
  * (with that device current -- it must be the context's device); make that
- * first call before any stream capture.  A step whose scratch need at the
- * bound (batch, prefix) exceeds the array returns GR00T_EINVAL with the need
+ * first call before any stream capture.  The call runs gr00t_denoise_step's
+ * own launch sequence; a step whose scratch need in that sequence, at the
+ * bound (batch, prefix), exceeds the array returns GR00T_EINVAL with the need
  * in gr00t_last_error, before anything is enqueued.  All calls in the process
  * share the one array: calls that overlap on the GPU (other streams, other
  * contexts) race on it.  The array keeps the last call's contents; every
@@ -272,8 +273,8 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
                                      2: mma.sync head-folded kernel; 3: tcgen05/TMEM kernel */
 #define GR00T_OPT_TIME_KERNEL 5   /* bracket every launch of one kernel class with timing events
                                      (GR00T_KCLASS_*, 0 = off); read with gr00t_kernel_times */
-#define GR00T_OPT_SPLIT_CAP 6     /* largest split-K factor of GEMMs that reduce in-kernel (1..16, power of 2; default 8) */
-#define GR00T_OPT_RESID_SPLIT_CAP 7 /* same for residual GEMMs whose partials the next kernel folds in (default 16) */
+#define GR00T_OPT_SPLIT_CAP 6     /* largest split-K factor of GEMMs that reduce in-kernel (1..16, power of 2; default 4) */
+#define GR00T_OPT_RESID_SPLIT_CAP 7 /* same for residual GEMMs whose partials the next kernel folds in (default 8) */
 #define GR00T_OPT_PERSISTENT_GEMM 8 /* 1 (default): persistent tensor-core GEMM for unsplit shapes with > 64 tokens */
 #define GR00T_OPT_L2_PREFETCH 9   /* 1: each layer's first GEMM prefetches the next layer's weights (default 0)
                                      and prefix K/V into L2 */

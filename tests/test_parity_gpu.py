@@ -175,3 +175,17 @@ def test_single_token_horizon_unsplit_epilogue():
     fmv = _fmv()
     check_case(synth.make_case("small_bf16", prefix=0, horizon=1, batch=5),
                options=[(fmv.OPT_SPLIT_CAP, 1)])
+
+
+# split-K reduced on chip (partial tiles exchanged between the CTAs of a
+# cluster): 128-token tiles with 2- and 4-way splits, and 8-way splits of the
+# full-size DiT projections
+@pytest.mark.parametrize("cap", [2, 4])
+def test_onchip_split_k_small(cap):
+    fmv = _fmv()
+    check_case(synth.make_case("small_bf16", batch=2, prefix=120), options=[(fmv.OPT_SPLIT_CAP, cap)])
+
+
+def test_onchip_split_k_dit_8way():
+    fmv = _fmv()
+    check_case(synth.make_case("gr00t"), options=[(fmv.OPT_SPLIT_CAP, 8)])

@@ -44,8 +44,8 @@ def test_noalloc_step_matches_regular_step_twice(name):
 
 def test_noalloc_rejects_a_step_larger_than_its_scratch():
     fmv = _fmv()
-    # 32 samples of a 1024-wide expert: the output projection's split-K scratch
-    # is 3.7 M floats, more than the fixed 3 * 2^20-float array
+    # 32 samples of a 1024-wide expert: the output projection's split-K
+    # partials (2 x 1600 x 1024 = 3.3 M floats) exceed the fixed 3 * 2^20-float array
     c = synth.make_case("small_bf16", hidden=1024, mlp_dim=1024, batch=32, layers=1, prefix=64,
                         time_dim=256)
     loop, held = fmv.from_case(c)
