@@ -93,6 +93,43 @@ def step_work(g: dict, batch: int, prefix: int):
 
 KCLASS = {"qkv_gemm": 1, "attention": 2, "o_gemm": 3, "up_gemm": 4, "down_gemm": 5}
 
+# DRAM bytes (read + write) per launch of a kernel class, from one `ncu --set full`
+# capture (profiles/pi05_b1_kernels_full.md, profiles/pi05_b32_kernels_full.md),
+# with the SHA-1 prefixes of the sources those kernels were built from: a value
+# is reported only while every listed source is unchanged.
+_GEMM_SRC = {"gemm_tc.cu": "7b6258111770fb71", "epilogue.cuh": "4ef82817124f9117"}
+_ATTN_SRC = {"attention_tc5.cu": "385ad902f0a25be4"}
+TRAFFIC = {
+    ("pi05", "attention"): (1.29e6 + 1.89e6, _ATTN_SRC),   # attention + split merge
+    ("pi05", "o_gemm"): (4.47e6, _GEMM_SRC),
+    ("pi05", "up_gemm"): (16.96e6, _GEMM_SRC),
+    ("pi05", "down_gemm"): (8.87e6, _GEMM_SRC),
+    ("pi05_b32", "qkv_gemm"): (8.66e6, _GEMM_SRC),
+    ("pi05_b32", "attention"): (39.95e6, _ATTN_SRC),
+    ("pi05_b32", "o_gemm"): (10.82e6, _GEMM_SRC),
+    ("pi05_b32", "up_gemm"): (20.14e6, _GEMM_SRC),
+    ("pi05_b32", "down_gemm"): (21.57e6, _GEMM_SRC),
+}
+
+
+def measured_traffic(workload: str, kernel: str):
+    """Per-launch DRAM bytes of ``kernel`` from the committed capture, or None when
+    there is none for this workload or a listed source changed since."""
+    import hashlib
+    ent = TRAFFIC.get((workload, kernel))
+    if ent is None:
+        return None
+    nbytes, srcs = ent
+    csrc = os.path.join(ROOT, "flow_matching_vla_gb300", "csrc")
+    for name, digest in srcs.items():
+        try:
+            with open(os.path.join(csrc, name), "rb") as f:
+                if hashlib.sha1(f.read()).hexdigest()[:16] != digest:
+                    return None
+        except OSError:
+            return None
+    return nbytes
+
 
 # ----------------------------------------------------------------------------
 # clocks during the timed region
@@ -381,7 +418,8 @@ def main(argv=None):
             else:
                 achieved, peak, unit = d["bytes"] / t / 1e9, hbm_peak, "GB/s"
             roofline = {"kernel": dom, "bound": "tensor" if tensor else "hbm", "achieved": achieved,
-                        "peak": peak, "unit": unit, "frac": achieved / peak, "traffic": None,
+                        "peak": peak, "unit": unit, "frac": achieved / peak,
+                        "traffic": measured_traffic(args.workload, dom),
                         "peak_source": peak_src, "avg_launch_us": d["avg_us"],
                         "algorithmic_bytes_per_launch": d["bytes"],
                         "algorithmic_flops_per_launch": d["flops"]}

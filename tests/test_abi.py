@@ -123,3 +123,15 @@ def test_bench_work_accounting_matches_weight_shapes():
     assert gemm_weight_bytes < total_w < gemm_weight_bytes * 1.08   # + activations
     kv = w["attention"][0] * w["attention"][1]
     assert kv > 18 * 968 * 256 * 2 * 2
+
+
+def test_bench_traffic_needs_unchanged_sources(monkeypatch):
+    import bench
+    assert bench.measured_traffic("no_such_workload", "attention") is None
+    for (w, k), (nbytes, srcs) in bench.TRAFFIC.items():
+        assert nbytes > 0 and srcs and k in bench.KCLASS
+    # a digest that no longer matches the source hides the number
+    key = next(iter(bench.TRAFFIC))
+    nbytes, srcs = bench.TRAFFIC[key]
+    monkeypatch.setitem(bench.TRAFFIC, key, (nbytes, {name: "0" * 16 for name in srcs}))
+    assert bench.measured_traffic(*key) is None
