@@ -40,7 +40,10 @@ namespace {
 
 constexpr int ROWS = 128;   // folded query rows per CTA (MMA M)
 constexpr int KT = 64;      // keys per tile (MMA N of S, K of PV)
-constexpr int kThreads = 224;   // warp 0: K loads, 1: MMA, 2..5: softmax, 6: V loads
+// warp 0: K loads, 1: MMA, 2..9: softmax (two warps per TMEM lane quadrant, one per
+// half of the keys of a tile and of O's columns), 10: V loads
+constexpr int kThreads = 352;
+constexpr int kSlack = 256;   // alignment slack of the dynamic shared memory (checked)
 
 template <int DH>
 struct T5Smem {
@@ -52,9 +55,10 @@ struct T5Smem {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = Q_BYTES;
   static constexpr int OFF_P = OFF_KV + 2 * STAGE;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2;
-  static constexpr int TOTAL = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static constexpr int OFF_X = OFF_P + 2 * P_BYTES;   // row-maximum exchange [2 parities][2 halves][ROWS]
+  static constexpr int OFF_BAR = OFF_X + 2 * 2 * ROWS * 4;
+  static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 8;
+  static constexpr int TOTAL = OFF_BAR + NBAR * 8 + 16 + kSlack;
 };
 
 // MN-major (V) descriptor: 64-element rows of 128 bytes along N in groups of 8 K-rows
@@ -85,6 +89,25 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// One TMA request per tile: a tensor copy keeps its issuing thread busy for a
+// fixed time (~0.25 us measured) whatever its size, so whole tiles move in one
+// request rather than one per 64-column box.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(ptx::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z,
+                                            int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(ptx::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
@@ -123,6 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = T5Smem<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (smem - smem_raw > kSlack) {   // the layout assumes (almost) 1024-byte aligned dynamic memory
+    if (threadIdx.x == 0) atomicExch(a.err, 1);
+    return;
+  }
   uint8_t* sQ = smem + L::OFF_Q;
   uint8_t* sKV = smem + L::OFF_KV;
   uint8_t* sP = smem + L::OFF_P;
@@ -136,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = bars + 11;  // [2] the PV reading P buffer b completed
   uint64_t* v_full = bars + 13;   // [2] V tile of ring slot landed
   uint64_t* v_empty = bars + 15;  // [2] PV read it
+  uint64_t* x_bar = bars + 17;    // [4 quadrants][2 parities] the two halves of a row exchanged
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
+  float* xm = reinterpret_cast<float*>(smem + L::OFF_X);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int S = (int)gridDim.y;
@@ -160,12 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&v_full[i], 1);
       ptx::mbar_init(&v_empty[i], 1);
       ptx::mbar_init(&s_full[i], 1);
-      ptx::mbar_init(&s_empty[i], 4);
+      ptx::mbar_init(&s_empty[i], 8);
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&p_full[i], 4);
+      ptx::mbar_init(&p_full[i], 8);
       ptx::mbar_init(&pv_done[i], 1);
     }
+    for (int i = 0; i < 8; ++i) ptx::mbar_init(&x_bar[i], 64);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmQ);
@@ -187,8 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicExch(a.err, 1);
   };
 
-  if (warp == 0 || warp == 6) {
-    // ---------------- TMA producers: warp 0 streams K tiles, warp 6 V tiles ----------------
+  if (warp == 0 || warp == 10) {
+    // ---------------- TMA producers: warp 0 streams K tiles, warp 10 V tiles ----------------
     if (lane == 0) {
       const bool is_k = warp == 0;
       uint64_t* full = is_k ? k_full : v_full;
@@ -197,14 +227,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const KeyTile kt = key_tile(t_begin + i, b, a.P, a.H);
         uint8_t* dst = sKV + st * L::STAGE + (is_k ? 0 : L::KV_BYTES);
         ptx::mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
-        for (int x = 0; x < L::BOXES; ++x) {
-          if (kt.prefix)
-            ptx::tma_load_2d(dst + x * KT * 128, is_k ? &tmKp : &tmVp, &full[st], x * 64, kt.row,
-                             ptx::policy_evict_first());
-          else
-            ptx::tma_load_2d(dst + x * KT * 128, is_k ? &tmKs : &tmVs, &full[st], (is_k ? a.k_off : a.v_off) + x * 64,
-                             kt.row, ptx::policy_evict_last());
-        }
+        // [Dh/64 boxes][KT rows][64 columns] in one request (3-D map: columns, rows, boxes)
+        if (kt.prefix)
+          tma_load_3d_hint(dst, is_k ? &tmKp : &tmVp, &full[st], 0, kt.row, 0, ptx::policy_evict_first());
+        else
+          tma_load_3d_hint(dst, is_k ? &tmKs : &tmVs, &full[st], 0, kt.row, 0, ptx::policy_evict_last());
       };
       // bound prefix tiles do not depend on the previous kernel: stage them first
       int pre = 0;
@@ -215,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_k) {
         ptx::mbar_arrive_expect_tx(q_full, L::Q_BYTES);
         const int tokens_per_tile = ROWS / a.Hq;
-        for (int x = 0; x < L::BOXES; ++x)
-          tma_load_3d(sQ + x * ROWS * 128, &tmQ, q_full, x * 64, 0, b * a.H + blockIdx.x * tokens_per_tile);
+        // [Dh/64 boxes][tokens][heads][64 columns]: folded row r = t * Hq + h, one request
+        tma_load_4d(sQ, &tmQ, q_full, 0, 0, b * a.H + blockIdx.x * tokens_per_tile, 0);
       }
       int loaded = pre;
       for (int i = pre; i < nt && !*abort_flag; ++i) {
@@ -273,48 +300,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- softmax (warps 2..5: TMEM lane quadrant = warp % 4) ----------------
-    ptx::pdl_wait();
-    const int quad = warp & 3;
+    // ---------------- softmax (warps 2..9: TMEM lane quadrant = warp % 4) ----------------
+    const int quad = warp & 3, g = (warp - 2) >> 2;   // g: which half of the keys / of O's columns
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    constexpr int OH = DH / 2;                          // O columns per half
     const float sl2 = rsqrtf((float)DH) * 1.4426950408889634f;
-    float m_used = -INFINITY, l = 0.f;
+    // the two threads of a row swap a value through shared memory; exchange e
+    // uses parity e & 1 of this quadrant's barrier pair (64 arrivals, bounded wait)
+    auto exchange = [&](int e, float mine) -> float {
+      const int par = e & 1;
+      xm[(par * 2 + g) * ROWS + row] = mine;
+      ptx::mbar_arrive(&x_bar[quad * 2 + par]);
+      if (!ptx::mbar_wait(&x_bar[quad * 2 + par], (e >> 1) & 1, lim)) fail();
+      return xm[(par * 2 + (g ^ 1)) * ROWS + row];
+    };
+    ptx::pdl_wait();
+    float m_used = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
     for (int j = 0; j < nt; ++j) {
       const int sb = j & 1;
       if (!ptx::mbar_wait(&s_full[sb], (j >> 1) & 1, lim)) { fail(); break; }
       ptx::tc_fence_after();
-      float sv[64];
-      {
-        float v0[32], v1[32];
-        ptx::tmem_ld32(tS + sb * KT + lane_off, v0);
-        ptx::tmem_ld32(tS + sb * KT + 32 + lane_off, v1);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          sv[c] = v0[c];
-          sv[32 + c] = v1[c];
-        }
-      }
+      float sv[32];
+      ptx::tmem_ld32(tS + sb * KT + 32 * g + lane_off, sv);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s_empty[sb]);
-      const int valid = key_tile(t_begin + j, b, a.P, a.H).valid;
-      // tile maximum of the raw scores (4 independent chains); keys past the tile end masked
+      const int valid = key_tile(t_begin + j, b, a.P, a.H).valid - 32 * g;   // keys of this half in range
+      // half-tile maximum of the raw scores (4 independent chains); keys past the tile end masked
       float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         if (c >= valid) sv[c] = -INFINITY;
         mq[c & 3] = fmaxf(mq[c & 3], sv[c]);
       }
-      const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
+      const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
+      const float mt = fmaxf(mh, exchange(j, mh));
       // raise the running maximum only when this tile exceeds it by more than 2^8
       const bool raise = mt > m_used + 8.f;
       const float m_new = raise ? mt : m_used;
       const float corr = raise ? ex2_approx(m_used - m_new) : 1.f;   // 0 on the first tile
       float pq[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
+      for (int c = 0; c < 32; c += 2) {
         // p = 2^(s * log2e / sqrt(d) - m): the scale folded into one fma
         const float p0 = ex2_approx(fmaf(sv[c], sl2, -m_new));
         const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, -m_new));
@@ -322,18 +351,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
         pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      const float ps = (pq[0] + pq[1]) + (pq[2] + pq[3]);
-      l = l * corr + ps;
+      l = l * corr + ((pq[0] + pq[1]) + (pq[2] + pq[3]));
       const int pb = j & 1;
       // P buffer pb is free once PV(j-2) has completed
       if (j >= 2 && !ptx::mbar_wait(&pv_done[pb], ((j - 2) >> 1) & 1, lim)) { fail(); break; }
-      const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
+      const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);   // same in both warps of the rows
       // O is stable once PV(j-1) has completed: needed only to rescale it
       if (rescale && !ptx::mbar_wait(&pv_done[pb ^ 1], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
       ptx::tc_fence_after();
-      if (rescale) {  // rescale this warp's O rows in TMEM
+      if (rescale) {  // rescale this warp's half of its O rows in TMEM
 #pragma unroll 1
-        for (int c0 = 0; c0 < DH; c0 += 32) {
+        for (int c0 = g * OH; c0 < g * OH + OH; c0 += 32) {
           float o[32];
           ptx::tmem_ld32(tO + c0 + lane_off, o);
 #pragma unroll
@@ -342,11 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       m_used = m_new;
-      // P row -> shared memory, K-major 128-byte swizzled (16-byte chunk c at c ^ (row % 8))
+      // this half of the P row -> shared memory, K-major 128-byte swizzled (chunk c at c ^ (row % 8))
       uint4* prow = reinterpret_cast<uint4*>(sP + pb * L::P_BYTES + row * 128);
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        prow[c ^ (row & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < 4; ++c)
+        prow[(4 * g + c) ^ (row & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
       ptx::tc_fence_before();
       __syncwarp();
@@ -355,53 +383,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the last PV (it follows every earlier one on the tensor pipe)
     if (nt > 0 && !*abort_flag && !ptx::mbar_wait(&pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, lim)) fail();
     ptx::tc_fence_after();
-    // l over the row is complete in-thread (one thread per row)
+    l += exchange(nt, l);   // the whole row's sum (both halves add the same two numbers)
     const int gr = r0 + row;
     const bool aborted = *abort_flag != 0;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    bf16* dst;
     if (S == 1) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
       const int t = gr / a.Hq, h = gr % a.Hq;
-      bf16* orow = (bf16*)a.out + ((long long)b * a.H + t) * a.ldo + h * DH;
-#pragma unroll 1
-      for (int c0 = 0; c0 < DH; c0 += 32) {
-        float o[32];
-        if (nt > 0 && !aborted) {
-          ptx::tmem_ld32(tO + c0 + lane_off, o);
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0.f;
-        }
-        if (gr < nrows) {
-#pragma unroll
-          for (int c = 0; c < 32; c += 8) {
-            uint4 w;
-            uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(o[c + 2 * q] * inv, o[c + 2 * q + 1] * inv);
-              wp[q] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            *reinterpret_cast<uint4*>(orow + c0 + c) = w;
-          }
-        }
-      }
+      dst = (bf16*)a.out + ((long long)b * a.H + t) * a.ldo + h * DH;
     } else {
       // this split's partial -> workspace: O / l as bf16 and (max, sum);
       // attn_t5_combine merges the S splits of every row
       const long long tiles = (long long)gridDim.x * gridDim.z;
       const long long slot = ((long long)b * gridDim.x + blockIdx.x) * S + split;
-      bf16* wrow = reinterpret_cast<bf16*>(a.ws) + (slot * ROWS + row) * DH;
+      dst = reinterpret_cast<bf16*>(a.ws) + (slot * ROWS + row) * DH;
       float2* wml = reinterpret_cast<float2*>(reinterpret_cast<bf16*>(a.ws) + tiles * S * ROWS * DH);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (g == 0) wml[slot * ROWS + row] = make_float2(nt > 0 ? m_used : -INFINITY, l);
+    }
+    const bool store = S > 1 || gr < nrows;
 #pragma unroll 1
-      for (int c0 = 0; c0 < DH; c0 += 32) {
-        float o[32];
-        if (nt > 0 && !aborted) {
-          ptx::tmem_ld32(tO + c0 + lane_off, o);
-        } else {
+    for (int c0 = g * OH; c0 < g * OH + OH; c0 += 32) {
+      float o[32];
+      if (nt > 0 && !aborted) {
+        ptx::tmem_ld32(tO + c0 + lane_off, o);
+      } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0.f;
-        }
+        for (int c = 0; c < 32; ++c) o[c] = 0.f;
+      }
+      if (store) {
 #pragma unroll
         for (int c = 0; c < 32; c += 8) {
           uint4 w;
@@ -411,10 +420,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat162 h2 = __floats2bfloat162_rn(o[c + 2 * q] * inv, o[c + 2 * q + 1] * inv);
             wp[q] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          *reinterpret_cast<uint4*>(wrow + c0 + c) = w;
+          *reinterpret_cast<uint4*>(dst + c0 + c) = w;
         }
       }
-      wml[slot * ROWS + row] = make_float2(nt > 0 ? m_used : -INFINITY, l);
     }
   }
 
@@ -511,7 +519,7 @@ cudaError_t encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* 
                                                      cudaEnableDefault, &q);
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode5) return cudaErrorNotSupported;
   }
-  cuuint32_t es[3] = {1, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = g_encode5(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -545,25 +553,28 @@ long long attn_t5_workspace_floats(const AttnT5Args& a, int S) {
 //       [3] suffix K, [4] suffix V (2-D over qkv [B*H][ldq]; x offsets k_off / v_off)
 cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, CUtensorMap* maps) {
   const int D = a.Dh;
-  const cuuint64_t qd[3] = {(cuuint64_t)D, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.H};
-  const cuuint64_t qs[2] = {(cuuint64_t)D * 2, (cuuint64_t)a.ldq * 2};
-  const cuuint32_t qb[3] = {64, (cuuint32_t)a.Hq, (cuuint32_t)(ROWS / a.Hq)};
-  cudaError_t e = encode(&maps[0], a.qkv, 3, qd, qs, qb);
+  const cuuint32_t nbox = (cuuint32_t)(D / 64);
+  // Q: (64 columns, heads, tokens, Dh/64 boxes) over the q columns of qkv
+  const cuuint64_t qd[4] = {64, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.H, nbox};
+  const cuuint64_t qs[3] = {(cuuint64_t)D * 2, (cuuint64_t)a.ldq * 2, 128};
+  const cuuint32_t qb[4] = {64, (cuuint32_t)a.Hq, (cuuint32_t)(ROWS / a.Hq), nbox};
+  cudaError_t e = encode(&maps[0], a.qkv, 4, qd, qs, qb);
   if (e != cudaSuccess) return e;
-  const cuuint32_t kb[2] = {64, KT};
+  // K / V tiles: (64 columns, rows, Dh/64 boxes), box = one 64-key tile
+  const cuuint32_t kb[3] = {64, KT, nbox};
   const long long prow = (long long)a.B * (a.P > 0 ? a.P : 1);
-  const cuuint64_t pd[2] = {(cuuint64_t)D, (cuuint64_t)prow};
-  const cuuint64_t ps[1] = {(cuuint64_t)D * 2};
+  const cuuint64_t pd[3] = {64, (cuuint64_t)prow, nbox};
+  const cuuint64_t ps[2] = {(cuuint64_t)D * 2, 128};
   // with no prefix the prefix maps are never used: point them at the suffix rows
-  e = encode(&maps[1], a.P > 0 ? kp : a.qkv, 2, pd, ps, kb);
+  e = encode(&maps[1], a.P > 0 ? kp : a.qkv, 3, pd, ps, kb);
   if (e != cudaSuccess) return e;
-  e = encode(&maps[2], a.P > 0 ? vp : a.qkv, 2, pd, ps, kb);
+  e = encode(&maps[2], a.P > 0 ? vp : a.qkv, 3, pd, ps, kb);
   if (e != cudaSuccess) return e;
-  const cuuint64_t sd[2] = {(cuuint64_t)a.ldq, (cuuint64_t)a.B * a.H};
-  const cuuint64_t ss[1] = {(cuuint64_t)a.ldq * 2};
-  e = encode(&maps[3], a.qkv, 2, sd, ss, kb);
+  const cuuint64_t sd[3] = {64, (cuuint64_t)a.B * a.H, nbox};
+  const cuuint64_t ss[2] = {(cuuint64_t)a.ldq * 2, 128};
+  e = encode(&maps[3], static_cast<const bf16*>(a.qkv) + a.k_off, 3, sd, ss, kb);
   if (e != cudaSuccess) return e;
-  return encode(&maps[4], a.qkv, 2, sd, ss, kb);
+  return encode(&maps[4], static_cast<const bf16*>(a.qkv) + a.v_off, 3, sd, ss, kb);
 }
 
 cudaError_t attention_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl) {
