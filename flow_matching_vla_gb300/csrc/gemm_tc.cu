@@ -665,6 +665,9 @@ cudaError_t tc_make_map(CUtensorMap* m, const void* ptr, long long rows, long lo
 TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split, bool partial) {
   TcPlan p;
   p.BN = M <= 64 ? 64 : (M <= 128 ? 128 : 256);
+  // unsplit GEMMs whose 256-token tiles leave more than half the SMs idle: halve
+  // the tiles (still one wave) to put twice the SMs on the weights
+  if (p.BN == 256 && !partial && 2LL * ((N + BM - 1) / BM) * ((M + 255) / 256) <= sm_count) p.BN = 128;
   const int KB = K / BK;
   const long long tiles = (long long)((N + BM - 1) / BM) * ((M + p.BN - 1) / p.BN);
   // a CTA fills an SM's shared memory: the split stays within one wave.  A

@@ -19,7 +19,10 @@
 #include "gr00t.h"
 #include "kernels.h"
 
-using namespace g3;
+using // Size (fp32 elements) of the fixed scratch array of the allocation-free step.
+#define G3_NOALLOC_SCRATCH_FLOATS (3 << 20)
+
+namespace g3;
 
 struct gr00t_ctx {
   gr00t_geometry g{};
@@ -82,6 +85,7 @@ struct gr00t_ctx {
   int opt_pdl = 1;
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
   int opt_l2_ahead = 0;     // each layer's first GEMM prefetches the next layer into L2 (off: measured slower)
+  long long noalloc_limit = -1;   // scratch bound of the allocation-free step (-1: the whole fixed array)
   int split_cap = 4;        // GEMMs that reduce their split-K partials in-kernel
   int resid_split_cap = 8;  // residual GEMMs whose partials the next kernel folds in
 
@@ -975,6 +979,11 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
     case GR00T_OPT_L2_PREFETCH:
       c->opt_l2_ahead = value ? 1 : 0;
       break;
+    case GR00T_OPT_NOALLOC_LIMIT:
+      if (value < 0 || value > G3_NOALLOC_SCRATCH_FLOATS)
+        return set_err(c, GR00T_EINVAL, "no-alloc limit: 0 .. %lld floats", (long long)G3_NOALLOC_SCRATCH_FLOATS);
+      c->noalloc_limit = value;
+      break;
     case GR00T_OPT_SPLIT_CAP:
     case GR00T_OPT_RESID_SPLIT_CAP:
       if (value < 1 || value > 16 || (value & (value - 1))) return set_err(c, GR00T_EINVAL, "split cap: 1, 2, 4, 8 or 16");
@@ -1056,7 +1065,6 @@ extern "C" int gr00t_kernel_times(gr00t_ctx* c, float* ms, int max, int* count) 
 // image, 12 MiB of fp32 on every GPU that loads the library, held until the
 // process exits.  Host code cannot use the symbol itself as a device address;
 // its device address is looked up once per device with that device current.
-#define G3_NOALLOC_SCRATCH_FLOATS (3 << 20)
 static __device__ __align__(256) float g_noalloc_scratch[G3_NOALLOC_SCRATCH_FLOATS];
 
 namespace {
@@ -1135,12 +1143,13 @@ extern "C" int gr00t_denoise_step_noalloc(gr00t_ctx* c, int k, const float* x_in
     return set_err(c, GR00T_EINVAL, "device %d is current; the context lives on device %d", dev, c->device);
   // the step's launch sequence is the regular entry point's (planned against the
   // context's own scratch); it runs here only if its scratch fits the fixed array
-  const long long cap = G3_NOALLOC_SCRATCH_FLOATS;
+  const long long cap = c->noalloc_limit >= 0 ? c->noalloc_limit : G3_NOALLOC_SCRATCH_FLOATS;
   const long long need = step_scratch(c, c->gemm_ws_floats);
   if (need > cap)
     return set_err(c, GR00T_EINVAL,
-                   "this step needs %lld floats of scratch at batch %d, prefix %d; the fixed array holds %lld "
-                   "(use gr00t_denoise_step)", need, c->bB, c->bP, cap);
+                   "this step needs %lld floats of scratch at batch %d, prefix %d; the no-alloc bound is %lld of "
+                   "the fixed array's %lld (use gr00t_denoise_step)", need, c->bB, c->bP, cap,
+                   (long long)G3_NOALLOC_SCRATCH_FLOATS);
   float* scratch = nullptr;
   CK(c, noalloc_scratch(dev, &scratch));
   const size_t bytes = (size_t)c->bB * c->H * c->A * sizeof(float);

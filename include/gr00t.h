@@ -278,6 +278,10 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
 #define GR00T_OPT_PERSISTENT_GEMM 8 /* 1 (default): persistent tensor-core GEMM for unsplit shapes with > 64 tokens */
 #define GR00T_OPT_L2_PREFETCH 9   /* 1: each layer's first GEMM prefetches the next layer's weights (default 0)
                                      and prefix K/V into L2 */
+#define GR00T_OPT_NOALLOC_LIMIT 10 /* scratch (fp32 elements) gr00t_denoise_step_noalloc may take from its fixed
+                                      array: 0 .. 3 * 2^20 (default: the whole array).  With the split planner's
+                                      one-wave rule no step on a 152-SM GPU needs the whole array, so a lower
+                                      limit is how the refusal is exercised */
 int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
 
 #define GR00T_INFO_KERNELS_PER_STEP 1   /* kernel launches of one denoise step            */
