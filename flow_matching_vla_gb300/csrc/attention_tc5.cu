@@ -44,6 +44,7 @@ constexpr int KT = 64;      // keys per tile (MMA N of S, K of PV)
 // half of the keys of a tile and of O's columns), 10: V loads
 constexpr int kThreads = 352;
 constexpr int kSlack = 256;   // alignment slack of the dynamic shared memory (checked)
+constexpr int kMaxSplits = 32;   // key splits (a lane of the merge kernel's warp per split)
 
 template <int DH>
 struct T5Smem {
@@ -455,9 +456,9 @@ __global__ void __launch_bounds__(256) attn_t5_combine_kernel(AttnT5Args a, int 
   const bf16* part = reinterpret_cast<const bf16*>(a.ws);
   const float2* wml = reinterpret_cast<const float2*>(part + tiles * S * ROWS * DH);
   typedef typename std::conditional<PER == 8, uint4, typename std::conditional<PER == 4, uint2, uint32_t>::type>::type V;
-  V v[16];   // the partial rows, loaded together with the (max, sum) pairs
+  V v[kMaxSplits];   // the partial rows, loaded together with the (max, sum) pairs
 #pragma unroll
-  for (int sp = 0; sp < 16; ++sp)
+  for (int sp = 0; sp < kMaxSplits; ++sp)
     if (sp < S) v[sp] = *reinterpret_cast<const V*>(part + ((slot0 + sp) * ROWS + row) * DH + lane * PER);
   const float2 ml = lane < S ? wml[(slot0 + lane) * ROWS + row] : make_float2(-INFINITY, 0.f);
   float mx = ml.x;
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(256) attn_t5_combine_kernel(AttnT5Args a, int 
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
 #pragma unroll
-  for (int sp = 0; sp < 16; ++sp) {
+  for (int sp = 0; sp < kMaxSplits; ++sp) {
     if (sp >= S) break;
     const float ws = __shfl_sync(0xffffffffu, w, sp);
     const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[sp]);
@@ -531,12 +532,12 @@ cudaError_t encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* 
 bool attn_t5_supported(int Dh, int Hq) { return (Dh == 64 || Dh == 128 || Dh == 256) && Hq > 0 && ROWS % Hq == 0; }
 
 int attn_t5_splits(const AttnT5Args& a, int sm_count) {
-  // at most one CTA per SM and 16 splits; then as few splits as keep that many
+  // at most one CTA per SM and kMaxSplits splits; then as few splits as keep that many
   // key tiles per split, so no split is left empty
   const int tiles = (a.Hq * a.H + ROWS - 1) / ROWS * a.B;
   const int ntiles = (a.P + KT - 1) / KT + (a.H + KT - 1) / KT;
   int S = sm_count / (tiles > 0 ? tiles : 1);
-  S = S < 1 ? 1 : (S > 16 ? 16 : S);
+  S = S < 1 ? 1 : (S > kMaxSplits ? kMaxSplits : S);
   if (S > ntiles) S = ntiles > 0 ? ntiles : 1;
   const int tps = (ntiles + S - 1) / S;
   return tps > 0 ? (ntiles + tps - 1) / tps : 1;
@@ -579,7 +580,7 @@ cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, CU
 
 cudaError_t attention_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl) {
   if (a.B <= 0 || a.Hq * a.H <= 0) return cudaSuccess;
-  if (!attn_t5_supported(a.Dh, a.Hq) || S < 1 || S > 16) return cudaErrorInvalidValue;
+  if (!attn_t5_supported(a.Dh, a.Hq) || S < 1 || S > kMaxSplits) return cudaErrorInvalidValue;
   if (attn_t5_workspace_floats(a, S) > a.ws_floats) return cudaErrorInvalidValue;
   switch (a.Dh) {
     case 64: return launch_t5<64>(a, maps, S, s, pdl);
