@@ -134,13 +134,13 @@ __device__ __forceinline__ void epi_pair(const Epi& e, int m, int n, float a0, f
 // ---------------------------------------------------------------------------
 // Epilogue of one thread's output pairs for a run of token columns, with the
 // per-thread invariants hoisted (the thread's weight rows n, n+1 are fixed).
-// ``lo``/``hi`` give the pair (rows n, n+1) of column m0 + 2*jj + par, where
-// the thread handles every other column starting at parity ``par`` (the lane-
-// pair swap of the tensor-core epilogue).  Used by the tensor-core kernels.
+// Split into a branch-free compute() and a store(), so that a lane's 16 column
+// pairs form 16 independent dependency chains the compiler can interleave (a
+// guard around each pair serialises them: measured ~60 ns per pair).  ACT is
+// the activation of EPI_STORE.  Used by the tensor-core kernels.
 // ---------------------------------------------------------------------------
-template <int KIND>
+template <int KIND, int ACT = ACT_NONE>
 struct EpiRun {
-  // Called once per thread before the column loop.
   __device__ __forceinline__ EpiRun(const Epi& e, int n) : e_(e), n_(n) {
     if (KIND == EPI_STORE) {
       b0_ = e.bias ? e.bias[n] : 0.f;
@@ -157,37 +157,59 @@ struct EpiRun {
   }
   // RoPE (cos, sin) of token index j (j < tok_rope) for this thread's frequency.
   __device__ __forceinline__ float2 rope_cs(int j) const { return e_.rope_tab[j * half_ + i_]; }
-  // Column m (token row of the output); cs = rope_cs(m % tok_rope), loaded ahead by the caller.
-  __device__ __forceinline__ void operator()(int m, float2 cs, float a0, float a1) const {
+  // Outputs of the pair (a0, a1) = rows (n, n+1) of one token column.
+  __device__ __forceinline__ void compute(float a0, float a1, float2 cs, float& o0, float& o1) const {
     if (KIND == EPI_STORE) {
       a0 += b0_;
       a1 += b1_;
-      if (e_.act == ACT_SWISH) {
+      if (ACT == ACT_SWISH) {
         a0 = swishf(a0);
         a1 = swishf(a1);
-      } else if (e_.act == ACT_GELU) {
+      } else if (ACT == ACT_GELU) {
         a0 = gelu_tanh_fast(a0);
         a1 = gelu_tanh_fast(a1);
       }
+      o0 = a0;
+      o1 = a1;
+    } else if (KIND == EPI_ROPE) {
+      o0 = rope_ ? a0 * cs.x - a1 * cs.y : a0;
+      o1 = rope_ ? a1 * cs.x + a0 * cs.y : a1;
+    } else if (KIND == EPI_GEGLU) {
+      o0 = gelu_tanh_fast(a0) * a1;
+      o1 = 0.f;
+    } else {
+      o0 = a0;
+      o1 = a1;
+    }
+  }
+  // Store the outputs of token column m.
+  __device__ __forceinline__ void store(int m, float o0, float o1) const {
+    if (KIND == EPI_STORE) {
       const long long r = e_.rg ? (long long)(m / e_.rg) * e_.rs + e_.ro + m % e_.rg : (long long)m;
       if (e_.out_f32)
-        store_pair<float>((float*)e_.out + r * e_.ldo + n_, a0, a1);
+        store_pair<float>((float*)e_.out + r * e_.ldo + n_, o0, o1);
       else
-        store_pair<bf16>((bf16*)e_.out + r * e_.ldo + n_, a0, a1);
+        store_pair<bf16>((bf16*)e_.out + r * e_.ldo + n_, o0, o1);
     } else if (KIND == EPI_ROPE) {
       bf16* o = (bf16*)e_.out + (long long)m * e_.ldo;
       if (rope_) {
-        o[col0_] = __float2bfloat16_rn(a0 * cs.x - a1 * cs.y);
-        o[col0_ + half_] = __float2bfloat16_rn(a1 * cs.x + a0 * cs.y);
+        o[col0_] = __float2bfloat16_rn(o0);
+        o[col0_ + half_] = __float2bfloat16_rn(o1);
       } else {
-        store_pair<bf16>(o + n_, a0, a1);
+        store_pair<bf16>(o + n_, o0, o1);
       }
     } else if (KIND == EPI_GEGLU) {
-      ((bf16*)e_.out)[(long long)m * e_.ldo + (n_ >> 1)] = __float2bfloat16_rn(gelu_tanh_fast(a0) * a1);
-    } else {  // residual kinds
+      ((bf16*)e_.out)[(long long)m * e_.ldo + (n_ >> 1)] = __float2bfloat16_rn(o0);
+    } else {  // residual kinds: operands loaded here
       const EpiPre p = epi_prefetch<bf16>(e_, m, n_);
-      epi_pair<bf16>(e_, m, n_, a0, a1, p);
+      epi_pair<bf16>(e_, m, n_, o0, o1, p);
     }
+  }
+  // compute + store of one pair (callers with one pair at a time)
+  __device__ __forceinline__ void operator()(int m, float2 cs, float a0, float a1) const {
+    float o0, o1;
+    compute(a0, a1, cs, o0, o1);
+    store(m, o0, o1);
   }
   const Epi& e_;
   int n_;
@@ -199,10 +221,11 @@ struct EpiRun {
 // 32 accumulator columns c0..c0+31 of rows (n, n+1) held by a lane pair; this
 // lane finishes columns of parity ``odd``.  For RoPE the 16 (cos, sin) pairs
 // are loaded together up front (token index kept in [0, tok_rope), so every
-// load is in bounds even past M), not one dependent load per column.
-template <int KIND>
-__device__ __forceinline__ void epi_columns(const EpiRun<KIND>& run, const float (&v)[32], bool odd, int m_first,
-                                            int M, int tok_rope) {
+// load is in bounds even past M).  All 16 pairs are computed before any store,
+// unconditionally; only the stores are guarded.
+template <int KIND, int ACT>
+__device__ __forceinline__ void epi_columns(const EpiRun<KIND, ACT>& run, const float (&v)[32], bool odd,
+                                            int m_first, int M, int tok_rope) {
   float2 cs[16];
   if (KIND == EPI_ROPE) {
     int j = m_first % tok_rope;
@@ -214,13 +237,16 @@ __device__ __forceinline__ void epi_columns(const EpiRun<KIND>& run, const float
       if (j >= tok_rope) j -= tok_rope;
     }
   }
-  int m = m_first;
+  float o0[16], o1[16];
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
     const float send = odd ? v[c] : v[c + 1];
     const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-    if (m < M) run(m, KIND == EPI_ROPE ? cs[c >> 1] : make_float2(1.f, 0.f), odd ? recv : v[c], odd ? v[c + 1] : recv);
-    m += 2;
+    run.compute(odd ? recv : v[c], odd ? v[c + 1] : recv, KIND == EPI_ROPE ? cs[c >> 1] : make_float2(1.f, 0.f),
+                o0[c >> 1], o1[c >> 1]);
   }
+#pragma unroll
+  for (int q = 0; q < 16; ++q)
+    if (m_first + 2 * q < M) run.store(m_first + 2 * q, o0[q], o1[q]);
 }
 }  // namespace g3

@@ -77,7 +77,7 @@ __device__ __forceinline__ int part_idx(int r, int c) {
 // chunks swizzled by tile row) -- then the KIND epilogue.  One item is a row
 // pair and 4 consecutive tokens; the loops are kept rolled because this code
 // runs once per CTA on a cold instruction cache.
-template <int BN, int KIND>
+template <int BN, int KIND, int ACT = ACT_NONE>
 __device__ __forceinline__ void reduce_onchip(const Epi& e, const float* part, const float* recv, int S, int rank,
                                            int m0, int n0, int M, int N) {
   const int R = BM / S, pairs = R / 2, items = pairs * (BN / 4);
@@ -88,7 +88,7 @@ __device__ __forceinline__ void reduce_onchip(const Epi& e, const float* part, c
     const int rr = rank * R + 2 * p, j0 = 4 * q;
     const int n = n0 + rr;
     if (n >= N || m0 + j0 >= M) continue;
-    const EpiRun<KIND> run(e, n);
+    const EpiRun<KIND, ACT> run(e, n);
     float2 cs[4];
     if (KIND == EPI_ROPE) {
       int j = (m0 + j0) % tok;
@@ -110,9 +110,12 @@ __device__ __forceinline__ void reduce_onchip(const Epi& e, const float* part, c
       s1.x += u1.x; s1.y += u1.y; s1.z += u1.z; s1.w += u1.w;
     }
     const float a0[4] = {s0.x, s0.y, s0.z, s0.w}, a1[4] = {s1.x, s1.y, s1.z, s1.w};
+    float o0[4], o1[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) run.compute(a0[t], a1[t], KIND == EPI_ROPE ? cs[t] : make_float2(1.f, 0.f), o0[t], o1[t]);
 #pragma unroll
     for (int t = 0; t < 4; ++t)
-      if (m0 + j0 + t < M) run(m0 + j0 + t, KIND == EPI_ROPE ? cs[t] : make_float2(1.f, 0.f), a0[t], a1[t]);
+      if (m0 + j0 + t < M) run.store(m0 + j0 + t, o0[t], o1[t]);
   }
 }
 
@@ -161,17 +164,17 @@ __device__ __forceinline__ void reduce_rows(const Epi& e, const float* __restric
 }
 
 // Epilogue of accumulator columns [c_begin, c_end) of this warp's TMEM lanes.
-template <int KIND>
+template <int KIND, int ACT = ACT_NONE>
 __device__ __forceinline__ void tile_epilogue(const Epi& e, uint32_t taddr, int c_begin, int c_end, int m0,
                                               int n_even, int M, int N, bool odd) {
-  const EpiRun<KIND> run(e, n_even < N ? n_even : 0);
+  const EpiRun<KIND, ACT> run(e, n_even < N ? n_even : 0);
   const bool live = n_even < N;
   const int tok = KIND == EPI_ROPE ? e.tok_rope : 1;
 #pragma unroll 1
   for (int c0 = c_begin; c0 < c_end; c0 += 32) {
     float v[32];
     ptx::tmem_ld32(taddr + (uint32_t)c0, v);
-    epi_columns<KIND>(run, v, odd, m0 + c0 + (odd ? 1 : 0), live ? M : 0, tok);
+    epi_columns<KIND, ACT>(run, v, odd, m0 + c0 + (odd ? 1 : 0), live ? M : 0, tok);
   }
 }
 
@@ -335,7 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool odd = lane & 1;
     if (!aborted) {
       switch (e.kind) {
-        case EPI_STORE: tile_epilogue<EPI_STORE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        case EPI_STORE:
+          if (e.act == ACT_SWISH)
+            tile_epilogue<EPI_STORE, ACT_SWISH>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+          else if (e.act == ACT_GELU)
+            tile_epilogue<EPI_STORE, ACT_GELU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+          else
+            tile_epilogue<EPI_STORE, ACT_NONE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+          break;
         case EPI_ROPE: tile_epilogue<EPI_ROPE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
         case EPI_GEGLU: tile_epilogue<EPI_GEGLU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
         default: tile_epilogue<EPI_RESID>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
@@ -374,7 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!aborted && !*abort_flag) {
       switch (e.kind) {
-        case EPI_STORE: reduce_onchip<BN, EPI_STORE>(e, part, recv, S, rank, m0, n0, M, N); break;
+        case EPI_STORE:
+          if (e.act == ACT_SWISH)
+            reduce_onchip<BN, EPI_STORE, ACT_SWISH>(e, part, recv, S, rank, m0, n0, M, N);
+          else if (e.act == ACT_GELU)
+            reduce_onchip<BN, EPI_STORE, ACT_GELU>(e, part, recv, S, rank, m0, n0, M, N);
+          else
+            reduce_onchip<BN, EPI_STORE, ACT_NONE>(e, part, recv, S, rank, m0, n0, M, N);
+          break;
         case EPI_ROPE: reduce_onchip<BN, EPI_ROPE>(e, part, recv, S, rank, m0, n0, M, N); break;
         case EPI_GEGLU: reduce_onchip<BN, EPI_GEGLU>(e, part, recv, S, rank, m0, n0, M, N); break;
         default: reduce_onchip<BN, EPI_RESID>(e, part, recv, S, rank, m0, n0, M, N); break;
@@ -565,7 +582,14 @@ __global__ void __launch_bounds__(kPersThreads, 1)
       const int n_even = n0 + quad * 32 + (lane & ~1);
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN);
       switch (e.kind) {
-        case EPI_STORE: tile_epilogue<EPI_STORE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        case EPI_STORE:
+          if (e.act == ACT_SWISH)
+            tile_epilogue<EPI_STORE, ACT_SWISH>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+          else if (e.act == ACT_GELU)
+            tile_epilogue<EPI_STORE, ACT_GELU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+          else
+            tile_epilogue<EPI_STORE, ACT_NONE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+          break;
         case EPI_ROPE: tile_epilogue<EPI_ROPE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
         case EPI_GEGLU: tile_epilogue<EPI_GEGLU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
         default: tile_epilogue<EPI_RESID>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
