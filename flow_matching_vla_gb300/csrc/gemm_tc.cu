@@ -382,6 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicExch(abort_flag, 1);
       atomicExch(err, 1);
     }
+    // every copy into this CTA has landed: arrive now, wait at the end, so the
+    // barrier that keeps each source alive overlaps the reduction
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     if (!aborted && !*abort_flag) {
       switch (e.kind) {
         case EPI_STORE:
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         default: reduce_onchip<BN, EPI_RESID>(e, part, recv, S, rank, m0, n0, M, N); break;
       }
     }
-    cluster.sync();   // every copy out of this CTA has landed before it exits
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // every copy out of this CTA landed
   } else {
     // split-K: park the fp32 partial in the L2-resident workspace, one cluster
     // barrier (release/acquire orders the global writes), then each rank sums
