@@ -22,6 +22,7 @@ MLP_GELU, MLP_GEGLU = 0, 1
 MEM_HOST, MEM_DEVICE = 0, 1
 OPT_USE_GRAPH, OPT_GEMM_PATH, OPT_WAIT_LIMIT, OPT_ATTN_PATH, OPT_TIME_KERNEL = 1, 2, 3, 4, 5
 OPT_SPLIT_CAP, OPT_RESID_SPLIT_CAP, OPT_PERSISTENT_GEMM, OPT_L2_PREFETCH = 6, 7, 8, 9
+OPT_ATTN_SPLIT_CAP = 11
 OPT_NOALLOC_LIMIT = 10
 KCLASS_QKV_GEMM, KCLASS_ATTENTION, KCLASS_O_GEMM, KCLASS_UP_GEMM, KCLASS_DOWN_GEMM, KCLASS_NORM = 1, 2, 3, 4, 5, 6
 INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES, INFO_DEVICE_BYTES, INFO_ERROR_FLAG = 1, 2, 3, 4

@@ -109,6 +109,25 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
+// Tensor stores of a shared-memory tile (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(ptx::smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_5d(const CUtensorMap* m, const void* src, int x, int y, int z, int w,
+                                             int v) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(ptx::smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_drain() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
@@ -143,7 +162,8 @@ template <int DH>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_t5_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKp,
                    const __grid_constant__ CUtensorMap tmVp, const __grid_constant__ CUtensorMap tmKs,
-                   const __grid_constant__ CUtensorMap tmVs, AttnT5Args a) {
+                   const __grid_constant__ CUtensorMap tmVs, const __grid_constant__ CUtensorMap tmO,
+                   AttnT5Args a) {
   using L = T5Smem<DH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -204,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmVp);
     ptx::prefetch_tmap(&tmKs);
     ptx::prefetch_tmap(&tmVs);
+    ptx::prefetch_tmap(&tmO);
   }
   if (warp == 2) ptx::tmem_alloc(tmem_slot, 512);
   ptx::tc_fence_before();
@@ -385,23 +406,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nt > 0 && !*abort_flag && !ptx::mbar_wait(&pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, lim)) fail();
     ptx::tc_fence_after();
     l += exchange(nt, l);   // the whole row's sum (both halves add the same two numbers)
-    const int gr = r0 + row;
     const bool aborted = *abort_flag != 0;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    bf16* dst;
-    if (S == 1) {
-      const int t = gr / a.Hq, h = gr % a.Hq;
-      dst = (bf16*)a.out + ((long long)b * a.H + t) * a.ldo + h * DH;
-    } else {
+    long long slot = 0;
+    if (S > 1) {
       // this split's partial -> workspace: O / l as bf16 and (max, sum);
       // attn_t5_combine merges the S splits of every row
       const long long tiles = (long long)gridDim.x * gridDim.z;
-      const long long slot = ((long long)b * gridDim.x + blockIdx.x) * S + split;
-      dst = reinterpret_cast<bf16*>(a.ws) + (slot * ROWS + row) * DH;
+      slot = ((long long)b * gridDim.x + blockIdx.x) * S + split;
       float2* wml = reinterpret_cast<float2*>(reinterpret_cast<bf16*>(a.ws) + tiles * S * ROWS * DH);
       if (g == 0) wml[slot * ROWS + row] = make_float2(nt > 0 ? m_used : -INFINITY, l);
     }
-    const bool store = S > 1 || gr < nrows;
+    // O / l as bf16 into the idle Q buffer in the store map's layout: box j holds
+    // columns [64j, 64j + 64) as 128-byte rows (row = folded row), 16-byte chunk c
+    // of row r at chunk c ^ (r % 8); then one tensor store moves the whole tile
+    // (whole 128-byte lines instead of one scattered row segment per lane)
 #pragma unroll 1
     for (int c0 = g * OH; c0 < g * OH + OH; c0 += 32) {
       float o[32];
@@ -411,19 +430,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) o[c] = 0.f;
       }
-      if (store) {
+      uint8_t* dst = sQ + (c0 >> 6) * (ROWS * 128) + row * 128;
+      const int p0 = (c0 & 63) >> 3;   // first 16-byte chunk of these 32 columns in the box row
 #pragma unroll
-        for (int c = 0; c < 32; c += 8) {
-          uint4 w;
-          uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+      for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[c + 2 * q] * inv, o[c + 2 * q + 1] * inv);
-            wp[q] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          *reinterpret_cast<uint4*>(dst + c0 + c) = w;
+        for (int i = 0; i < 4; ++i) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(o[8 * q + 2 * i] * inv, o[8 * q + 2 * i + 1] * inv);
+          wp[i] = *reinterpret_cast<uint32_t*>(&h2);
         }
+        *reinterpret_cast<uint4*>(dst + (((p0 + q) ^ (row & 7)) << 4)) = w;
       }
+    }
+    fence_proxy_async_smem();
+    asm volatile("bar.sync 1, 256;" ::: "memory");   // the 8 softmax warps staged the tile
+    if (warp == 2 && lane == 0) {
+      if (S > 1)
+        tma_store_3d(&tmO, sQ, 0, (int)(slot * ROWS), 0);
+      else   // rows past this sample's H tokens fall outside the map and are dropped
+        tma_store_5d(&tmO, sQ, 0, 0, r0 / a.Hq, b, 0);
+      tma_store_drain();
     }
   }
 
@@ -504,7 +532,7 @@ cudaError_t launch_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaS
     configured = true;
   }
   cudaError_t e = launch_k(kern, dim3((a.Hq * a.H + ROWS - 1) / ROWS, S, a.B), dim3(kThreads), L::TOTAL, s, pdl,
-                           maps[0], maps[1], maps[2], maps[3], maps[4], a);
+                           maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
   if (e != cudaSuccess || S == 1) return e;
   const long long warps = (long long)a.B * a.Hq * a.H;
   return launch_k(attn_t5_combine_kernel<DH>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, pdl, a, S);
@@ -520,7 +548,7 @@ cudaError_t encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* 
                                                      cudaEnableDefault, &q);
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode5) return cudaErrorNotSupported;
   }
-  cuuint32_t es[4] = {1, 1, 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
   CUresult r = g_encode5(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -531,13 +559,14 @@ cudaError_t encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* 
 
 bool attn_t5_supported(int Dh, int Hq) { return (Dh == 64 || Dh == 128 || Dh == 256) && Hq > 0 && ROWS % Hq == 0; }
 
-int attn_t5_splits(const AttnT5Args& a, int sm_count) {
-  // at most one CTA per SM and kMaxSplits splits; then as few splits as keep that many
-  // key tiles per split, so no split is left empty
+int attn_t5_splits(const AttnT5Args& a, int sm_count, int cap) {
+  // at most one CTA per SM and kMaxSplits (or cap) splits; then as few splits as keep
+  // that many key tiles per split, so no split is left empty
   const int tiles = (a.Hq * a.H + ROWS - 1) / ROWS * a.B;
   const int ntiles = (a.P + KT - 1) / KT + (a.H + KT - 1) / KT;
   int S = sm_count / (tiles > 0 ? tiles : 1);
   S = S < 1 ? 1 : (S > kMaxSplits ? kMaxSplits : S);
+  if (cap > 0 && S > cap) S = cap;
   if (S > ntiles) S = ntiles > 0 ? ntiles : 1;
   const int tps = (ntiles + S - 1) / S;
   return tps > 0 ? (ntiles + tps - 1) / tps : 1;
@@ -551,8 +580,10 @@ long long attn_t5_workspace_floats(const AttnT5Args& a, int S) {
 }
 
 // maps: [0] Q (3-D over [B*H tokens][Hq][Dh] inside qkv), [1] prefix K, [2] prefix V ([B*P][Dh]),
-//       [3] suffix K, [4] suffix V (2-D over qkv [B*H][ldq]; x offsets k_off / v_off)
-cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, CUtensorMap* maps) {
+//       [3] suffix K, [4] suffix V (2-D over qkv [B*H][ldq]; x offsets k_off / v_off),
+//       [5] the output tile: S > 1 the workspace partials [slot * 128 + row][Dh], S = 1 the
+//           attention output [B][H][Hq][Dh] inside out (row stride ldo)
+cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, int S, CUtensorMap* maps) {
   const int D = a.Dh;
   const cuuint32_t nbox = (cuuint32_t)(D / 64);
   // Q: (64 columns, heads, tokens, Dh/64 boxes) over the q columns of qkv
@@ -575,7 +606,22 @@ cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, CU
   const cuuint64_t ss[2] = {(cuuint64_t)a.ldq * 2, 128};
   e = encode(&maps[3], static_cast<const bf16*>(a.qkv) + a.k_off, 3, sd, ss, kb);
   if (e != cudaSuccess) return e;
-  return encode(&maps[4], static_cast<const bf16*>(a.qkv) + a.v_off, 3, sd, ss, kb);
+  e = encode(&maps[4], static_cast<const bf16*>(a.qkv) + a.v_off, 3, sd, ss, kb);
+  if (e != cudaSuccess) return e;
+  if (S > 1) {
+    // (64 columns, partial rows, Dh/64 boxes): one 128-row tile per request
+    const long long rows = (long long)((a.Hq * a.H + ROWS - 1) / ROWS) * a.B * S * ROWS;
+    const cuuint64_t od[3] = {64, (cuuint64_t)rows, nbox};
+    const cuuint64_t os[2] = {(cuuint64_t)D * 2, 128};
+    const cuuint32_t ob[3] = {64, ROWS, nbox};
+    return encode(&maps[5], a.ws, 3, od, os, ob);
+  }
+  // (64 columns, heads, tokens, samples, Dh/64 boxes): a tile's folded rows in box order,
+  // tokens past H outside the map
+  const cuuint64_t od[5] = {64, (cuuint64_t)a.Hq, (cuuint64_t)a.H, (cuuint64_t)a.B, nbox};
+  const cuuint64_t os[4] = {(cuuint64_t)D * 2, (cuuint64_t)a.ldo * 2, (cuuint64_t)a.H * a.ldo * 2, 128};
+  const cuuint32_t ob[5] = {64, (cuuint32_t)a.Hq, (cuuint32_t)(ROWS / a.Hq), 1, nbox};
+  return encode(&maps[5], a.out, 5, od, os, ob);
 }
 
 cudaError_t attention_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl) {

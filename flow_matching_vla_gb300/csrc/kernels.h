@@ -151,10 +151,10 @@ struct AttnT5Args {
 #include <cuda.h>
 namespace g3 {
 bool attn_t5_supported(int Dh, int Hq);
-int attn_t5_splits(const AttnT5Args& a, int sm_count);
+int attn_t5_splits(const AttnT5Args& a, int sm_count, int cap = 0);   // cap > 0: at most cap splits
 long long attn_t5_workspace_floats(const AttnT5Args& a, int S);
-// maps[5]: Q, prefix K, prefix V, suffix K, suffix V
-cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, CUtensorMap* maps);
+// maps[6]: Q, prefix K, prefix V, suffix K, suffix V, the output tile (S: the key splits)
+cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, int S, CUtensorMap* maps);
 cudaError_t attention_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl);
 
 // ---- schedule / bind / create helpers --------------------------------------------

@@ -83,6 +83,7 @@ struct gr00t_ctx {
   long long gemm_ws_floats = 0;
   std::map<std::tuple<const void*, long long, long long, long long, int>, CUtensorMap> tmaps;
   int opt_pdl = 1;
+  int opt_attn_splits = 0;  // expert attention key-split cap (0: automatic)
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
   int opt_l2_ahead = 0;     // each layer's first GEMM prefetches the next layer into L2 (off: measured slower)
   long long noalloc_limit = -1;   // scratch bound of the allocation-free step (-1: the whole fixed array)
@@ -517,9 +518,9 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         a5.out = c->att; a5.ldo = c->qd;
         a5.ws = c->gemm_ws; a5.ws_floats = c->gemm_ws_floats;
         a5.err = c->err_flag; a5.wait_limit = c->wait_limit;
-        CUtensorMap maps[5];
-        CK(c, attn_t5_maps(a5, c->host_table[2 * l], c->host_table[2 * l + 1], maps));
-        const int splits = attn_t5_splits(a5, c->sm_count);
+        const int splits = attn_t5_splits(a5, c->sm_count, c->opt_attn_splits);
+        CUtensorMap maps[6];
+        CK(c, attn_t5_maps(a5, c->host_table[2 * l], c->host_table[2 * l + 1], splits, maps));
         if (splits > 1) ++c->launches;   // the split merge is a second kernel
         CK(c, attention_t5(a5, maps, splits, s, c->opt_pdl != 0));
       } else if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 2) && attn_fold_supported(c->Dh)) {
@@ -979,6 +980,10 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
     case GR00T_OPT_L2_PREFETCH:
       c->opt_l2_ahead = value ? 1 : 0;
       break;
+    case GR00T_OPT_ATTN_SPLIT_CAP:
+      if (value < 0 || value > 32) return set_err(c, GR00T_EINVAL, "attention split cap: 0 (automatic) .. 32");
+      c->opt_attn_splits = (int)value;
+      break;
     case GR00T_OPT_NOALLOC_LIMIT:
       if (value < 0 || value > G3_NOALLOC_SCRATCH_FLOATS)
         return set_err(c, GR00T_EINVAL, "no-alloc limit: 0 .. %lld floats", (long long)G3_NOALLOC_SCRATCH_FLOATS);
@@ -1121,7 +1126,7 @@ long long step_scratch(gr00t_ctx* c, long long cap) {
   if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 3) && attn_t5_supported(c->Dh, c->Hq)) {
     AttnT5Args a5;
     a5.B = B; a5.H = c->H; a5.Hq = c->Hq; a5.Dh = c->Dh; a5.P = c->bP;
-    take(attn_t5_workspace_floats(a5, attn_t5_splits(a5, c->sm_count)));
+    take(attn_t5_workspace_floats(a5, attn_t5_splits(a5, c->sm_count, c->opt_attn_splits)));
   } else if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 2) && attn_fold_supported(c->Dh)) {
     AttnFoldArgs af;
     af.B = B; af.H = c->H; af.Hq = c->Hq; af.Dh = c->Dh; af.P = c->bP;

@@ -282,6 +282,8 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
                                       array: 0 .. 3 * 2^20 (default: the whole array).  With the split planner's
                                       one-wave rule no step on a 152-SM GPU needs the whole array, so a lower
                                       limit is how the refusal is exercised */
+#define GR00T_OPT_ATTN_SPLIT_CAP 11 /* expert family, tcgen05 attention: at most this many key splits
+                                       (1 .. 32; 0 = automatic: as many as fill the SMs, up to 32) */
 int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
 
 #define GR00T_INFO_KERNELS_PER_STEP 1   /* kernel launches of one denoise step            */
