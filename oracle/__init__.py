@@ -28,7 +28,7 @@ listed in the repository's design notes (readings S1-S14).
 Pins: every function is checked in ``tests/test_oracle_pins.py`` against
 closed forms, invariants, library routines (torch CPU) or brute force.
 """
-from .ops import (gelu_tanh, swish, rms_norm, layer_norm, rope_rotate_half,
+from .ops import (gelu_tanh, swish, rms_norm, layer_norm, rope_rotate_half, e4m3_decode, dequantize_rows,
                   attention, error_metrics)
 from .schedule import schedule, euler, time_embedding, time_condition, modulation_table
 from .expert import expert_velocity, expert_denoise
@@ -40,5 +40,5 @@ __all__ = [
     "attention", "error_metrics", "schedule", "time_embedding",
     "time_condition", "modulation_table", "expert_velocity", "expert_denoise",
     "dit_velocity", "dit_denoise", "action_time_bias", "denoise", "velocity",
-    "euler",
+    "euler", "e4m3_decode", "dequantize_rows",
 ]

@@ -7,11 +7,15 @@ from __future__ import annotations
 
 import numpy as np
 
-from .ops import attention, gelu_tanh, rms_norm, rope_rotate_half
+from .ops import dequantize_rows, attention, gelu_tanh, rms_norm, rope_rotate_half
 from .schedule import euler, modulation_table
 
 
 def _w(w, name, dtype):
+    """Weight ``name`` as a real matrix: FP8 weights (codes with a ``.scale``
+    entry per output row) are dequantized, the rest are taken as stored."""
+    if name + ".scale" in w:
+        return dequantize_rows(w[name], w[name + ".scale"]).astype(dtype, copy=False)
     return w[name].astype(dtype, copy=False)
 
 

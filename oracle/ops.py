@@ -91,3 +91,27 @@ def error_metrics(a, a_ref):
     nr = float(np.linalg.norm(r))
     e_rel = float(np.linalg.norm(diff)) / nr if nr > 0 else float(np.linalg.norm(diff))
     return e_inf, e_rel
+
+
+def e4m3_decode(codes):
+    """Values of 8-bit E4M3 floating-point codes (the OCP 8-bit floating point
+    format that FP8 weight streaming uses, "pi0.5 Design", precision notes).
+
+    Bit 7 is the sign, bits 6..3 the exponent field e (bias 7), bits 2..0 the
+    mantissa field m.  e = 0: subnormal, (m / 8) * 2^-6.  e >= 1: (1 + m / 8) *
+    2^(e - 7).  The format has no infinities: e = 15 with m = 7 is NaN, so the
+    largest finite magnitude is (1 + 6/8) * 2^8 = 448.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & ((c & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+def dequantize_rows(codes, scales):
+    """W[n, k] = e4m3(codes[n, k]) * scales[n]: row-scaled FP8 weights ([out, in]
+    codes, one scale per output row) as the real matrix they stand for."""
+    return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[:, None]

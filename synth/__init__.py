@@ -39,13 +39,15 @@ DTYPE_FP32 = 0
 DTYPE_BF16 = 1
 MLP_GELU = 0
 MLP_GEGLU = 1
+WFMT_NATIVE = 0   # weights in the workload dtype
+WFMT_FP8 = 1      # per-layer projections as E4M3 codes + one fp32 scale per output row
 
 _BASE = dict(
     family=FAMILY_EXPERT, dtype=DTYPE_BF16, layers=2, hidden=256, q_heads=4,
     kv_heads=1, head_dim=64, mlp_dim=1024, mlp_kind=MLP_GELU, horizon=16,
     action_dim=8, state_tokens=0, batch=1, prefix=64, steps=4,
     time_dim=256, time_mlp=0, rope_theta=10000.0, norm_eps=1e-6,
-    direction=-1,
+    direction=-1, weight_format=WFMT_NATIVE,
 )
 
 
@@ -85,6 +87,18 @@ CONFIGS = {
                     kv_heads=8, head_dim=48, mlp_dim=1536, horizon=16,
                     action_dim=32, state_tokens=1, batch=2, prefix=300,
                     steps=4, time_dim=384, time_mlp=1, direction=+1),
+    # FP8 weight streaming (E4M3 per-layer projections): full-size and small
+    "pi05_fp8": _g(**dict(_PI05, weight_format=WFMT_FP8)),
+    "gr00t_fp8": _g(**dict(_GR00T, weight_format=WFMT_FP8)),
+    "small_fp8": _g(layers=2, hidden=256, q_heads=2, head_dim=256,
+                    mlp_dim=512, mlp_kind=MLP_GEGLU, horizon=50,
+                    action_dim=32, batch=3, prefix=200, steps=3,
+                    time_dim=256, time_mlp=1, weight_format=WFMT_FP8),
+    "small_dit_fp8": _g(family=FAMILY_DIT, layers=4, hidden=384, q_heads=8,
+                        kv_heads=8, head_dim=48, mlp_dim=1536, horizon=16,
+                        action_dim=32, state_tokens=1, batch=2, prefix=300,
+                        steps=4, time_dim=384, time_mlp=1, direction=+1,
+                        weight_format=WFMT_FP8),
     "small_dit_fp32": _g(family=FAMILY_DIT, dtype=DTYPE_FP32, layers=2,
                          hidden=192, q_heads=4, kv_heads=4, head_dim=48,
                          mlp_dim=768, horizon=16, action_dim=32,
@@ -233,12 +247,48 @@ def _normal(seed, name, shape, std, bf16):
     return _normal_many([(seed, name, shape, std, bf16)])[0]
 
 
+FP8_LAYERED = ("qkv_w", "o_w", "up_w", "down_w")   # the projections stored as E4M3 in FP8 workloads
+
+
+def _e4m3_codes(y: np.ndarray) -> np.ndarray:
+    """Storage codes of values |y| <= 448 in the E4M3 8-bit format (sign bit 7,
+    exponent field bits 6..3 with bias 7, mantissa bits 2..0; subnormals below
+    2^-6), magnitudes truncated toward zero.  Any code is a valid input: both
+    sides of the parity tests read the same codes."""
+    a = np.abs(y).astype(np.float64)
+    f, x = np.frexp(a)                       # a = f * 2^x, f in [0.5, 1)
+    normal = a >= 2.0 ** -6
+    e = np.clip(x + 6, 1, 15)                # biased exponent of a = 2f * 2^(x - 1)
+    m = np.clip(np.floor((2.0 * f - 1.0) * 8.0), 0, 7)
+    m = np.where(e == 15, np.minimum(m, 6), m)   # (15, 7) is NaN
+    sub = np.clip(np.floor(a * 2.0 ** 9), 0, 7)
+    mag = np.where(normal, e * 8 + m, sub).astype(np.uint8)
+    return np.where(y < 0, mag | np.uint8(0x80), mag).astype(np.uint8)
+
+
+def _to_fp8_rows(w: np.ndarray):
+    """(codes, scales) of a [out, in] matrix: scale = max |row| / 448 per row."""
+    amax = np.max(np.abs(w), axis=1).astype(np.float32)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    y = np.clip(w / scale[:, None], -448.0, 448.0)
+    return _e4m3_codes(y), scale
+
+
 def make_weights(g: dict, seed: int = 0, std: float = 0.02) -> dict:
-    """Weights ~N(0, std), rounded to bf16 for bf16 workloads (float32 arrays)."""
+    """Weights ~N(0, std), rounded to bf16 for bf16 workloads (float32 arrays).
+
+    FP8 workloads (``weight_format`` WFMT_FP8) store the per-layer projections
+    as uint8 E4M3 codes ``name`` plus float32 row scales ``name + '.scale'``.
+    """
     bf16 = g["dtype"] == DTYPE_BF16
     shapes = weight_shapes(g)
     arrs = _normal_many([(seed, "w." + k, s, std, bf16) for k, s in shapes.items()])
-    return dict(zip(shapes.keys(), arrs))
+    w = dict(zip(shapes.keys(), arrs))
+    if g.get("weight_format", WFMT_NATIVE) == WFMT_FP8:
+        for k in list(w):
+            if k.split(".")[0] in FP8_LAYERED:
+                w[k], w[k + ".scale"] = _to_fp8_rows(w[k])
+    return w
 
 
 def make_prefix_kv(g: dict, seed: int = 0, batch: int | None = None, prefix: int | None = None):

@@ -509,3 +509,76 @@ def test_modulation_table_shape_matches_contract():
     w = {k: np.zeros(s, np.float32) for k, s in synth.weight_shapes(g).items()
          if k.startswith(("cond", "time"))}
     assert oracle.modulation_table(g, w, 2, 3).shape == (6, 37, 3072)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) weights: decode, row scales, and the oracle's use of them
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    got = oracle.e4m3_decode(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def test_e4m3_decode_closed_forms():
+    d = lambda c: float(oracle.e4m3_decode(np.uint8(c)))
+    assert d(0x38) == 1.0 and d(0xB8) == -1.0
+    assert d(0x7E) == 448.0 and d(0xFE) == -448.0        # largest finite magnitude
+    assert d(0x08) == 2.0 ** -6 and d(0x01) == 2.0 ** -9   # smallest normal / subnormal
+    assert d(0x07) == 7 * 2.0 ** -9 and d(0x0F) == 1.875 * 2.0 ** -6
+    assert d(0x00) == 0.0 and math.copysign(1.0, d(0x80)) == -1.0
+    assert math.isnan(d(0x7F)) and math.isnan(d(0xFF))
+    v = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    assert np.all(np.diff(v) > 0)   # finite codes are ordered by magnitude
+
+
+def test_dequantize_rows_scales_each_output_row():
+    codes = np.full((3, 5), 0x38, np.uint8)    # 1.0
+    codes[1, 2] = 0xC0                          # -2.0
+    sc = np.array([0.5, 2.0, 3.0], np.float32)
+    W = oracle.dequantize_rows(codes, sc)
+    ref = np.repeat(sc[:, None].astype(np.float64), 5, axis=1)
+    ref[1, 2] = -4.0
+    np.testing.assert_array_equal(W, ref)
+
+
+def _dequantized(w8):
+    wd = {k: v for k, v in w8.items() if not k.endswith(".scale")}
+    for k in list(wd):
+        if k + ".scale" in w8:
+            wd[k] = oracle.dequantize_rows(w8[k], w8[k + ".scale"])
+        else:
+            wd[k] = wd[k].astype(np.float64)
+    return wd
+
+
+def test_fp8_expert_case_runs_on_the_dequantized_matrices():
+    c = synth.make_case("small_fp8", batch=2)
+    g, w8 = c["geom"], c["weights"]
+    assert w8["qkv_w.0"].dtype == np.uint8 and w8["qkv_w.0.scale"].dtype == np.float32
+    wd = _dequantized(w8)
+    B = g["batch"]
+    rows = oracle.modulation_table(g, wd, g["steps"], B)[B:2 * B]
+    v8 = expert_velocity(g, w8, c["x_noise"], rows, c["K"], c["V"])
+    vd = expert_velocity(g, wd, c["x_noise"], rows, c["K"], c["V"])
+    assert np.array_equal(v8, vd)
+    ref = torch_expert_velocity(g, wd, c["x_noise"], rows, c["K"], c["V"])
+    np.testing.assert_allclose(v8, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_fp8_dit_case_runs_on_the_dequantized_matrices():
+    c = synth.make_case("small_dit_fp8")
+    g, w8 = c["geom"], c["weights"]
+    wd = _dequantized(w8)
+    B = g["batch"]
+    rows = oracle.modulation_table(g, wd, g["steps"], B)[2 * B:3 * B]
+    atb = oracle.action_time_bias(g, wd, g["steps"])[2]
+    args = (c["x_noise"], rows, atb, c["K"], c["V"], c["text_mask"], c["image_mask"], c["state"])
+    v8 = dit_velocity(g, w8, *args)
+    assert np.array_equal(v8, dit_velocity(g, wd, *args))
+    np.testing.assert_allclose(v8, torch_dit_velocity(g, wd, *args), rtol=1e-10, atol=1e-12)
