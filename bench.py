@@ -43,6 +43,9 @@ WORKLOAD_TEXT = {
              "32x48 heads) and self-attention (1 state + 16 action tokens), hidden 1536, FF 6144, batch 1, 4 steps",
     "pi05_b32": "pi0.5-shaped expert as above at batch 32 (per-sample prefix 968), 10 steps",
     "pi05_long": "pi0.5-shaped expert, batch 8, prefix 4096 per sample, horizon 50, 10 steps",
+    "pi05_fp8": "pi0.5-shaped expert as pi05 with the per-layer projections streamed as E4M3 codes + fp32 "
+                "row scales (bf16 activations), batch 1, 10 steps",
+    "gr00t_fp8": "GR00T-N1.7-shaped DiT head as gr00t with E4M3 per-layer projections, batch 1, 4 steps",
     "tiny": "tiny expert, fp32: 2 layers, hidden 256, 4x64 heads, GeLU 1024, prefix 64, horizon 16, batch 1, 4 steps",
 }
 
@@ -54,6 +57,9 @@ WORKLOAD_TEXT = {
 def kernel_work(g: dict, batch: int, prefix: int):
     """Per kernel class: (launches per denoise step, bytes per launch, FLOPs per launch)."""
     es = 2 if g["dtype"] == synth.DTYPE_BF16 else 4
+    fp8 = g.get("weight_format", synth.WFMT_NATIVE) == synth.WFMT_FP8
+    ws = 1 if fp8 else es            # bytes per element of the per-layer projections
+    sc = 4 if fp8 else 0             # FP8: one fp32 scale per output row
     D, L, F, H, A = g["hidden"], g["layers"], g["mlp_dim"], g["horizon"], g["action_dim"]
     Hq, Dh = g["q_heads"], g["head_dim"]
     tok = H + g["state_tokens"]
@@ -69,10 +75,10 @@ def kernel_work(g: dict, batch: int, prefix: int):
 
     for l in range(L):
         nq = synth.qkv_rows(g, l)
-        add("qkv_gemm", 1, nq * D * es + M * D * es + M * nq * es, 2.0 * M * nq * D)
-        add("o_gemm", 1, D * qd * es + M * qd * es + M * D * 8 + batch * D * es, 2.0 * M * D * qd)
-        add("up_gemm", 1, up_rows * D * es + M * D * es + M * F * es, 2.0 * M * up_rows * D)
-        add("down_gemm", 1, D * F * es + M * F * es + M * D * 8 + batch * D * es, 2.0 * M * D * F)
+        add("qkv_gemm", 1, nq * (D * ws + sc) + M * D * es + M * nq * es, 2.0 * M * nq * D)
+        add("o_gemm", 1, D * (qd * ws + sc) + M * qd * es + M * D * 8 + batch * D * es, 2.0 * M * D * qd)
+        add("up_gemm", 1, up_rows * (D * ws + sc) + M * D * es + M * F * es, 2.0 * M * up_rows * D)
+        add("down_gemm", 1, D * (F * ws + sc) + M * F * es + M * D * 8 + batch * D * es, 2.0 * M * D * F)
         if dit and l % 2 == 0:
             keys, kv = prefix, batch * prefix * g["kv_heads"] * Dh * 2 * es
         elif dit:

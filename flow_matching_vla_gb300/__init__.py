@@ -32,7 +32,7 @@ from ._abi import (DTYPE_BF16, DTYPE_FP32, FAMILY_DIT, FAMILY_EXPERT, MLP_GEGLU,
                    OPT_ATTN_SPLIT_CAP,
                    INFO_DEVICE_BYTES, INFO_ERROR_FLAG, INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES,
                    KCLASS_ATTENTION, KCLASS_DOWN_GEMM, KCLASS_NORM, KCLASS_O_GEMM, KCLASS_QKV_GEMM,
-                   KCLASS_UP_GEMM)
+                   KCLASS_UP_GEMM, WFMT_NATIVE, WFMT_FP8)
 
 __all__ = ["DenoiseLoop", "Gr00tError", "validate_geometry", "load_library", "FAMILY_EXPERT",
            "FAMILY_DIT", "DTYPE_FP32", "DTYPE_BF16", "MLP_GELU", "MLP_GEGLU"]
@@ -65,6 +65,7 @@ def _geometry(g: dict) -> _abi.Geometry:
     s.max_steps = int(g.get("max_steps", g.get("steps", 1)))
     s.rope_theta = float(g.get("rope_theta", 10000.0))
     s.norm_eps = float(g.get("norm_eps", 1e-6))
+    s.weight_format = int(g.get("weight_format", WFMT_NATIVE))
     return s
 
 
@@ -123,17 +124,28 @@ class DenoiseLoop:
                 keep.append(t)
                 setattr(w, name, _ptr(t))
         arrays = {}
+        fp8 = int(geom.get("weight_format", WFMT_NATIVE)) == WFMT_FP8
         for name in _LAYERED:
-            ts = []
-            for l in range(L):
-                t = _storage_tensor(weights[f"{name}.{l}"], self.dtype_code)
-                if device_weights:
-                    t = t.cuda()
-                ts.append(t)
-            keep += ts
-            arr = (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
-            arrays[name] = arr
-            setattr(w, name, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
+            for suffix, field in (("", name), (".scale", name[:-1] + "s")):
+                if suffix and not fp8:
+                    continue
+                ts = []
+                for l in range(L):
+                    a = weights[f"{name}.{l}{suffix}"]
+                    if fp8 and not suffix:     # E4M3 codes, passed as stored
+                        t = a if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a))
+                        t = t.view(torch.uint8).contiguous()
+                    elif suffix:               # fp32 row scales
+                        t = _storage_tensor(a, DTYPE_FP32)
+                    else:
+                        t = _storage_tensor(a, self.dtype_code)
+                    if device_weights:
+                        t = t.cuda()
+                    ts.append(t)
+                keep += ts
+                arr = (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
+                arrays[field] = arr
+                setattr(w, field, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
         ctx = ctypes.c_void_p()
         with torch.cuda.device(self.stream.device):
             rc = self._lib.gr00t_create(ctypes.byref(self._g), ctypes.byref(w),

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(PKG)
 HEADER = os.path.join(ROOT, "include", "gr00t.h")
 LIB_PATH = os.path.join(PKG, "libgr00t.so")
 
-ABI_VERSION = 1
+ABI_VERSION = 2
+WFMT_NATIVE, WFMT_FP8 = 0, 1
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, EUNSUPPORTED, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 FAMILY_EXPERT, FAMILY_DIT = 0, 1
 DTYPE_FP32, DTYPE_BF16 = 0, 1
@@ -36,7 +37,7 @@ class Geometry(ctypes.Structure):
         "abi_version", "family", "dtype", "layers", "hidden", "q_heads", "kv_heads", "head_dim",
         "mlp_dim", "mlp_kind", "horizon", "action_dim", "state_tokens", "time_dim", "time_mlp",
         "direction", "max_batch", "max_prefix", "max_steps")] + [
-        ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float)]
+        ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float), ("weight_format", ctypes.c_int32)]
 
 
 _VP = ctypes.c_void_p
@@ -47,7 +48,8 @@ class Weights(ctypes.Structure):
     _fields_ = [("location", ctypes.c_int32)] + [(n, _VP) for n in (
         "time_mlp_in_w", "time_mlp_in_b", "time_mlp_out_w", "time_mlp_out_b", "cond_w", "cond_b",
         "action_in_w", "action_in_b", "enc_w1", "enc_b1", "enc_w2", "enc_b2", "enc_w3", "enc_b3",
-        "action_out_w", "action_out_b")] + [(n, _VPP) for n in ("qkv_w", "o_w", "up_w", "down_w")]
+        "action_out_w", "action_out_b")] + [(n, _VPP) for n in (
+        "qkv_w", "o_w", "up_w", "down_w", "qkv_s", "o_s", "up_s", "down_s")]
 
 
 # exported symbol -> (restype, argtypes)

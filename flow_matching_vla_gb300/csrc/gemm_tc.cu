@@ -19,6 +19,7 @@
 //  * Every mbarrier wait is bounded; on timeout the CTA records an error
 //    flag for the host, drains its own in-flight copies and exits normally.
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
 #include "epilogue.cuh"
@@ -35,13 +36,22 @@ constexpr int BM = 128;  // weight rows per CTA (MMA M)
 constexpr int BK = 64;   // K elements per stage: one 128-byte swizzle row of bf16
 constexpr int A_BYTES = BM * BK * 2;
 
-template <int BN, int STAGES>
+// F8: E4M3 weights.  A stage then covers 128 K elements: the producer streams
+// 128 x 128-byte code tiles into a 2-slot ring, five converter warps widen them
+// (exactly) into the bf16 A tile of the stage, and the MMA reads that.
+template <int BN, int STAGES, bool F8 = false>
 struct TcSmem {
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int BKX = F8 ? 2 * BK : BK;    // K elements per stage
+  static constexpr int A_STAGE = BM * BKX * 2;    // bf16 A tile(s) of a stage
+  static constexpr int B_BYTES = BN * BKX * 2;
+  static constexpr int STAGE_BYTES = A_STAGE + B_BYTES;
   static constexpr int PIPE = STAGES * STAGE_BYTES;
-  static constexpr int BAR = (2 * STAGES + 2) * 8 + 16;
-  static constexpr int TOTAL = PIPE + BAR + 1024;  // + alignment slack
+  static constexpr int RAW = F8 ? 2 : 0;          // E4M3 code tiles in flight
+  static constexpr int RAW_BYTES = BM * 128;
+  static constexpr int BAR_OFF = PIPE + RAW * RAW_BYTES;
+  static constexpr int NBAR = 2 * STAGES + 2 + (F8 ? STAGES + 2 * RAW : 0);
+  static constexpr int BAR = NBAR * 8 + 16;
+  static constexpr int TOTAL = BAR_OFF + BAR + 1024;  // + alignment slack
   // split-K reduced on chip: the idle pipeline holds this CTA's fp32 partial
   // tile and the row slices its peers send it (one tile's worth)
   static constexpr int PART_BYTES = BN * BM * 4;
@@ -163,10 +173,11 @@ __device__ __forceinline__ void reduce_rows(const Epi& e, const float* __restric
   }
 }
 
-// Epilogue of accumulator columns [c_begin, c_end) of this warp's TMEM lanes.
-template <int KIND, int ACT = ACT_NONE>
+// Epilogue of accumulator columns [c_begin, c_end) of this warp's TMEM lanes
+// (SCALED: each lane's accumulator row times ``sc``, the FP8 row scale).
+template <int KIND, int ACT = ACT_NONE, bool SCALED = false>
 __device__ __forceinline__ void tile_epilogue(const Epi& e, uint32_t taddr, int c_begin, int c_end, int m0,
-                                              int n_even, int M, int N, bool odd) {
+                                              int n_even, int M, int N, bool odd, float sc = 1.f) {
   const EpiRun<KIND, ACT> run(e, n_even < N ? n_even : 0);
   const bool live = n_even < N;
   const int tok = KIND == EPI_ROPE ? e.tok_rope : 1;
@@ -174,6 +185,10 @@ __device__ __forceinline__ void tile_epilogue(const Epi& e, uint32_t taddr, int 
   for (int c0 = c_begin; c0 < c_end; c0 += 32) {
     float v[32];
     ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+    if constexpr (SCALED) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= sc;
+    }
     epi_columns<KIND, ACT>(run, v, odd, m0 + c0 + (odd ? 1 : 0), live ? M : 0, tok);
   }
 }
@@ -194,21 +209,163 @@ inline L2Ahead l2_ahead(const GemmArgs& a) {
   return r;
 }
 
+// ---------------------------------------------------------------------------
+// E4M3 weights (GR00T_WFMT_FP8).  Roles: warp 0 streams the 128 x 128-byte code
+// tiles (no dependency wait: no kernel writes weights); warp 2 waits for the
+// previous kernel and streams the activation stages; warps 3..7 widen each code
+// tile into the stage's bf16 A tile; warp 1 issues the MMAs once both halves of
+// a stage are in place.  E4M3 -> f16 -> f32 -> bf16 is exact (3 mantissa bits,
+// exponents 2^-9 .. 2^8), so the MMA sums e4m3(code) * x exactly as the bf16
+// path sums w * x; the row scale is applied in the epilogue.
+// ---------------------------------------------------------------------------
+constexpr int kF8Converters = 5;   // warps 3..7
+
+// 16 E4M3 codes -> 16 bf16 (two 16-byte chunks).
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t f16x2;
+      const unsigned short pair = (unsigned short)(w[i] >> (16 * h));
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+      __half2 hv = *reinterpret_cast<__half2*>(&f16x2);
+      const float2 f = __half22float2(hv);
+      __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+      o[2 * i + h] = *reinterpret_cast<uint32_t*>(&b);
+    }
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 template <int BN, int STAGES>
+__device__ __forceinline__ void f8_main_loop(const CUtensorMap& tmW, const CUtensorMap& tmX, uint8_t* sA,
+                                             uint8_t* sB, uint8_t* sRaw, uint64_t* full, uint64_t* empty,
+                                             uint64_t* done, uint64_t* cvt_full, uint64_t* raw_full,
+                                             uint64_t* raw_empty, uint32_t tmem, int* abort_flag, int* err,
+                                             long long wait_limit, int n0, int m0, int kb0, int nkb, int warp,
+                                             int lane) {
+  using L = TcSmem<BN, STAGES, true>;
+  constexpr int RAW = L::RAW;
+  auto fail = [&]() {
+    atomicExch(abort_flag, 1);
+    atomicExch(err, 1);
+  };
+  if (warp == 0) {
+    if (lane == 0) {   // code tiles: [128 rows][128 bytes], 128-byte swizzle
+      const uint64_t pw = ptx::policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int r = i % RAW;
+        if (i >= RAW && !ptx::mbar_wait(&raw_empty[r], ((i / RAW) & 1) ^ 1, wait_limit)) {
+          fail();
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&raw_full[r], L::RAW_BYTES);
+        ptx::tma_load_2d(sRaw + r * L::RAW_BYTES, &tmW, &raw_full[r], (kb0 + i) * 128, n0, pw);
+        issued = i + 1;
+      }
+      if (*abort_flag)   // drain this thread's copies in flight (bounded)
+        for (int i = issued - 1; i >= 0 && i >= issued - RAW; --i)
+          ptx::mbar_wait(&raw_full[i % RAW], (i / RAW) & 1, wait_limit);
+    }
+  } else if (warp == 2) {
+    if (lane == 0) {   // activations: two 64-column boxes per stage, after the dependency wait
+      const uint64_t px = ptx::policy_evict_last();
+      ptx::pdl_wait();
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES && !ptx::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, wait_limit)) {
+          fail();
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&full[s], L::B_BYTES);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          ptx::tma_load_2d(sB + s * L::B_BYTES + h * (BN * 128), &tmX, &full[s], (kb0 + i) * 128 + h * 64, m0, px);
+        issued = i + 1;
+      }
+      if (*abort_flag)
+        for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
+          ptx::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, wait_limit);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % STAGES;
+        if (!ptx::mbar_wait(&full[s], (i / STAGES) & 1, wait_limit) ||
+            !ptx::mbar_wait(&cvt_full[s], (i / STAGES) & 1, wait_limit)) {
+          fail();
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {   // two 64-column boxes, four K-16 steps each
+          const uint64_t ad = ptx::sdesc_sw128(ptx::smem_u32(sA + s * L::A_STAGE + (k >> 2) * (BM * 128)));
+          const uint64_t bd = ptx::sdesc_sw128(ptx::smem_u32(sB + s * L::B_BYTES + (k >> 2) * (BN * 128)));
+          ptx::mma_bf16(tmem, ad + 2 * (k & 3), bd + 2 * (k & 3), idesc, (i | k) != 0);
+        }
+        ptx::mma_commit(&empty[s]);
+      }
+      ptx::mma_commit(done);
+    }
+  } else {
+    // converters: 16-byte chunk c of code row r (stored at chunk c ^ (r % 8))
+    // -> bf16 box c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1 (each ^ (r % 8))
+    const int ct = (int)threadIdx.x - 96;
+    for (int i = 0; i < nkb; ++i) {
+      const int r = i % RAW, s = i % STAGES;
+      if (!ptx::mbar_wait(&raw_full[r], (i / RAW) & 1, wait_limit) ||
+          (i >= STAGES && !ptx::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, wait_limit))) {
+        fail();
+        break;
+      }
+      const uint8_t* src = sRaw + r * L::RAW_BYTES;
+      uint8_t* dst = sA + s * L::A_STAGE;
+#pragma unroll 2
+      for (int q = ct; q < BM * 8; q += 32 * kF8Converters) {
+        const int row = q >> 3, c = q & 7, sw = row & 7;
+        const uint4 in = *reinterpret_cast<const uint4*>(src + row * 128 + ((c ^ sw) << 4));
+        uint4 lo, hi;
+        e4m3x16_to_bf16(in, lo, hi);
+        uint8_t* box = dst + (c >> 2) * (BM * 128) + row * 128;
+        *reinterpret_cast<uint4*>(box + (((2 * (c & 3)) ^ sw) << 4)) = lo;
+        *reinterpret_cast<uint4*>(box + (((2 * (c & 3) + 1) ^ sw) << 4)) = hi;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the tensor core reads the A tile
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&raw_empty[r]);
+        ptx::mbar_arrive(&cvt_full[s]);
+      }
+    }
+  }
+}
+
+template <int BN, int STAGES, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
                    int N, int kb_per_split, Epi e, float* __restrict__ ws, int* err, long long wait_limit,
                    L2Ahead ahead) {
-  using L = TcSmem<BN, STAGES>;
+  using L = TcSmem<BN, STAGES, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::PIPE);
+  uint8_t* sB = smem + STAGES * L::A_STAGE;
+  uint8_t* sRaw = smem + L::PIPE;               // F8: E4M3 code tiles
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* done = empty + STAGES;
   uint64_t* recv_bar = done + 1;                // split-K: the peers' row slices landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
+  uint64_t* cvt_full = recv_bar + 1;            // F8: [STAGES] the stage's A tile is converted
+  uint64_t* raw_full = cvt_full + (F8 ? STAGES : 0);   // F8: [RAW] a code tile landed
+  uint64_t* raw_empty = raw_full + L::RAW;             // F8: [RAW] the converters read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_empty + L::RAW);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -227,13 +384,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(done, 1);
     ptx::mbar_init(recv_bar, 1);
+    if constexpr (F8) {
+      for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&cvt_full[s], kF8Converters);
+      for (int r = 0; r < L::RAW; ++r) {
+        ptx::mbar_init(&raw_full[r], 1);
+        ptx::mbar_init(&raw_empty[r], kF8Converters);
+      }
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
     if (onchip) ptx::mbar_arrive_expect_tx(recv_bar, (uint32_t)((S - 1) * (BM / S) * BN * 4));
     ptx::prefetch_tmap(&tmW);
     ptx::prefetch_tmap(&tmX);
   }
-  if (threadIdx.x == 32)
+  if (!F8 && threadIdx.x == 32)
     for (int i = 0; i < 3; ++i) ptx::prefetch_l2_slice(ahead.p[i], ahead.bytes[i]);
   if (warp == 2) ptx::tmem_alloc(tmem_slot, BN);
   ptx::tc_fence_before();
@@ -242,14 +406,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   ptx::pdl_launch_dependents();
 
-  if (warp == 0) {
+  if constexpr (F8) {
+    f8_main_loop<BN, STAGES>(tmW, tmX, sA, sB, sRaw, full, empty, done, cvt_full, raw_full, raw_empty, tmem,
+                             abort_flag, err, wait_limit, n0, m0, kb0, nkb, warp, lane);
+  } else if (warp == 0) {
     if (lane == 0) {
       const uint64_t pw = ptx::policy_evict_first(), px = ptx::policy_evict_last();
       // weights first: no earlier kernel writes them, so they stream before the dependency wait
       const int pre = nkb < STAGES ? nkb : STAGES;
       for (int i = 0; i < pre; ++i) {
         ptx::mbar_arrive_expect_tx(&full[i], L::STAGE_BYTES);
-        ptx::tma_load_2d(sA + i * A_BYTES, &tmW, &full[i], (kb0 + i) * BK, n0, pw);
+        ptx::tma_load_2d(sA + i * L::A_STAGE, &tmW, &full[i], (kb0 + i) * BK, n0, pw);
       }
       ptx::pdl_wait();
       int issued = pre;
@@ -262,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
-          ptx::tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], (kb0 + i) * BK, n0, pw);
+          ptx::tma_load_2d(sA + s * L::A_STAGE, &tmW, &full[s], (kb0 + i) * BK, n0, pw);
           issued = i + 1;
         }
         ptx::tma_load_2d(sB + s * L::B_BYTES, &tmX, &full[s], (kb0 + i) * BK, m0, px);
@@ -286,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        const uint64_t ad = ptx::sdesc_sw128(ptx::smem_u32(sA + s * A_BYTES));
+        const uint64_t ad = ptx::sdesc_sw128(ptx::smem_u32(sA + s * L::A_STAGE));
         const uint64_t bd = ptx::sdesc_sw128(ptx::smem_u32(sB + s * L::B_BYTES));
 #pragma unroll
         for (int k = 0; k < BK / 16; ++k)  // 16 bf16 = 32 bytes = 2 descriptor units per MMA
@@ -299,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   // every thread but the producer (which waited before its activation loads)
   // waits for the previous kernel before touching activation memory
-  if (threadIdx.x != 0) ptx::pdl_wait();
+  if (F8 || threadIdx.x != 0) ptx::pdl_wait();
 
   if (!ptx::mbar_wait(done, 0, wait_limit)) {
     atomicExch(abort_flag, 1);
@@ -314,6 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row = quad * 32 + lane;          // TMEM lane = weight row n0 + row
   const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16);
   const int c_begin = (warp >> 2) * (BN / 2), c_end = c_begin + BN / 2;
+  // F8: the accumulator holds sum_k e4m3(code) x; the row's scale finishes it
+  const float wsc = F8 ? (n0 + row < N ? e.wscale[n0 + row] : 0.f) : 1.f;
 
   if (e.kind == EPI_PARTIAL) {
     // split partial straight to the consumer's buffer: out[(split * M + m) * ldo + n]
@@ -327,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n < N) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (m0 + c0 + j < M) part[(long long)(m0 + c0 + j) * e.ldo + n] = v[j];
+            if (m0 + c0 + j < M) part[(long long)(m0 + c0 + j) * e.ldo + n] = F8 ? v[j] * wsc : v[j];
         }
       }
     }
@@ -340,15 +509,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       switch (e.kind) {
         case EPI_STORE:
           if (e.act == ACT_SWISH)
-            tile_epilogue<EPI_STORE, ACT_SWISH>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+            tile_epilogue<EPI_STORE, ACT_SWISH, F8>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd, wsc);
           else if (e.act == ACT_GELU)
-            tile_epilogue<EPI_STORE, ACT_GELU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+            tile_epilogue<EPI_STORE, ACT_GELU, F8>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd, wsc);
           else
-            tile_epilogue<EPI_STORE, ACT_NONE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
+            tile_epilogue<EPI_STORE, ACT_NONE, F8>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd, wsc);
           break;
-        case EPI_ROPE: tile_epilogue<EPI_ROPE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
-        case EPI_GEGLU: tile_epilogue<EPI_GEGLU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
-        default: tile_epilogue<EPI_RESID>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+        case EPI_ROPE: tile_epilogue<EPI_ROPE, ACT_NONE, F8>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd, wsc); break;
+        case EPI_GEGLU: tile_epilogue<EPI_GEGLU, ACT_NONE, F8>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd, wsc); break;
+        default: tile_epilogue<EPI_RESID, ACT_NONE, F8>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd, wsc); break;
       }
     }
   } else if (onchip) {
@@ -363,6 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         float v[32];
         ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+        if constexpr (F8) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= wsc;
+        }
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           *reinterpret_cast<float4*>(part + part_idx<BN>(row, c0 + j)) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
@@ -413,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float v[32];
         ptx::tmem_ld32(taddr + (uint32_t)c0, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) my[(c0 + j) * BM + row] = v[j];
+        for (int j = 0; j < 32; ++j) my[(c0 + j) * BM + row] = F8 ? v[j] * wsc : v[j];
       }
     }
     cluster.sync();
@@ -657,6 +830,38 @@ cudaError_t launch_persistent(const CUtensorMap& tw, const CUtensorMap& tx, cons
   return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, a.K / BK, a.epi, err, lim);
 }
 
+template <int BN, int STAGES>
+cudaError_t launch_f8(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int S, float* ws,
+                      int* err, long long lim, cudaStream_t s, bool pdl) {
+  using L = TcSmem<BN, STAGES, true>;
+  static_assert(L::TOTAL <= 232448, "shared memory of the E4M3 GEMM");
+  auto kern = gemm_tc_kernel<BN, STAGES, true>;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e1 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
+    if (e1 != cudaSuccess) return e1;
+    e1 = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e1 != cudaSuccess) return e1;
+    configured = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.N + BM - 1) / BM, (a.M + BN - 1) / BN, S);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = a.epi.kind == EPI_PARTIAL ? 1 : S;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const int KB = a.K / (2 * BK);
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim, L2Ahead{});
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 template <int BN, int STAGES>
@@ -729,6 +934,44 @@ TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split, bool partial) {
 }
 
 bool tc_supported(int M, int N, int K) { return M > 0 && N > 0 && K > 0 && K % BK == 0 && N % 2 == 0; }
+
+bool tc_supported_e4m3(int M, int N, int K) { return M > 0 && N > 0 && K > 0 && K % (2 * BK) == 0 && N % 2 == 0; }
+
+TcPlan tc_plan_e4m3(int M, int N, int K, int sm_count, int max_split, bool partial) {
+  // a stage covers 128 K elements: plan as a bf16 GEMM of half the K blocks
+  return tc_plan(M, N, K / 2, sm_count, max_split, partial);
+}
+
+cudaError_t tc_make_map_e4m3(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld) {
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&g_encode, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode) return cudaErrorNotSupported;
+  }
+  if (((uintptr_t)ptr & 15) || ld % 16 || cols % 128) return cudaErrorInvalidValue;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t gemm_tc_e4m3(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
+                         float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl) {
+  if (!tc_supported_e4m3(a.M, a.N, a.K) || (a.K / (2 * BK)) % p.S || !a.epi.wscale) return cudaErrorInvalidValue;
+  if (a.epi.kind != EPI_PARTIAL && tc_workspace_floats(p, a.M, a.N) > ws_floats) return cudaErrorInvalidValue;
+  switch (p.BN) {
+    // ~180 KB at most for the small-batch tiles, so a next kernel's CTA still fits beside one
+    case 64: return launch_f8<64, 3>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);    // 3 x 48 KB stages
+    case 128: return launch_f8<128, 2>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);  // 2 x 64 KB
+    case 256: return launch_f8<256, 2>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);  // 2 x 96 KB
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 long long tc_workspace_floats(const TcPlan& p, int M, int N) {
   if (p.S == 1) return 0;

@@ -28,6 +28,15 @@ long long tc_workspace_floats(const TcPlan& p, int M, int N);
 cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
                     float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl);
 
+// E4M3 weights (uint8 codes [N][K], one fp32 scale per row in a.epi.wscale):
+// K a multiple of 128; the W map from tc_make_map_e4m3 (box 128 x 128 bytes),
+// the X map as above.
+bool tc_supported_e4m3(int M, int N, int K);
+TcPlan tc_plan_e4m3(int M, int N, int K, int sm_count, int max_split, bool partial);
+cudaError_t tc_make_map_e4m3(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld);
+cudaError_t gemm_tc_e4m3(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
+                         float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl);
+
 // Large token counts (no split, M > 64): persistent CTAs with a double-buffered
 // TMEM accumulator so each tile's epilogue overlaps the next tile's MMAs.
 bool tc_use_persistent(const TcPlan& p, int M);

@@ -41,6 +41,9 @@ struct Epi {
   int rope_cols = 0, hd = 0;
   const float2* rope_tab = nullptr;  // [tok_rope][hd/2] (cos, sin) for positions P + j
   int tok_rope = 1;                  // token rows per sample
+  // E4M3 weights: fp32 scale of weight row n (output column n); the tensor-core
+  // E4M3 GEMM multiplies each accumulator row by it before the epilogue
+  const float* wscale = nullptr;
 };
 
 struct GemmArgs {
@@ -168,6 +171,8 @@ enum PermMode : int { PERM_NONE = 0, PERM_ROPE = 1, PERM_GEGLU = 2 };
 // dst row r <- src row perm(r); rows of row_bytes bytes (multiple of 16, 16B-aligned pointers)
 cudaError_t permute_rows(const void* src, void* dst, int rows, int row_bytes, int mode, int p0,
                          int p1, cudaStream_t s);
+// dst[r] <- src[perm(r)] for one float per row (the row scales of an FP8 matrix)
+cudaError_t permute_floats(const float* src, float* dst, int rows, int mode, int p0, int p1, cudaStream_t s);
 // dst[i] = float(src[i]) for a DType source
 cudaError_t to_f32(DType dt, const void* src, float* dst, long long n, cudaStream_t s);
 

@@ -19,10 +19,10 @@
 #include "gr00t.h"
 #include "kernels.h"
 
-using // Size (fp32 elements) of the fixed scratch array of the allocation-free step.
+// Size (fp32 elements) of the fixed scratch array of the allocation-free step.
 #define G3_NOALLOC_SCRATCH_FLOATS (3 << 20)
 
-namespace g3;
+using namespace g3;
 
 struct gr00t_ctx {
   gr00t_geometry g{};
@@ -44,8 +44,10 @@ struct gr00t_ctx {
   char* arena = nullptr;
   size_t arena_bytes = 0;
 
-  // weights (activation dtype), biases (fp32)
+  // weights (activation dtype; the per-layer projections E4M3 codes when fp8w), biases (fp32)
+  bool fp8w = false;          // GR00T_WFMT_FP8: per-layer projections as codes + row scales
   std::vector<void*> w_qkv, w_o, w_up, w_down;
+  std::vector<float*> s_qkv, s_o, s_up, s_down;   // fp8w: fp32 scale of each output row
   void *w_tin = nullptr, *w_tout = nullptr, *w_cond = nullptr, *w_in = nullptr, *w_out = nullptr;
   void *w_enc1 = nullptr, *w_enc2 = nullptr, *w_enc3 = nullptr;
   float *b_tin = nullptr, *b_tout = nullptr, *b_cond = nullptr, *b_in = nullptr, *b_out = nullptr;
@@ -158,6 +160,13 @@ int validate(const gr00t_geometry* g, char* msg, size_t len) {
   if (g->max_steps < 1 || g->max_steps > 4096) return bad(GR00T_EINVAL, "max_steps out of range");
   if (g->max_prefix < 0 || g->max_prefix > (1 << 20)) return bad(GR00T_EINVAL, "max_prefix out of range");
   if (!(g->norm_eps > 0.f)) return bad(GR00T_EINVAL, "norm_eps must be > 0");
+  if (g->weight_format != GR00T_WFMT_NATIVE && g->weight_format != GR00T_WFMT_FP8)
+    return bad(GR00T_EINVAL, "unknown weight_format");
+  if (g->weight_format == GR00T_WFMT_FP8) {
+    if (g->dtype != GR00T_DTYPE_BF16) return bad(GR00T_EINVAL, "FP8 weights need dtype BF16");
+    if (g->hidden % 128 || g->mlp_dim % 128 || (g->q_heads * g->head_dim) % 128)
+      return bad(GR00T_EINVAL, "FP8 weights need hidden, mlp_dim and q_heads*head_dim multiples of 128");
+  }
   if (g->family == GR00T_FAMILY_EXPERT) {
     if (g->kv_heads != 1)
       return bad(GR00T_EINVAL, "expert family needs kv_heads == 1 (the head fold is exact only with one KV head)");
@@ -196,12 +205,23 @@ void plan_buffers(gr00t_ctx* c, Plan& pl) {
   c->w_o.assign(L, nullptr);
   c->w_up.assign(L, nullptr);
   c->w_down.assign(L, nullptr);
+  c->s_qkv.assign(L, nullptr);
+  c->s_o.assign(L, nullptr);
+  c->s_up.assign(L, nullptr);
+  c->s_down.assign(L, nullptr);
   const int up_rows = (c->g.mlp_kind == GR00T_MLP_GEGLU ? 2 : 1) * c->F;
+  const size_t wes = c->fp8w ? 1 : es;   // bytes per element of the per-layer projections
   for (int l = 0; l < L; ++l) {
-    pl.add(&c->w_qkv[l], (size_t)c->nqkv[l] * D * es);
-    pl.add(&c->w_o[l], (size_t)D * c->qd * es);
-    pl.add(&c->w_up[l], (size_t)up_rows * D * es);
-    pl.add(&c->w_down[l], (size_t)D * c->F * es);
+    pl.add(&c->w_qkv[l], (size_t)c->nqkv[l] * D * wes);
+    pl.add(&c->w_o[l], (size_t)D * c->qd * wes);
+    pl.add(&c->w_up[l], (size_t)up_rows * D * wes);
+    pl.add(&c->w_down[l], (size_t)D * c->F * wes);
+    if (c->fp8w) {
+      pl.add((void**)&c->s_qkv[l], (size_t)c->nqkv[l] * 4);
+      pl.add((void**)&c->s_o[l], (size_t)D * 4);
+      pl.add((void**)&c->s_up[l], (size_t)up_rows * 4);
+      pl.add((void**)&c->s_down[l], (size_t)D * 4);
+    }
   }
   if (c->g.time_mlp) {
     pl.add(&c->w_tin, (size_t)E * E * es);
@@ -259,8 +279,8 @@ void plan_buffers(gr00t_ctx* c, Plan& pl) {
 
 // Copy one weight matrix [rows][cols] into library memory, re-laid-out by ``mode``.
 int upload_matrix(gr00t_ctx* c, const void* src, bool on_dev, void* dst, int rows, int cols,
-                  int mode, int p0, int p1, void* staging) {
-  const size_t row_bytes = (size_t)cols * c->esz;
+                  int mode, int p0, int p1, void* staging, size_t esz = 0) {
+  const size_t row_bytes = (size_t)cols * (esz ? esz : c->esz);
   const size_t bytes = row_bytes * rows;
   if (mode == PERM_NONE) {
     CK(c, cudaMemcpyAsync(dst, src, bytes, on_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
@@ -275,6 +295,20 @@ int upload_matrix(gr00t_ctx* c, const void* src, bool on_dev, void* dst, int row
   }
   CK(c, permute_rows(s, dst, rows, (int)row_bytes, mode, p0, p1, c->stream));
   // the staging buffer is reused by the next matrix: order host copies after this permute
+  CK(c, cudaStreamSynchronize(c->stream));
+  return GR00T_OK;
+}
+
+// One fp32 scale per row of an FP8 matrix, re-ordered like its rows.
+int upload_scales(gr00t_ctx* c, const void* src, bool on_dev, float* dst, int rows, int mode, int p0, int p1,
+                  void* staging) {
+  const void* s = src;
+  if (!on_dev || ((uintptr_t)src & 3)) {
+    CK(c, cudaMemcpyAsync(staging, src, (size_t)rows * 4, on_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                          c->stream));
+    s = staging;
+  }
+  CK(c, permute_floats((const float*)s, dst, rows, mode, p0, p1, c->stream));
   CK(c, cudaStreamSynchronize(c->stream));
   return GR00T_OK;
 }
@@ -308,6 +342,13 @@ int check_weights(gr00t_ctx* c, const gr00t_weights* w) {
   for (int l = 0; l < c->L; ++l)
     if (!w->qkv_w[l] || !w->o_w[l] || !w->up_w[l] || !w->down_w[l])
       return set_err(c, GR00T_EINVAL, "layer %d has a NULL weight", l);
+  if (c->fp8w) {
+    if (!w->qkv_s || !w->o_s || !w->up_s || !w->down_s)
+      return set_err(c, GR00T_EINVAL, "FP8 weights need the per-layer scale arrays qkv_s/o_s/up_s/down_s");
+    for (int l = 0; l < c->L; ++l)
+      if (!w->qkv_s[l] || !w->o_s[l] || !w->up_s[l] || !w->down_s[l])
+        return set_err(c, GR00T_EINVAL, "layer %d has a NULL scale", l);
+  }
   return GR00T_OK;
 }
 
@@ -328,16 +369,24 @@ int upload_weights(gr00t_ctx* c, const gr00t_weights* w) {
   auto M = [&](const void* s, void* d, int rows, int cols, int mode, int p0, int p1) {
     if (rc == GR00T_OK) rc = upload_matrix(c, s, on_dev, d, rows, cols, mode, p0, p1, staging);
   };
+  // per-layer projections: E4M3 codes (1 byte) and their row scales when fp8w
+  auto P = [&](const void* s, const void* sc, void* d, float* dsc, int rows, int cols, int mode, int p0, int p1) {
+    if (rc == GR00T_OK)
+      rc = upload_matrix(c, s, on_dev, d, rows, cols, mode, p0, p1, staging, c->fp8w ? 1 : c->esz);
+    if (rc == GR00T_OK && c->fp8w) rc = upload_scales(c, sc, on_dev, dsc, rows, mode, p0, p1, staging);
+  };
   auto Bv = [&](const void* s, float* d, long long n) {
     if (rc == GR00T_OK) rc = upload_bias(c, s, on_dev, d, n, staging);
   };
   for (int l = 0; l < c->L; ++l) {
     const bool rope = !dit;  // expert: q heads and the k head carry rotate-half RoPE
-    M(w->qkv_w[l], c->w_qkv[l], c->nqkv[l], D, rope ? PERM_ROPE : PERM_NONE,
+    auto sc = [&](const void* const* a) { return c->fp8w ? a[l] : nullptr; };
+    P(w->qkv_w[l], sc(w->qkv_s), c->w_qkv[l], c->s_qkv[l], c->nqkv[l], D, rope ? PERM_ROPE : PERM_NONE,
       (c->Hq + c->Hkv) * c->Dh, c->Dh);
-    M(w->o_w[l], c->w_o[l], D, c->qd, PERM_NONE, 0, 0);
-    M(w->up_w[l], c->w_up[l], (geglu ? 2 : 1) * c->F, D, geglu ? PERM_GEGLU : PERM_NONE, c->F, 0);
-    M(w->down_w[l], c->w_down[l], D, c->F, PERM_NONE, 0, 0);
+    P(w->o_w[l], sc(w->o_s), c->w_o[l], c->s_o[l], D, c->qd, PERM_NONE, 0, 0);
+    P(w->up_w[l], sc(w->up_s), c->w_up[l], c->s_up[l], (geglu ? 2 : 1) * c->F, D, geglu ? PERM_GEGLU : PERM_NONE,
+      c->F, 0);
+    P(w->down_w[l], sc(w->down_s), c->w_down[l], c->s_down[l], D, c->F, PERM_NONE, 0, 0);
   }
   if (c->g.time_mlp) {
     M(w->time_mlp_in_w, c->w_tin, E, E, PERM_NONE, 0, 0);
@@ -388,13 +437,40 @@ const CUtensorMap* tmap(gr00t_ctx* c, const void* ptr, long long rows, long long
   auto it = c->tmaps.find(key);
   if (it != c->tmaps.end()) return &it->second;
   CUtensorMap m;
-  if (tc_make_map(&m, ptr, rows, cols, ld, box_rows) != cudaSuccess) return nullptr;
+  // box_rows -1: E4M3 codes (uint8, 128 x 128-byte boxes); else bf16, 64 columns x box_rows
+  const cudaError_t e = box_rows < 0 ? tc_make_map_e4m3(&m, ptr, rows, cols, ld)
+                                     : tc_make_map(&m, ptr, rows, cols, ld, box_rows);
+  if (e != cudaSuccess) return nullptr;
   return &c->tmaps.emplace(key, m).first->second;
+}
+
+// The split-K plan of a tensor-core GEMM (E4M3 weights: stages of 128 K elements).
+TcPlan plan_of(gr00t_ctx* c, const GemmArgs& a, bool partial) {
+  const int cap = partial ? c->resid_split_cap : c->split_cap;
+  return a.epi.wscale ? tc_plan_e4m3(a.M, a.N, a.K, c->sm_count, cap, partial)
+                      : tc_plan(a.M, a.N, a.K, c->sm_count, cap, partial);
+}
+
+bool tc_ok(gr00t_ctx* c, const GemmArgs& a) {
+  if (c->dt != DT_BF16 || c->opt_gemm != 0) return false;
+  return a.epi.wscale ? tc_supported_e4m3(a.M, a.N, a.K) : tc_supported(a.M, a.N, a.K);
 }
 
 int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
   ++c->launches;
   tmark(c, cls);
+  if (a.epi.wscale) {   // E4M3 weights: the tensor-core path is the only one
+    if (!tc_ok(c, a))
+      return set_err(c, GR00T_EUNSUPPORTED, "FP8 weights need the tensor-core GEMM (GEMM path 0, K %% 128 == 0)");
+    const TcPlan p = plan_of(c, a, a.epi.kind == EPI_PARTIAL);
+    const CUtensorMap* tw = tmap(c, a.W, a.N, a.K, a.ldw, -1);
+    const CUtensorMap* tx = tmap(c, a.A, a.M, a.K, a.lda, p.BN);
+    if (!tw || !tx) return set_err(c, GR00T_ECUDA, "TMA descriptor encode failed (alignment?)");
+    CK(c, gemm_tc_e4m3(*tw, *tx, a, p, c->gemm_ws, c->gemm_ws_floats, c->err_flag, c->wait_limit, c->stream,
+                       c->opt_pdl != 0));
+    tmark(c, cls);
+    return GR00T_OK;
+  }
   if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
     const bool partial = a.epi.kind == EPI_PARTIAL;
     const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, partial ? c->resid_split_cap : c->split_cap, partial);
@@ -418,8 +494,8 @@ int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
 // S fp32 partials go to the scratch workspace and the next norm / out_proj
 // kernel folds them into h (pending), saving a reduction phase here.
 int gemm_resid(gr00t_ctx* c, GemmArgs a, int cls) {
-  if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
-    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, c->resid_split_cap, true);
+  if (tc_ok(c, a)) {
+    const TcPlan p = plan_of(c, a, true);
     if (p.S > 1 && (long long)p.S * a.M * a.N <= c->gemm_ws_floats) {
       c->pending.part = c->gemm_ws;
       c->pending.S = p.S;
@@ -490,6 +566,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     for (int l = 0; l < L; ++l) {
       GemmArgs g;
       g.A = c->n; g.lda = D; g.W = c->w_qkv[l]; g.ldw = D; g.M = M; g.N = nq; g.K = D;
+      g.epi.wscale = c->fp8w ? c->s_qkv[l] : nullptr;
       g.epi.kind = EPI_ROPE; g.epi.out = c->qkv; g.epi.ldo = nq;
       g.epi.rope_cols = (c->Hq + 1) * c->Dh; g.epi.hd = c->Dh; g.epi.rope_tab = c->rope_tab;
       g.epi.tok_rope = tok;
@@ -543,6 +620,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
 
       GemmArgs go;
       go.A = c->att; go.lda = c->qd; go.W = c->w_o[l]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
+      go.epi.wscale = c->fp8w ? c->s_o[l] : nullptr;
       go.epi.kind = EPI_RESID_GATED; go.epi.resid = c->h; go.epi.ldr = D;
       go.epi.gate = ptr_at(site(2 * l), 2LL * D, es); go.epi.gate_bstride = bstride; go.epi.tok = tok;
       RC(gemm_resid(c, go, GR00T_KCLASS_O_GEMM));
@@ -556,6 +634,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
 
       GemmArgs gu;
       gu.A = c->n; gu.lda = D; gu.W = c->w_up[l]; gu.ldw = D; gu.M = M; gu.K = D;
+      gu.epi.wscale = c->fp8w ? c->s_up[l] : nullptr;
       if (c->g.mlp_kind == GR00T_MLP_GEGLU) {
         gu.N = 2 * c->F; gu.epi.kind = EPI_GEGLU;
       } else {
@@ -566,6 +645,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
 
       GemmArgs gd;
       gd.A = c->u; gd.lda = c->F; gd.W = c->w_down[l]; gd.ldw = c->F; gd.M = M; gd.N = D; gd.K = c->F;
+      gd.epi.wscale = c->fp8w ? c->s_down[l] : nullptr;
       gd.epi.kind = EPI_RESID_GATED; gd.epi.resid = c->h; gd.epi.ldr = D;
       gd.epi.gate = ptr_at(site(2 * l + 1), 2LL * D, es); gd.epi.gate_bstride = bstride; gd.epi.tok = tok;
       RC(gemm_resid(c, gd, GR00T_KCLASS_DOWN_GEMM));
@@ -623,6 +703,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     const int nq = c->nqkv[i];
     GemmArgs g;
     g.A = c->n; g.lda = D; g.W = c->w_qkv[i]; g.ldw = D; g.M = M; g.N = nq; g.K = D;
+    g.epi.wscale = c->fp8w ? c->s_qkv[i] : nullptr;
     g.epi.kind = EPI_STORE; g.epi.out = c->qkv; g.epi.ldo = nq;
     RC(gemm(c, g, GR00T_KCLASS_QKV_GEMM));
     AttnArgs at;
@@ -646,6 +727,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     tmark(c, GR00T_KCLASS_ATTENTION);
     GemmArgs go;
     go.A = c->att; go.lda = c->qd; go.W = c->w_o[i]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
+    go.epi.wscale = c->fp8w ? c->s_o[i] : nullptr;
     go.epi.kind = EPI_RESID; go.epi.resid = c->h; go.epi.ldr = D;
     RC(gemm_resid(c, go, GR00T_KCLASS_O_GEMM));
     NormArgs n3 = na;
@@ -656,10 +738,12 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     tmark(c, GR00T_KCLASS_NORM);
     GemmArgs gu;
     gu.A = c->n; gu.lda = D; gu.W = c->w_up[i]; gu.ldw = D; gu.M = M; gu.N = c->F; gu.K = D;
+    gu.epi.wscale = c->fp8w ? c->s_up[i] : nullptr;
     gu.epi.kind = EPI_STORE; gu.epi.act = ACT_GELU; gu.epi.out = c->u; gu.epi.ldo = c->F;
     RC(gemm(c, gu, GR00T_KCLASS_UP_GEMM));
     GemmArgs gd;
     gd.A = c->u; gd.lda = c->F; gd.W = c->w_down[i]; gd.ldw = c->F; gd.M = M; gd.N = D; gd.K = c->F;
+    gd.epi.wscale = c->fp8w ? c->s_down[i] : nullptr;
     gd.epi.kind = EPI_RESID; gd.epi.resid = c->h; gd.epi.ldr = D;
     RC(gemm_resid(c, gd, GR00T_KCLASS_DOWN_GEMM));
   }
@@ -767,6 +851,7 @@ extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, voi
   c->device = dev;
   c->dt = g->dtype == GR00T_DTYPE_BF16 ? DT_BF16 : DT_F32;
   c->esz = c->dt == DT_BF16 ? 2 : 4;
+  c->fp8w = g->weight_format == GR00T_WFMT_FP8;
   c->D = g->hidden; c->L = g->layers; c->Hq = g->q_heads; c->Hkv = g->kv_heads; c->Dh = g->head_dim;
   c->F = g->mlp_dim; c->H = g->horizon; c->A = g->action_dim; c->Ns = g->state_tokens; c->E = g->time_dim;
   c->tok = c->H + c->Ns;
@@ -1024,9 +1109,11 @@ extern "C" int gr00t_get_info(gr00t_ctx* c, int what, int64_t* value) {
     case GR00T_INFO_WEIGHT_BYTES: {
       long long b = 0;
       const int up_rows = (c->g.mlp_kind == GR00T_MLP_GEGLU ? 2 : 1) * c->F;
-      for (int l = 0; l < c->L; ++l)
+      for (int l = 0; l < c->L; ++l) {
+        const long long rows = (long long)c->nqkv[l] + c->D + up_rows + c->D;   // output rows (FP8: one scale each)
         b += ((long long)c->nqkv[l] * c->D + (long long)c->D * c->qd + (long long)up_rows * c->D +
-              (long long)c->D * c->F) * c->esz;
+              (long long)c->D * c->F) * (c->fp8w ? 1 : (long long)c->esz) + (c->fp8w ? rows * 4 : 0);
+      }
       b += (long long)c->A * c->D * c->esz;
       if (c->g.family == GR00T_FAMILY_EXPERT)
         b += (long long)c->D * c->A * c->esz;
@@ -1094,13 +1181,17 @@ cudaError_t noalloc_scratch(int dev, float** out) {
 
 // Scratch (fp32 elements) one GEMM of the step uses when the scratch holds ``cap``
 // elements; mirrors gemm() / gemm_resid().
-long long gemm_scratch(gr00t_ctx* c, int M, int N, int K, bool resid, long long cap) {
-  if (!(c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(M, N, K))) return 0;
+long long gemm_scratch(gr00t_ctx* c, int M, int N, int K, bool resid, long long cap, bool e4m3 = false) {
+  GemmArgs a;
+  a.M = M; a.N = N; a.K = K;
+  static const float kAnyScale = 1.f;
+  a.epi.wscale = e4m3 ? &kAnyScale : nullptr;   // selects the E4M3 planner only
+  if (!tc_ok(c, a)) return 0;
   if (resid) {
-    const TcPlan p = tc_plan(M, N, K, c->sm_count, c->resid_split_cap, true);
+    const TcPlan p = plan_of(c, a, true);
     if (p.S > 1 && (long long)p.S * M * N <= cap) return (long long)p.S * M * N;
   }
-  return tc_workspace_floats(tc_plan(M, N, K, c->sm_count, c->split_cap, false), M, N);
+  return tc_workspace_floats(plan_of(c, a, false), M, N);
 }
 
 // Largest scratch any kernel of one denoise step needs at the bound (batch, prefix).
@@ -1112,17 +1203,17 @@ long long step_scratch(gr00t_ctx* c, long long cap) {
   if (c->g.family == GR00T_FAMILY_DIT) {
     take(gemm_scratch(c, MA, D, D, false, cap));
     for (int l = 0; l < c->L; ++l) {
-      take(gemm_scratch(c, M, c->nqkv[l], D, false, cap));
-      take(gemm_scratch(c, M, D, c->qd, true, cap));
-      take(gemm_scratch(c, M, up_rows, D, false, cap));
-      take(gemm_scratch(c, M, D, c->F, true, cap));
+      take(gemm_scratch(c, M, c->nqkv[l], D, false, cap, c->fp8w));
+      take(gemm_scratch(c, M, D, c->qd, true, cap, c->fp8w));
+      take(gemm_scratch(c, M, up_rows, D, false, cap, c->fp8w));
+      take(gemm_scratch(c, M, D, c->F, true, cap, c->fp8w));
     }
     return need;
   }
-  take(gemm_scratch(c, M, c->nqkv[0], D, false, cap));
-  take(gemm_scratch(c, M, D, c->qd, true, cap));
-  take(gemm_scratch(c, M, up_rows, D, false, cap));
-  take(gemm_scratch(c, M, D, c->F, true, cap));
+  take(gemm_scratch(c, M, c->nqkv[0], D, false, cap, c->fp8w));
+  take(gemm_scratch(c, M, D, c->qd, true, cap, c->fp8w));
+  take(gemm_scratch(c, M, up_rows, D, false, cap, c->fp8w));
+  take(gemm_scratch(c, M, D, c->F, true, cap, c->fp8w));
   if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 3) && attn_t5_supported(c->Dh, c->Hq)) {
     AttnT5Args a5;
     a5.B = B; a5.H = c->H; a5.Hq = c->Hq; a5.Dh = c->Dh; a5.P = c->bP;

@@ -62,6 +62,12 @@ __global__ void permute_rows_kernel(const uint4* __restrict__ src, uint4* __rest
   for (int i = threadIdx.x; i < row_vec; i += blockDim.x) d[i] = s[i];
 }
 
+__global__ void permute_floats_kernel(const float* __restrict__ src, float* __restrict__ dst, int rows, int mode,
+                                      int p0, int p1) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r < rows) dst[r] = src[perm_src(r, mode, p0, p1)];
+}
+
 template <typename T>
 __global__ void to_f32_kernel(const T* __restrict__ src, float* __restrict__ dst, long long n) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
@@ -93,6 +99,12 @@ cudaError_t permute_rows(const void* src, void* dst, int rows, int row_bytes, in
   if (row_bytes % 16 || ((uintptr_t)src & 15) || ((uintptr_t)dst & 15)) return cudaErrorInvalidValue;
   permute_rows_kernel<<<rows, 128, 0, s>>>((const uint4*)src, (uint4*)dst, row_bytes / 16, mode, p0,
                                            p1);
+  return cudaGetLastError();
+}
+
+cudaError_t permute_floats(const float* src, float* dst, int rows, int mode, int p0, int p1, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  permute_floats_kernel<<<(rows + 255) / 256, 256, 0, s>>>(src, dst, rows, mode, p0, p1);
   return cudaGetLastError();
 }
 

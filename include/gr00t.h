@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define GR00T_ABI_VERSION 1
+#define GR00T_ABI_VERSION 2
 
 /* ---- status codes ------------------------------------------------------ */
 #define GR00T_OK 0
@@ -98,7 +98,18 @@ typedef struct gr00t_geometry {
   int32_t max_steps;     /* largest denoise step count                        */
   float rope_theta;      /* RoPE base (EXPERT family)                         */
   float norm_eps;        /* epsilon of RMSNorm / LayerNorm                    */
+  int32_t weight_format; /* GR00T_WFMT_*: storage of the per-layer projections */
 } gr00t_geometry;
+
+/* Storage of the per-layer projections (qkv_w, o_w, up_w, down_w).  FP8: each
+ * matrix is uint8 E4M3 codes [out, in] (sign bit 7, exponent bits 6..3 with
+ * bias 7, mantissa bits 2..0, no infinities) with one fp32 scale per output row
+ * (qkv_s .. down_s): the real weight is e4m3(code) * scale.  Streaming half the
+ * bytes is the lever of the bandwidth-bound small-batch loop ("pi0.5 Design",
+ * precision notes; vla.cpp Table V).  Requires dtype BF16: activations stay
+ * bf16 and the codes are widened to bf16 on chip, exactly. */
+#define GR00T_WFMT_NATIVE 0   /* the geometry's dtype                           */
+#define GR00T_WFMT_FP8 1      /* E4M3 codes + per-row fp32 scales (dtype BF16)  */
 
 /*
  * Weights, all in the geometry's dtype (fp32 or bf16), nn.Linear [out, in].
@@ -114,7 +125,8 @@ typedef struct gr00t_geometry {
  *   DIT:    enc_w1 [D, A], enc_b1 [D], enc_w2 [D, D+E] acting on
  *           concat(W1 x + b1, temb(tau)), enc_b2 [D], enc_w3 [D, D], enc_b3 [D]
  *   action_out_w [A, D], action_out_b [A]
- *   per layer l (arrays of ``layers`` pointers):
+ *   per layer l (arrays of ``layers`` pointers; with GR00T_WFMT_FP8 these four
+ *   are uint8 E4M3 codes and qkv_s .. down_s their fp32 row scales):
  *     qkv_w[l]  EXPERT: [Hq*Dh + 2*Dh, D] rows (q heads, k, v)
  *               DIT even l: [Hq*Dh, D] (q only); odd l: [3*Hq*Dh, D] (q, k, v)
  *     o_w[l]    [D, Hq*Dh]
@@ -143,6 +155,12 @@ typedef struct gr00t_weights {
   const void* const* o_w;
   const void* const* up_w;
   const void* const* down_w;
+  /* GR00T_WFMT_FP8 only (else NULL): per layer, fp32 scale of each output row
+   * of qkv_w / o_w / up_w / down_w, in the same location as the codes */
+  const void* const* qkv_s;
+  const void* const* o_s;
+  const void* const* up_s;
+  const void* const* down_s;
 } gr00t_weights;
 
 typedef struct gr00t_ctx gr00t_ctx;

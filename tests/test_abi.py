@@ -69,6 +69,17 @@ def test_bad_geometry_is_refused(lib, field, value, needle):
     assert rc == -1 and needle in msg
 
 
+def test_fp8_weight_geometry_rules(lib):
+    import flow_matching_vla_gb300 as fmv
+    assert fmv.validate_geometry(synth.config("pi05_fp8"))[0] == 0
+    rc, msg = fmv.validate_geometry(synth.config("pi05_fp8", dtype=synth.DTYPE_FP32))
+    assert rc == -1 and "BF16" in msg
+    rc, msg = fmv.validate_geometry(synth.config("pi05_fp8", hidden=1088))   # 64 | 1088, 128 does not
+    assert rc == -1 and "128" in msg
+    rc, msg = fmv.validate_geometry(synth.config("pi05", weight_format=7))
+    assert rc == -1 and "weight_format" in msg
+
+
 def test_dit_geometry_rules(lib):
     import flow_matching_vla_gb300 as fmv
     g = synth.config("gr00t")

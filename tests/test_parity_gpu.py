@@ -189,3 +189,29 @@ def test_onchip_split_k_small(cap):
 def test_onchip_split_k_dit_8way():
     fmv = _fmv()
     check_case(synth.make_case("gr00t"), options=[(fmv.OPT_SPLIT_CAP, 8)])
+
+
+# FP8 weight streaming: per-layer projections as E4M3 codes + row scales (the
+# oracle runs on the same codes, dequantized); several tiles, split-K reduced
+# on chip and as partials, both families, then the full-size workloads
+@pytest.mark.parametrize("name", ["small_fp8", "small_dit_fp8"])
+def test_fp8_weights_parity_small(name):
+    check_case(synth.make_case(name))
+
+
+def test_fp8_weights_many_rows_and_caps():
+    fmv = _fmv()
+    check_case(synth.make_case("small_fp8", batch=8), options=[(fmv.OPT_SPLIT_CAP, 1)])
+    check_case(synth.make_case("small_fp8", batch=2, prefix=120), options=[(fmv.OPT_SPLIT_CAP, 4)])
+
+
+def test_pi05_fp8_full_size():
+    check_case(synth.make_case("pi05_fp8"))
+
+
+def test_gr00t_fp8_full_size():
+    check_case(synth.make_case("gr00t_fp8"))
+
+
+def test_pi05_fp8_batch32_sampled():
+    check_case(synth.make_case("pi05_fp8", batch=32), samples=[0, 31])
