@@ -36,20 +36,34 @@ constexpr int BM = 128;  // weight rows per CTA (MMA M)
 constexpr int BK = 64;   // K elements per stage: one 128-byte swizzle row of bf16
 constexpr int A_BYTES = BM * BK * 2;
 
-// F8: E4M3 weights.  A stage then covers 128 K elements: the producer streams
-// 128 x 128-byte code tiles into a 2-slot ring, five converter warps widen them
-// (exactly) into the bf16 A tile of the stage, and the MMA reads that.
-template <int BN, int STAGES, bool F8 = false>
+// Weight paths (WF): WF_SMEM -- bf16 weight tiles stay in shared memory and the
+// MMA reads A from there.  WF_E4M3 -- E4M3 weights with A in TENSOR memory: the
+// producer streams 128 x 128-byte code tiles (128 K elements) into a 2-slot ring,
+// four warps widen them exactly to bf16 into the stage's A tile in tensor memory
+// (lane = weight row, 32-bit column j = K elements 2j, 2j+1), and the MMA reads A
+// from there, so after the dependency wait shared memory only feeds the
+// activations to the tensor core (an MMA with N = 64 reading both operands from
+// shared memory is bound by that: ~48 cycles measured).  The same tensor-memory A
+// for bf16 weights (a plain copy instead of the widening) measured slower at
+// batch 1 than WF_SMEM: it doubles the bytes moved through the ring.
+constexpr int WF_SMEM = 0, WF_E4M3 = 1;
+
+template <int BN, int STAGES, int WF = WF_SMEM>
 struct TcSmem {
+  static constexpr bool F8 = WF == WF_E4M3, TA = WF != WF_SMEM;
   static constexpr int BKX = F8 ? 2 * BK : BK;    // K elements per stage
-  static constexpr int A_STAGE = BM * BKX * 2;    // bf16 A tile(s) of a stage
+  static constexpr int A_STAGE = TA ? 0 : BM * BKX * 2;   // bf16 A tile of a stage in shared memory
+  static constexpr int A_COLS = BKX / 2;          // TA: tensor-memory columns of one stage's A tile
+  static constexpr int TMEM_NEED = BN + (TA ? STAGES * A_COLS : 0);
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
+                                 : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int B_BYTES = BN * BKX * 2;
   static constexpr int STAGE_BYTES = A_STAGE + B_BYTES;
   static constexpr int PIPE = STAGES * STAGE_BYTES;
-  static constexpr int RAW = F8 ? 2 : 0;          // E4M3 code tiles in flight
+  static constexpr int RAW = TA ? 2 : 0;          // E4M3 code tiles in flight to tensor memory
   static constexpr int RAW_BYTES = BM * 128;
   static constexpr int BAR_OFF = PIPE + RAW * RAW_BYTES;
-  static constexpr int NBAR = 2 * STAGES + 2 + (F8 ? STAGES + 2 * RAW : 0);
+  static constexpr int NBAR = 2 * STAGES + 2 + (TA ? STAGES + 2 * RAW : 0);
   static constexpr int BAR = NBAR * 8 + 16;
   static constexpr int TOTAL = BAR_OFF + BAR + 1024;  // + alignment slack
   // split-K reduced on chip: the idle pipeline holds this CTA's fp32 partial
@@ -218,12 +232,11 @@ inline L2Ahead l2_ahead(const GemmArgs& a) {
 // exponents 2^-9 .. 2^8), so the MMA sums e4m3(code) * x exactly as the bf16
 // path sums w * x; the row scale is applied in the epilogue.
 // ---------------------------------------------------------------------------
-constexpr int kF8Converters = 5;   // warps 3..7
+constexpr int kTaMovers = 4;   // warps 4..7: one per tensor-memory lane quadrant
 
-// 16 E4M3 codes -> 16 bf16 (two 16-byte chunks).
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint4& hi) {
+// 16 E4M3 codes -> 8 bf16 pairs (element 2j in the low half of word j).
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint32_t (&o)[8]) {
   const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-  uint32_t o[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -237,19 +250,39 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint
       o[2 * i + h] = *reinterpret_cast<uint32_t*>(&b);
     }
   }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-template <int BN, int STAGES>
-__device__ __forceinline__ void f8_main_loop(const CUtensorMap& tmW, const CUtensorMap& tmX, uint8_t* sA,
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// D (+)= A B^T with A (M = 128 rows, K = 16) read from tensor memory.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((int)accumulate)
+      : "memory");
+}
+
+template <int BN, int STAGES, int WF>
+__device__ __forceinline__ void ta_main_loop(const CUtensorMap& tmW, const CUtensorMap& tmX, uint8_t* sA,
                                              uint8_t* sB, uint8_t* sRaw, uint64_t* full, uint64_t* empty,
                                              uint64_t* done, uint64_t* cvt_full, uint64_t* raw_full,
                                              uint64_t* raw_empty, uint32_t tmem, int* abort_flag, int* err,
                                              long long wait_limit, int n0, int m0, int kb0, int nkb, int warp,
                                              int lane) {
-  using L = TcSmem<BN, STAGES, true>;
-  constexpr int RAW = L::RAW;
+  using L = TcSmem<BN, STAGES, WF>;
+  constexpr int RAW = L::RAW, BKX = L::BKX;
+  (void)sA;
   auto fail = [&]() {
     atomicExch(abort_flag, 1);
     atomicExch(err, 1);
@@ -265,7 +298,7 @@ __device__ __forceinline__ void f8_main_loop(const CUtensorMap& tmW, const CUten
           break;
         }
         ptx::mbar_arrive_expect_tx(&raw_full[r], L::RAW_BYTES);
-        ptx::tma_load_2d(sRaw + r * L::RAW_BYTES, &tmW, &raw_full[r], (kb0 + i) * 128, n0, pw);
+        ptx::tma_load_2d(sRaw + r * L::RAW_BYTES, &tmW, &raw_full[r], (kb0 + i) * BKX, n0, pw);
         issued = i + 1;
       }
       if (*abort_flag)   // drain this thread's copies in flight (bounded)
@@ -273,7 +306,7 @@ __device__ __forceinline__ void f8_main_loop(const CUtensorMap& tmW, const CUten
           ptx::mbar_wait(&raw_full[i % RAW], (i / RAW) & 1, wait_limit);
     }
   } else if (warp == 2) {
-    if (lane == 0) {   // activations: two 64-column boxes per stage, after the dependency wait
+    if (lane == 0) {   // activations: BKX / 64 boxes of 64 columns per stage, after the dependency wait
       const uint64_t px = ptx::policy_evict_last();
       ptx::pdl_wait();
       int issued = 0;
@@ -285,8 +318,8 @@ __device__ __forceinline__ void f8_main_loop(const CUtensorMap& tmW, const CUten
         }
         ptx::mbar_arrive_expect_tx(&full[s], L::B_BYTES);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          ptx::tma_load_2d(sB + s * L::B_BYTES + h * (BN * 128), &tmX, &full[s], (kb0 + i) * 128 + h * 64, m0, px);
+        for (int h = 0; h < BKX / 64; ++h)
+          ptx::tma_load_2d(sB + s * L::B_BYTES + h * (BN * 128), &tmX, &full[s], (kb0 + i) * BKX + h * 64, m0, px);
         issued = i + 1;
       }
       if (*abort_flag)
@@ -298,26 +331,28 @@ __device__ __forceinline__ void f8_main_loop(const CUtensorMap& tmW, const CUten
       constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN);
       for (int i = 0; i < nkb; ++i) {
         const int s = i % STAGES;
-        if (!ptx::mbar_wait(&full[s], (i / STAGES) & 1, wait_limit) ||
-            !ptx::mbar_wait(&cvt_full[s], (i / STAGES) & 1, wait_limit)) {
+        if (!ptx::mbar_wait(&cvt_full[s], (i / STAGES) & 1, wait_limit) ||
+            !ptx::mbar_wait(&full[s], (i / STAGES) & 1, wait_limit)) {
           fail();
           break;
         }
         ptx::tc_fence_after();
+        const uint32_t ta = tmem + (uint32_t)(BN + s * L::A_COLS);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {   // two 64-column boxes, four K-16 steps each
-          const uint64_t ad = ptx::sdesc_sw128(ptx::smem_u32(sA + s * L::A_STAGE + (k >> 2) * (BM * 128)));
+        for (int k = 0; k < BKX / 16; ++k) {   // 8 columns (16 K elements) of A per step; B: 64-column boxes
           const uint64_t bd = ptx::sdesc_sw128(ptx::smem_u32(sB + s * L::B_BYTES + (k >> 2) * (BN * 128)));
-          ptx::mma_bf16(tmem, ad + 2 * (k & 3), bd + 2 * (k & 3), idesc, (i | k) != 0);
+          mma_bf16_ta(tmem, ta + 8 * k, bd + 2 * (k & 3), idesc, (i | k) != 0);
         }
         ptx::mma_commit(&empty[s]);
       }
       ptx::mma_commit(done);
     }
-  } else {
-    // converters: 16-byte chunk c of code row r (stored at chunk c ^ (r % 8))
-    // -> bf16 box c / 4, chunks 2 (c % 4) and 2 (c % 4) + 1 (each ^ (r % 8))
-    const int ct = (int)threadIdx.x - 96;
+  } else if (warp >= 4) {
+    // movers: warp w owns weight rows 32 (w % 4) .. +31 (its tensor-memory lane
+    // quadrant); a lane widens its row's 128 codes (16-byte chunk c stored at chunk
+    // c ^ (row % 8)) into 64 columns of the stage's A tile
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     for (int i = 0; i < nkb; ++i) {
       const int r = i % RAW, s = i % STAGES;
       if (!ptx::mbar_wait(&raw_full[r], (i / RAW) & 1, wait_limit) ||
@@ -325,19 +360,22 @@ __device__ __forceinline__ void f8_main_loop(const CUtensorMap& tmW, const CUten
         fail();
         break;
       }
-      const uint8_t* src = sRaw + r * L::RAW_BYTES;
-      uint8_t* dst = sA + s * L::A_STAGE;
-#pragma unroll 2
-      for (int q = ct; q < BM * 8; q += 32 * kF8Converters) {
-        const int row = q >> 3, c = q & 7, sw = row & 7;
-        const uint4 in = *reinterpret_cast<const uint4*>(src + row * 128 + ((c ^ sw) << 4));
-        uint4 lo, hi;
-        e4m3x16_to_bf16(in, lo, hi);
-        uint8_t* box = dst + (c >> 2) * (BM * 128) + row * 128;
-        *reinterpret_cast<uint4*>(box + (((2 * (c & 3)) ^ sw) << 4)) = lo;
-        *reinterpret_cast<uint4*>(box + (((2 * (c & 3) + 1) ^ sw) << 4)) = hi;
+      ptx::tc_fence_after();
+      const uint8_t* src = sRaw + r * L::RAW_BYTES + row * 128;
+      const uint32_t ta = lane_base + (uint32_t)(BN + s * L::A_COLS);
+      uint32_t a[64];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 in = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) << 4));
+        uint32_t o[8];
+        e4m3x16_to_bf16(in, o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[8 * c + j] = o[j];
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the tensor core reads the A tile
+      tmem_st32u(ta, a);
+      tmem_st32u(ta + 32, a + 32);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         ptx::mbar_arrive(&raw_empty[r]);
@@ -347,24 +385,25 @@ __device__ __forceinline__ void f8_main_loop(const CUtensorMap& tmW, const CUten
   }
 }
 
-template <int BN, int STAGES, bool F8 = false>
+template <int BN, int STAGES, int WF = WF_SMEM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
                    int N, int kb_per_split, Epi e, float* __restrict__ ws, int* err, long long wait_limit,
                    L2Ahead ahead) {
-  using L = TcSmem<BN, STAGES, F8>;
+  using L = TcSmem<BN, STAGES, WF>;
+  constexpr bool F8 = L::F8, TA = L::TA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * L::A_STAGE;
-  uint8_t* sRaw = smem + L::PIPE;               // F8: E4M3 code tiles
+  uint8_t* sRaw = smem + L::PIPE;               // TA: weight tiles on their way to tensor memory
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* done = empty + STAGES;
   uint64_t* recv_bar = done + 1;                // split-K: the peers' row slices landed
-  uint64_t* cvt_full = recv_bar + 1;            // F8: [STAGES] the stage's A tile is converted
-  uint64_t* raw_full = cvt_full + (F8 ? STAGES : 0);   // F8: [RAW] a code tile landed
-  uint64_t* raw_empty = raw_full + L::RAW;             // F8: [RAW] the converters read it
+  uint64_t* cvt_full = recv_bar + 1;            // TA: [STAGES] the stage's A tile is in tensor memory
+  uint64_t* raw_full = cvt_full + (TA ? STAGES : 0);   // TA: [RAW] a weight tile landed
+  uint64_t* raw_empty = raw_full + L::RAW;             // TA: [RAW] the movers read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_empty + L::RAW);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
@@ -384,11 +423,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(done, 1);
     ptx::mbar_init(recv_bar, 1);
-    if constexpr (F8) {
-      for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&cvt_full[s], kF8Converters);
+    if constexpr (TA) {
+      for (int s = 0; s < STAGES; ++s) ptx::mbar_init(&cvt_full[s], kTaMovers);
       for (int r = 0; r < L::RAW; ++r) {
         ptx::mbar_init(&raw_full[r], 1);
-        ptx::mbar_init(&raw_empty[r], kF8Converters);
+        ptx::mbar_init(&raw_empty[r], kTaMovers);
       }
     }
     *abort_flag = 0;
@@ -397,17 +436,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmW);
     ptx::prefetch_tmap(&tmX);
   }
-  if (!F8 && threadIdx.x == 32)
+  if (!TA && threadIdx.x == 32)
     for (int i = 0; i < 3; ++i) ptx::prefetch_l2_slice(ahead.p[i], ahead.bytes[i]);
-  if (warp == 2) ptx::tmem_alloc(tmem_slot, BN);
+  if (warp == 2) ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   ptx::pdl_launch_dependents();
 
-  if constexpr (F8) {
-    f8_main_loop<BN, STAGES>(tmW, tmX, sA, sB, sRaw, full, empty, done, cvt_full, raw_full, raw_empty, tmem,
+  if constexpr (TA) {
+    ta_main_loop<BN, STAGES, WF>(tmW, tmX, sA, sB, sRaw, full, empty, done, cvt_full, raw_full, raw_empty, tmem,
                              abort_flag, err, wait_limit, n0, m0, kb0, nkb, warp, lane);
   } else if (warp == 0) {
     if (lane == 0) {
@@ -466,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   // every thread but the producer (which waited before its activation loads)
   // waits for the previous kernel before touching activation memory
-  if (F8 || threadIdx.x != 0) ptx::pdl_wait();
+  if (TA || threadIdx.x != 0) ptx::pdl_wait();
 
   if (!ptx::mbar_wait(done, 0, wait_limit)) {
     atomicExch(abort_flag, 1);
@@ -606,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 2) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, BN);
+    ptx::tmem_dealloc(tmem, L::TMEM_COLS);
   }
 }
 
@@ -830,12 +869,13 @@ cudaError_t launch_persistent(const CUtensorMap& tw, const CUtensorMap& tx, cons
   return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, a.K / BK, a.epi, err, lim);
 }
 
-template <int BN, int STAGES>
-cudaError_t launch_f8(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int S, float* ws,
+template <int BN, int STAGES, int WF>
+cudaError_t launch_ta(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int S, float* ws,
                       int* err, long long lim, cudaStream_t s, bool pdl) {
-  using L = TcSmem<BN, STAGES, true>;
-  static_assert(L::TOTAL <= 232448, "shared memory of the E4M3 GEMM");
-  auto kern = gemm_tc_kernel<BN, STAGES, true>;
+  using L = TcSmem<BN, STAGES, WF>;
+  static_assert(L::TOTAL <= 232448, "shared memory of the tensor-memory-A GEMM");
+  static_assert(L::TMEM_NEED <= 512, "tensor memory of the tensor-memory-A GEMM");
+  auto kern = gemm_tc_kernel<BN, STAGES, WF>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e1 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
@@ -858,7 +898,7 @@ cudaError_t launch_f8(const CUtensorMap& tw, const CUtensorMap& tx, const GemmAr
   attr[1].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const int KB = a.K / (2 * BK);
+  const int KB = a.K / L::BKX;
   return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim, L2Ahead{});
 }
 
@@ -965,10 +1005,10 @@ cudaError_t gemm_tc_e4m3(const CUtensorMap& tw, const CUtensorMap& tx, const Gem
   if (!tc_supported_e4m3(a.M, a.N, a.K) || (a.K / (2 * BK)) % p.S || !a.epi.wscale) return cudaErrorInvalidValue;
   if (a.epi.kind != EPI_PARTIAL && tc_workspace_floats(p, a.M, a.N) > ws_floats) return cudaErrorInvalidValue;
   switch (p.BN) {
-    // ~180 KB at most for the small-batch tiles, so a next kernel's CTA still fits beside one
-    case 64: return launch_f8<64, 3>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);    // 3 x 48 KB stages
-    case 128: return launch_f8<128, 2>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);  // 2 x 64 KB
-    case 256: return launch_f8<256, 2>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);  // 2 x 96 KB
+    // A stages live in tensor memory (64 columns each, beside the BN-column accumulator)
+    case 64: return launch_ta<64, 4, WF_E4M3>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);    // 4 x 16 KB X stages
+    case 128: return launch_ta<128, 4, WF_E4M3>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);  // 4 x 32 KB
+    case 256: return launch_ta<256, 2, WF_E4M3>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);  // 2 x 64 KB
     default: return cudaErrorInvalidValue;
   }
 }
