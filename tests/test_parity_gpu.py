@@ -115,9 +115,20 @@ def test_expert_fp32_empty_prefix():
     check_case(synth.make_case("small_fp32", prefix=0))
 
 
-@pytest.mark.parametrize("steps", [1, 2, 5])
+@pytest.mark.parametrize("steps", [1, 2, 5, 16])
 def test_step_counts(steps):
     check_case(synth.make_case("small_bf16", steps=steps))
+
+
+# horizon variants: LIBERO-style 10 actions, and 50 actions (ALOHA) at the full
+# pi0.5 width with a short prefix
+@pytest.mark.parametrize("horizon", [10, 50])
+def test_horizon_variants(horizon):
+    check_case(synth.make_case("small_bf16", horizon=horizon, batch=2))
+
+
+def test_pi05_width_horizon_10():
+    check_case(synth.make_case("pi05", horizon=10, prefix=256, layers=4))
 
 
 def test_pi05_full_size():
