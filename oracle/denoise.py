@@ -6,11 +6,18 @@ from __future__ import annotations
 
 import numpy as np
 
-from .dit import action_time_bias, dit_denoise, dit_velocity
+from .dit import action_time_bias, dit_denoise, dit_velocity, project_context
 from .expert import expert_denoise, expert_velocity
 from .schedule import euler, modulation_table
 
 FAMILY_EXPERT = 0
+
+
+def _kv(case, dtype):
+    """The case's bound K/V, or (DiT with VL features) their cross projections."""
+    if case.get("features") is not None:
+        return project_context(case["geom"], case["weights"], case["features"], dtype)
+    return case["K"], case["V"]
 
 
 def denoise(case, steps=None, dtype=np.float64, record=False):
@@ -19,7 +26,8 @@ def denoise(case, steps=None, dtype=np.float64, record=False):
     T = g["steps"] if steps is None else steps
     if g["family"] == FAMILY_EXPERT:
         return expert_denoise(g, w, case["x_noise"], case["K"], case["V"], T, dtype, record)
-    return dit_denoise(g, w, case["x_noise"], case["K"], case["V"], T, case["text_mask"],
+    K, V = _kv(case, dtype)
+    return dit_denoise(g, w, case["x_noise"], K, V, T, case["text_mask"],
                        case["image_mask"], case["state"], dtype, record)
 
 
@@ -35,5 +43,6 @@ def velocity(case, x, k, steps=None, dtype=np.float64, mod=None, atb=None):
         return expert_velocity(g, w, x, rows, case["K"], case["V"], dtype)
     if atb is None:
         atb = action_time_bias(g, w, T, dtype)
-    return dit_velocity(g, w, x, rows, atb[k], case["K"], case["V"], case["text_mask"],
+    K, V = _kv(case, dtype)
+    return dit_velocity(g, w, x, rows, atb[k], K, V, case["text_mask"],
                         case["image_mask"], case["state"], dtype)

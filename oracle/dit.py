@@ -19,6 +19,25 @@ def _w(w, name, dtype):
     return w[name].astype(dtype, copy=False)
 
 
+def project_context(g, w, features, dtype=np.float64):
+    """Cross-attention K/V of every even (cross) block from the VL features
+    ("GR00T N1.7", vl_backbone: the VL engine ends with the DiT's cross-attention
+    K/V projections, cross_k / cross_v [B, S, 32, 48] for even blocks only).
+
+    ``features``: [B, S, context_dim].  K_i = features W_k,i^T and V_i = features
+    W_v,i^T, no bias (reading S11), reshaped to [B, S, kv_heads, head_dim];
+    odd blocks get None.  Returns (K, V) lists indexed by block.
+    """
+    B, S, _ = features.shape
+    Hkv, Dh = g["kv_heads"], g["head_dim"]
+    f = features.astype(dtype, copy=False)
+    K, V = [None] * g["layers"], [None] * g["layers"]
+    for l in range(0, g["layers"], 2):
+        K[l] = (f @ _w(w, f"cross_k_w.{l}", dtype).T).reshape(B, S, Hkv, Dh)
+        V[l] = (f @ _w(w, f"cross_v_w.{l}", dtype).T).reshape(B, S, Hkv, Dh)
+    return K, V
+
+
 def action_time_bias(g, w, steps, dtype=np.float64):
     """Hoisted action_time_bias [steps, D] ("GR00T N1.7", Build-time constants).
 

@@ -47,7 +47,7 @@ _BASE = dict(
     kv_heads=1, head_dim=64, mlp_dim=1024, mlp_kind=MLP_GELU, horizon=16,
     action_dim=8, state_tokens=0, batch=1, prefix=64, steps=4,
     time_dim=256, time_mlp=0, rope_theta=10000.0, norm_eps=1e-6,
-    direction=-1, weight_format=WFMT_NATIVE,
+    direction=-1, weight_format=WFMT_NATIVE, context_dim=0,
 )
 
 
@@ -99,6 +99,13 @@ CONFIGS = {
                         action_dim=32, state_tokens=1, batch=2, prefix=300,
                         steps=4, time_dim=384, time_mlp=1, direction=+1,
                         weight_format=WFMT_FP8),
+    # DiT with the cross K/V projected at bind time from VL features [B, P, context_dim]
+    "gr00t_ctx": _g(**dict(_GR00T, context_dim=2048)),
+    "small_dit_ctx": _g(family=FAMILY_DIT, layers=4, hidden=384, q_heads=8,
+                        kv_heads=8, head_dim=48, mlp_dim=1536, horizon=16,
+                        action_dim=32, state_tokens=1, batch=2, prefix=300,
+                        steps=4, time_dim=384, time_mlp=1, direction=+1,
+                        context_dim=256),
     "small_dit_fp32": _g(family=FAMILY_DIT, dtype=DTYPE_FP32, layers=2,
                          hidden=192, q_heads=4, kv_heads=4, head_dim=48,
                          mlp_dim=768, horizon=16, action_dim=32,
@@ -179,6 +186,12 @@ def weight_shapes(g: dict) -> dict:
         sh[f"o_w.{l}"] = (D, qd)
         sh[f"up_w.{l}"] = (up_rows(g), D)
         sh[f"down_w.{l}"] = (D, g["mlp_dim"])
+    Dc = g.get("context_dim", 0)
+    if g["family"] == FAMILY_DIT and Dc > 0:   # cross K/V projections of the even blocks
+        kd = g["kv_heads"] * g["head_dim"]
+        for l in range(0, L, 2):
+            sh[f"cross_k_w.{l}"] = (kd, Dc)
+            sh[f"cross_v_w.{l}"] = (kd, Dc)
     return sh
 
 
@@ -348,10 +361,26 @@ def make_masks(g: dict, seed: int = 0, batch: int | None = None, kind: str = "on
     return tuple(out)
 
 
+def make_context_features(g: dict, seed: int = 0, batch: int | None = None) -> np.ndarray:
+    """DiT family with context_dim > 0: VL features ~N(0,1), [B, P, context_dim]
+    (bf16-rounded for bf16 workloads), the input of the bind-time K/V projections."""
+    B = g["batch"] if batch is None else batch
+    return _normal(seed, "features", (B, g["prefix"], g["context_dim"]), 1.0, g["dtype"] == DTYPE_BF16)
+
+
 def make_case(name_or_geom, seed: int = 0, **overrides) -> dict:
-    """Everything one denoise call needs: geometry, weights, prefix, noise."""
+    """Everything one denoise call needs: geometry, weights, prefix, noise.
+
+    DiT workloads with ``context_dim`` > 0 carry VL ``features`` instead of
+    bound K/V (K and V are lists of None): the cross K/V are projected from them.
+    """
     g = config(name_or_geom, **overrides) if isinstance(name_or_geom, str) else dict(name_or_geom)
-    K, V = make_prefix_kv(g, seed)
     tm, im = make_masks(g, seed)
+    feats = None
+    if g["family"] == FAMILY_DIT and g.get("context_dim", 0) > 0:
+        feats = make_context_features(g, seed)
+        K, V = [None] * g["layers"], [None] * g["layers"]
+    else:
+        K, V = make_prefix_kv(g, seed)
     return dict(geom=g, weights=make_weights(g, seed), K=K, V=V, x_noise=make_noise(g, seed),
-                state=make_state_tokens(g, seed), text_mask=tm, image_mask=im, seed=seed)
+                state=make_state_tokens(g, seed), text_mask=tm, image_mask=im, features=feats, seed=seed)

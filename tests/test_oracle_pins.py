@@ -582,3 +582,29 @@ def test_fp8_dit_case_runs_on_the_dequantized_matrices():
     v8 = dit_velocity(g, w8, *args)
     assert np.array_equal(v8, dit_velocity(g, wd, *args))
     np.testing.assert_allclose(v8, torch_dit_velocity(g, wd, *args), rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# bind-time cross K/V projection (DiT with VL features)
+# ---------------------------------------------------------------------------
+
+def test_project_context_matches_torch_linear():
+    c = synth.make_case("small_dit_ctx")
+    g, w = c["geom"], c["weights"]
+    K, V = oracle.project_context(g, w, c["features"])
+    f = t64(c["features"])
+    B, P = c["features"].shape[:2]
+    for l in range(g["layers"]):
+        if l % 2:
+            assert K[l] is None and V[l] is None
+            continue
+        for M, name in ((K[l], "cross_k_w"), (V[l], "cross_v_w")):
+            ref = F.linear(f, t64(w[f"{name}.{l}"])).reshape(B, P, g["kv_heads"], g["head_dim"]).numpy()
+            np.testing.assert_allclose(M, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_context_case_equals_bound_projections():
+    c = synth.make_case("small_dit_ctx")
+    K, V = oracle.project_context(c["geom"], c["weights"], c["features"])
+    bound = dict(c, features=None, K=K, V=V)
+    assert np.array_equal(oracle.denoise(c), oracle.denoise(bound))

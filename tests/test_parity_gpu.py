@@ -84,7 +84,7 @@ def _subcase(case, idx):
     c["x_noise"] = case["x_noise"][idx]
     c["K"] = [None if k is None else k[idx] for k in case["K"]]
     c["V"] = [None if v is None else v[idx] for v in case["V"]]
-    for key in ("text_mask", "image_mask", "state"):
+    for key in ("text_mask", "image_mask", "state", "features"):
         if case.get(key) is not None:
             c[key] = case[key][idx]
     c["geom"] = dict(case["geom"], batch=len(idx))
