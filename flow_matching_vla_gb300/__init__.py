@@ -66,6 +66,7 @@ def _geometry(g: dict) -> _abi.Geometry:
     s.rope_theta = float(g.get("rope_theta", 10000.0))
     s.norm_eps = float(g.get("norm_eps", 1e-6))
     s.weight_format = int(g.get("weight_format", WFMT_NATIVE))
+    s.context_dim = int(g.get("context_dim", 0))
     return s
 
 
@@ -146,6 +147,15 @@ class DenoiseLoop:
                 arr = (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
                 arrays[field] = arr
                 setattr(w, field, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
+        if int(geom.get("context_dim", 0)) > 0:   # DiT cross K/V projections, even blocks
+            for field in ("cross_k_w", "cross_v_w"):
+                ts = [None if l % 2 else _storage_tensor(weights[f"{field}.{l}"], self.dtype_code) for l in range(L)]
+                if device_weights:
+                    ts = [None if t is None else t.cuda() for t in ts]
+                keep += [t for t in ts if t is not None]
+                arr = (ctypes.c_void_p * L)(*[0 if t is None else t.data_ptr() for t in ts])
+                arrays[field] = arr
+                setattr(w, field, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
         ctx = ctypes.c_void_p()
         with torch.cuda.device(self.stream.device):
             rc = self._lib.gr00t_create(ctypes.byref(self._g), ctypes.byref(w),
@@ -209,6 +219,25 @@ class DenoiseLoop:
             None if masks[0] is None else _ptr(masks[0]), None if masks[1] is None else _ptr(masks[1]),
             None if state is None else _ptr(state)))
         self._bound = (ks, vs, masks, state)   # the library borrows these
+        self.batch = B
+        return self
+
+    def bind_context(self, features, text_mask=None, image_mask=None, state=None):
+        """DiT with context_dim: project VL features (device tensor [B, P, context_dim]
+        of the geometry dtype) into the cross K/V on the GPU and bind them."""
+        torch = _torch()
+        if not (features.is_cuda and features.is_contiguous() and features.dtype == self.torch_dtype):
+            raise ValueError("features must be a contiguous CUDA tensor of the geometry dtype")
+        for m in (text_mask, image_mask):
+            if m is not None and not (m.is_cuda and m.dtype == torch.uint8 and m.is_contiguous()):
+                raise ValueError("masks must be contiguous CUDA uint8 tensors")
+        if state is not None and not (state.is_cuda and state.dtype == torch.float32 and state.is_contiguous()):
+            raise ValueError("state tokens must be a contiguous CUDA float32 tensor")
+        B, P = int(features.shape[0]), int(features.shape[1])
+        self._check(self._lib.gr00t_bind_context(
+            self._ctx, B, P, _ptr(features), None if text_mask is None else _ptr(text_mask),
+            None if image_mask is None else _ptr(image_mask), None if state is None else _ptr(state)))
+        self._bound = (features, [text_mask, image_mask], state)
         self.batch = B
         return self
 
@@ -281,11 +310,17 @@ def from_case(case: dict, stream=None, steps=None, device_weights=False, **geom_
         t = a if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a))
         return t.to(device="cuda", dtype=dtype).contiguous()
 
-    K = [dev(k, dt) for k in case["K"]]
-    V = [dev(v, dt) for v in case["V"]]
     tm = dev(case.get("text_mask"), torch.uint8)
     im = dev(case.get("image_mask"), torch.uint8)
     st = dev(case.get("state"), torch.float32)
+    if case.get("features") is not None:   # cross K/V projected on the GPU at bind time
+        feats = dev(case["features"], dt)
+        torch.cuda.synchronize()
+        loop.bind_context(feats, tm, im, st)
+        loop.set_schedule(steps or g["steps"], int(feats.shape[0]))
+        return loop, dict(features=feats, text_mask=tm, image_mask=im, state=st)
+    K = [dev(k, dt) for k in case["K"]]
+    V = [dev(v, dt) for v in case["V"]]
     torch.cuda.synchronize()
     loop.bind_prefix_kv(K, V, tm, im, st)
     B = next(k.shape[0] for k in K if k is not None)

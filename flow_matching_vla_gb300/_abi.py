@@ -37,7 +37,8 @@ class Geometry(ctypes.Structure):
         "abi_version", "family", "dtype", "layers", "hidden", "q_heads", "kv_heads", "head_dim",
         "mlp_dim", "mlp_kind", "horizon", "action_dim", "state_tokens", "time_dim", "time_mlp",
         "direction", "max_batch", "max_prefix", "max_steps")] + [
-        ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float), ("weight_format", ctypes.c_int32)]
+        ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float), ("weight_format", ctypes.c_int32),
+        ("context_dim", ctypes.c_int32)]
 
 
 _VP = ctypes.c_void_p
@@ -49,7 +50,7 @@ class Weights(ctypes.Structure):
         "time_mlp_in_w", "time_mlp_in_b", "time_mlp_out_w", "time_mlp_out_b", "cond_w", "cond_b",
         "action_in_w", "action_in_b", "enc_w1", "enc_b1", "enc_w2", "enc_b2", "enc_w3", "enc_b3",
         "action_out_w", "action_out_b")] + [(n, _VPP) for n in (
-        "qkv_w", "o_w", "up_w", "down_w", "qkv_s", "o_s", "up_s", "down_s")]
+        "qkv_w", "o_w", "up_w", "down_w", "qkv_s", "o_s", "up_s", "down_s", "cross_k_w", "cross_v_w")]
 
 
 # exported symbol -> (restype, argtypes)
@@ -58,6 +59,7 @@ SIGNATURES = {
     "gr00t_create": (ctypes.c_int, [ctypes.POINTER(Geometry), ctypes.POINTER(Weights), _VP,
                                     ctypes.POINTER(_VP)]),
     "gr00t_bind_prefix_kv": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VPP, _VPP, _VP, _VP, _VP]),
+    "gr00t_bind_context": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VP, _VP, _VP, _VP]),
     "gr00t_set_schedule": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int]),
     "gr00t_denoise": (ctypes.c_int, [_VP, _VP, _VP]),
     "gr00t_denoise_host": (ctypes.c_int, [_VP, _VP, _VP]),

@@ -48,6 +48,9 @@ struct gr00t_ctx {
   bool fp8w = false;          // GR00T_WFMT_FP8: per-layer projections as codes + row scales
   std::vector<void*> w_qkv, w_o, w_up, w_down;
   std::vector<float*> s_qkv, s_o, s_up, s_down;   // fp8w: fp32 scale of each output row
+  // DiT with context_dim: cross K/V projections of the even blocks, their outputs, the features
+  std::vector<void*> w_ck, w_cv, ctx_k, ctx_v;
+  void* ctx_feat = nullptr;
   void *w_tin = nullptr, *w_tout = nullptr, *w_cond = nullptr, *w_in = nullptr, *w_out = nullptr;
   void *w_enc1 = nullptr, *w_enc2 = nullptr, *w_enc3 = nullptr;
   float *b_tin = nullptr, *b_tout = nullptr, *b_cond = nullptr, *b_in = nullptr, *b_out = nullptr;
@@ -167,6 +170,10 @@ int validate(const gr00t_geometry* g, char* msg, size_t len) {
     if (g->hidden % 128 || g->mlp_dim % 128 || (g->q_heads * g->head_dim) % 128)
       return bad(GR00T_EINVAL, "FP8 weights need hidden, mlp_dim and q_heads*head_dim multiples of 128");
   }
+  if (g->context_dim < 0 || g->context_dim > 16384 || g->context_dim % 64)
+    return bad(GR00T_EINVAL, "context_dim must be 0 or a multiple of 64 up to 16384");
+  if (g->context_dim > 0 && g->family != GR00T_FAMILY_DIT)
+    return bad(GR00T_EINVAL, "context_dim (bind-time cross K/V projection) is a DiT-family field");
   if (g->family == GR00T_FAMILY_EXPERT) {
     if (g->kv_heads != 1)
       return bad(GR00T_EINVAL, "expert family needs kv_heads == 1 (the head fold is exact only with one KV head)");
@@ -244,6 +251,21 @@ void plan_buffers(gr00t_ctx* c, Plan& pl) {
   }
   pl.add(&c->w_out, (size_t)c->A * D * es);
   pl.add((void**)&c->b_out, (size_t)c->A * 4);
+  c->w_ck.assign(L, nullptr);
+  c->w_cv.assign(L, nullptr);
+  c->ctx_k.assign(L, nullptr);
+  c->ctx_v.assign(L, nullptr);
+  if (dit && c->g.context_dim > 0) {
+    const size_t kd = (size_t)c->Hkv * c->Dh, Dc = (size_t)c->g.context_dim;
+    const size_t rows = (size_t)c->g.max_batch * c->g.max_prefix;
+    for (int l = 0; l < L; l += 2) {
+      pl.add(&c->w_ck[l], kd * Dc * es);
+      pl.add(&c->w_cv[l], kd * Dc * es);
+      pl.add(&c->ctx_k[l], rows * kd * es);
+      pl.add(&c->ctx_v[l], rows * kd * es);
+    }
+    pl.add(&c->ctx_feat, rows * Dc * es);
+  }
 
   int nq = 0;
   for (int v : c->nqkv) nq = v > nq ? v : nq;
@@ -342,6 +364,12 @@ int check_weights(gr00t_ctx* c, const gr00t_weights* w) {
   for (int l = 0; l < c->L; ++l)
     if (!w->qkv_w[l] || !w->o_w[l] || !w->up_w[l] || !w->down_w[l])
       return set_err(c, GR00T_EINVAL, "layer %d has a NULL weight", l);
+  if (c->g.context_dim > 0) {
+    if (!w->cross_k_w || !w->cross_v_w)
+      return set_err(c, GR00T_EINVAL, "context_dim set: the cross_k_w / cross_v_w arrays are required");
+    for (int l = 0; l < c->L; l += 2)
+      if (!w->cross_k_w[l] || !w->cross_v_w[l]) return set_err(c, GR00T_EINVAL, "block %d has a NULL cross weight", l);
+  }
   if (c->fp8w) {
     if (!w->qkv_s || !w->o_s || !w->up_s || !w->down_s)
       return set_err(c, GR00T_EINVAL, "FP8 weights need the per-layer scale arrays qkv_s/o_s/up_s/down_s");
@@ -359,6 +387,7 @@ int upload_weights(gr00t_ctx* c, const gr00t_weights* w) {
   const bool geglu = c->g.mlp_kind == GR00T_MLP_GEGLU;
   // staging: the largest matrix
   size_t big = (size_t)c->S * c->R * E;
+  big = std::max(big, (size_t)c->Hkv * c->Dh * (size_t)c->g.context_dim);
   for (int l = 0; l < c->L; ++l) {
     big = std::max(big, (size_t)c->nqkv[l] * D);
     big = std::max(big, (size_t)(geglu ? 2 : 1) * c->F * D);
@@ -409,6 +438,11 @@ int upload_weights(gr00t_ctx* c, const gr00t_weights* w) {
   }
   M(w->action_out_w, c->w_out, c->A, D, PERM_NONE, 0, 0);
   Bv(w->action_out_b, c->b_out, c->A);
+  if (dit && c->g.context_dim > 0)
+    for (int l = 0; l < c->L; l += 2) {
+      M(w->cross_k_w[l], c->w_ck[l], c->Hkv * c->Dh, c->g.context_dim, PERM_NONE, 0, 0);
+      M(w->cross_v_w[l], c->w_cv[l], c->Hkv * c->Dh, c->g.context_dim, PERM_NONE, 0, 0);
+    }
   cudaError_t e1 = cudaStreamSynchronize(c->stream);
   cudaError_t e2 = cudaFree(staging);
   if (rc != GR00T_OK) return rc;
@@ -952,6 +986,34 @@ extern "C" int gr00t_bind_prefix_kv(gr00t_ctx* c, int batch, int prefix, const v
   c->bP = prefix;
   c->bound = true;
   return GR00T_OK;
+}
+
+extern "C" int gr00t_bind_context(gr00t_ctx* c, int batch, int prefix, const void* features,
+                                  const uint8_t* text_mask, const uint8_t* image_mask,
+                                  const float* state_tokens) {
+  if (!c) return GR00T_EINVAL;
+  if (c->g.family != GR00T_FAMILY_DIT || c->g.context_dim <= 0)
+    return set_err(c, GR00T_ESTATE, "gr00t_bind_context needs a DiT geometry with context_dim > 0");
+  if (!features) return set_err(c, GR00T_EINVAL, "features is NULL");
+  if (batch < 1 || batch > c->g.max_batch)
+    return set_err(c, GR00T_EINVAL, "batch %d outside [1, %d]", batch, c->g.max_batch);
+  if (prefix < 1 || prefix > c->g.max_prefix)
+    return set_err(c, GR00T_EINVAL, "prefix %d outside [1, %d]", prefix, c->g.max_prefix);
+  const int Dc = c->g.context_dim, kd = c->Hkv * c->Dh, M = batch * prefix;
+  // a library copy of the features: one fixed operand address for the cached tensor maps
+  CK(c, cudaMemcpyAsync(c->ctx_feat, features, (size_t)M * Dc * c->esz, cudaMemcpyDeviceToDevice, c->stream));
+  c->launches = 0;
+  for (int l = 0; l < c->L; l += 2) {
+    for (int which = 0; which < 2; ++which) {
+      GemmArgs a;
+      a.A = c->ctx_feat; a.lda = Dc; a.W = which ? c->w_cv[l] : c->w_ck[l]; a.ldw = Dc;
+      a.M = M; a.N = kd; a.K = Dc;
+      a.epi.kind = EPI_STORE; a.epi.out = which ? c->ctx_v[l] : c->ctx_k[l]; a.epi.ldo = kd;
+      RC(gemm(c, a));
+    }
+  }
+  return gr00t_bind_prefix_kv(c, batch, prefix, (const void* const*)c->ctx_k.data(),
+                              (const void* const*)c->ctx_v.data(), text_mask, image_mask, state_tokens);
 }
 
 extern "C" int gr00t_set_schedule(gr00t_ctx* c, int steps, int batch) {

@@ -99,6 +99,8 @@ typedef struct gr00t_geometry {
   float rope_theta;      /* RoPE base (EXPERT family)                         */
   float norm_eps;        /* epsilon of RMSNorm / LayerNorm                    */
   int32_t weight_format; /* GR00T_WFMT_*: storage of the per-layer projections */
+  int32_t context_dim;   /* DIT: width of the VL features gr00t_bind_context projects
+                            into the cross K/V (multiple of 64); 0: K/V bound directly */
 } gr00t_geometry;
 
 /* Storage of the per-layer projections (qkv_w, o_w, up_w, down_w).  FP8: each
@@ -161,6 +163,11 @@ typedef struct gr00t_weights {
   const void* const* o_s;
   const void* const* up_s;
   const void* const* down_s;
+  /* DIT with context_dim > 0 (else NULL): per block, the cross-attention K and V
+   * projections [kv_heads*head_dim, context_dim] of the even blocks (odd entries
+   * NULL), in the geometry's dtype, no bias */
+  const void* const* cross_k_w;
+  const void* const* cross_v_w;
 } gr00t_weights;
 
 typedef struct gr00t_ctx gr00t_ctx;
@@ -207,6 +214,25 @@ int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, void* stream, 
 int gr00t_bind_prefix_kv(gr00t_ctx* ctx, int batch, int prefix, const void* const* k,
                          const void* const* v, const uint8_t* text_mask,
                          const uint8_t* image_mask, const float* state_tokens);
+
+/*
+ * DIT with context_dim > 0: project the per-request VL features into the cross
+ * K/V of every even block and bind them ("GR00T N1.7", vl_backbone: the VL
+ * engine ends with the DiT's cross-attention K/V projections, producing
+ * cross_k / cross_v [B, S, 32, 48] for the even blocks; the step runs once per
+ * request, before the denoise loop).  K_i = features W_k,i^T, V_i = features
+ * W_v,i^T on the tensor cores into library-owned [batch, prefix, kv_heads,
+ * head_dim] buffers, then bound as by gr00t_bind_prefix_kv.
+ *
+ * ``features``: DEVICE [batch, prefix, context_dim] in the geometry's dtype,
+ * read asynchronously on the stream (keep it unchanged until the stream has
+ * run this call's work).  Masks and state tokens as for gr00t_bind_prefix_kv.
+ * GR00T_ESTATE for a geometry without context_dim; GR00T_EINVAL for a batch or
+ * prefix out of range or a NULL features pointer.  Enqueues 2 GEMMs per cross
+ * block and a small copy on the stream.
+ */
+int gr00t_bind_context(gr00t_ctx* ctx, int batch, int prefix, const void* features, const uint8_t* text_mask,
+                       const uint8_t* image_mask, const float* state_tokens);
 
 /*
  * Hoist the time conditioning for a step count and batch ("pi0.5 Design",

@@ -80,6 +80,15 @@ def test_fp8_weight_geometry_rules(lib):
     assert rc == -1 and "weight_format" in msg
 
 
+def test_context_dim_rules(lib):
+    import flow_matching_vla_gb300 as fmv
+    assert fmv.validate_geometry(synth.config("gr00t_ctx"))[0] == 0
+    rc, msg = fmv.validate_geometry(synth.config("pi05", context_dim=256))
+    assert rc == -1 and "DiT" in msg
+    rc, msg = fmv.validate_geometry(synth.config("gr00t_ctx", context_dim=100))
+    assert rc == -1 and "context_dim" in msg
+
+
 def test_dit_geometry_rules(lib):
     import flow_matching_vla_gb300 as fmv
     g = synth.config("gr00t")

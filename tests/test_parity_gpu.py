@@ -226,3 +226,22 @@ def test_gr00t_fp8_full_size():
 
 def test_pi05_fp8_batch32_sampled():
     check_case(synth.make_case("pi05_fp8", batch=32), samples=[0, 31])
+
+
+# DiT cross K/V projected from VL features at bind time (gr00t_bind_context):
+# the oracle projects in fp64, the GPU on the tensor cores into bf16 K/V
+def test_dit_context_projection_small():
+    check_case(synth.make_case("small_dit_ctx"))
+
+
+def test_gr00t_context_projection_full_size():
+    check_case(synth.make_case("gr00t_ctx"))
+
+
+def test_bind_context_refused_without_context_dim():
+    fmv = _fmv()
+    loop, held = fmv.from_case(synth.make_case("small_dit"))
+    import torch
+    f = torch.zeros((2, 300, 256), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fmv.Gr00tError, match="ESTATE"):
+        loop.bind_context(f)
