@@ -222,6 +222,22 @@ class DenoiseLoop:
         self.batch = B
         return self
 
+    def bind_kv_pool(self, pools, prefix: int):
+        """EXPERT: bind per-layer paged K/V pools (device tensors [2, B, capacity, 1, Dh]
+        of the geometry dtype, prefix K/V in slot rows [0, prefix)); each step writes its
+        suffix K/V into rows [prefix, prefix + H).  The pools are borrowed and written."""
+        L = int(self.geom["layers"])
+        for t in pools:
+            if not (t.is_cuda and t.is_contiguous() and t.dtype == self.torch_dtype and t.dim() == 5):
+                raise ValueError("pools must be contiguous 5-D CUDA tensors [2, B, capacity, 1, Dh]")
+        B, cap = int(pools[0].shape[1]), int(pools[0].shape[2])
+        arr = (ctypes.c_void_p * L)(*[t.data_ptr() for t in pools])
+        self._check(self._lib.gr00t_bind_kv_pool(self._ctx, B, int(prefix), cap,
+                                                 ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))))
+        self._bound = (list(pools),)
+        self.batch = B
+        return self
+
     def bind_context(self, features, text_mask=None, image_mask=None, state=None):
         """DiT with context_dim: project VL features (device tensor [B, P, context_dim]
         of the geometry dtype) into the cross K/V on the GPU and bind them."""

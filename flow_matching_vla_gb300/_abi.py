@@ -60,6 +60,7 @@ SIGNATURES = {
                                     ctypes.POINTER(_VP)]),
     "gr00t_bind_prefix_kv": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VPP, _VPP, _VP, _VP, _VP]),
     "gr00t_bind_context": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, _VP, _VP, _VP, _VP]),
+    "gr00t_bind_kv_pool": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int, _VPP]),
     "gr00t_set_schedule": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int]),
     "gr00t_denoise": (ctypes.c_int, [_VP, _VP, _VP]),
     "gr00t_denoise_host": (ctypes.c_int, [_VP, _VP, _VP]),

@@ -101,6 +101,14 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d_hint(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z,
+                                                 int w, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(ptx::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z,
                                             int w) {
   asm volatile(
@@ -114,6 +122,12 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(m)),
                "r"(ptx::smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* src, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(ptx::smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
                : "memory");
 }
 __device__ __forceinline__ void tma_store_5d(const CUtensorMap* m, const void* src, int x, int y, int z, int w,
@@ -139,21 +153,24 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
 // Key tile i of sample b: prefix tiles first (64-key steps over [0, P)), then suffix tiles over [P, P + H).
 struct KeyTile {
   bool prefix;
-  int row;    // first row in the prefix map ([B*P]) or the suffix map ([B*H])
+  int row;    // first row: within sample b's prefix (the prefix map is per sample) or in the suffix map ([B*H])
   int valid;  // keys of the tile in range
+  int srow;   // suffix tiles: first suffix row of the tile within the sample
 };
 __device__ __forceinline__ KeyTile key_tile(int i, int b, int P, int H) {
   const int np = (P + KT - 1) / KT;
   KeyTile t;
   if (i < np) {
     t.prefix = true;
-    t.row = b * P + i * KT;
+    t.row = i * KT;
     t.valid = min(KT, P - i * KT);
+    t.srow = 0;
   } else {
     const int j = (i - np) * KT;
     t.prefix = false;
     t.row = b * H + j;
     t.valid = min(KT, H - j);
+    t.srow = j;
   }
   return t;
 }
@@ -163,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_t5_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKp,
                    const __grid_constant__ CUtensorMap tmVp, const __grid_constant__ CUtensorMap tmKs,
                    const __grid_constant__ CUtensorMap tmVs, const __grid_constant__ CUtensorMap tmO,
+                   const __grid_constant__ CUtensorMap tmPk, const __grid_constant__ CUtensorMap tmPv,
                    AttnT5Args a) {
   using L = T5Smem<DH>;
   extern __shared__ uint8_t smem_raw[];
@@ -201,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_end = min(ntiles, t_begin + tps);
   const int nt = t_end > t_begin ? t_end - t_begin : 0;
   const long long lim = a.wait_limit;
+  // a bound K/V pool takes this step's suffix K/V into its slots [P, P + H): the CTAs of
+  // the first row tile own the suffix tiles of their key range and store them from shared memory
+  const bool pool_writer = a.pool_k != nullptr && blockIdx.x == 0;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
@@ -249,9 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const KeyTile kt = key_tile(t_begin + i, b, a.P, a.H);
         uint8_t* dst = sKV + st * L::STAGE + (is_k ? 0 : L::KV_BYTES);
         ptx::mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
-        // [Dh/64 boxes][KT rows][64 columns] in one request (3-D map: columns, rows, boxes)
+        // [Dh/64 boxes][KT rows][64 columns] in one request; prefix: 4-D map (columns, rows
+        // [0, P) of the sample, samples, boxes) so rows past P read as zeros, never as a
+        // neighbour's rows or a pool's other slots
         if (kt.prefix)
-          tma_load_3d_hint(dst, is_k ? &tmKp : &tmVp, &full[st], 0, kt.row, 0, ptx::policy_evict_first());
+          tma_load_4d_hint(dst, is_k ? &tmKp : &tmVp, &full[st], 0, kt.row, b, 0, ptx::policy_evict_first());
         else
           tma_load_3d_hint(dst, is_k ? &tmKs : &tmVs, &full[st], 0, kt.row, 0, ptx::policy_evict_last());
       };
@@ -295,6 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ptx::mbar_wait(&k_full[st], (j >> 1) & 1, lim)) { fail(); break; }
           if (j >= 2 && !ptx::mbar_wait(&s_empty[sb], ((j >> 1) & 1) ^ 1, lim)) { fail(); break; }
           ptx::tc_fence_after();
+          const KeyTile kt = key_tile(t_begin + j, b, a.P, a.H);
+          if (pool_writer && !kt.prefix)   // rows past H fall outside the pool map
+            tma_store_4d(&tmPk, sKV + st * L::STAGE, 0, kt.srow, b, 0);
           const uint32_t q0 = ptx::smem_u32(sQ), k0 = ptx::smem_u32(sKV + st * L::STAGE);
 #pragma unroll
           for (int x = 0; x < L::BOXES; ++x)
@@ -303,6 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::mma_bf16(tS + sb * KT, ptx::sdesc_sw128(q0 + x * ROWS * 128) + 2 * k,
                             ptx::sdesc_sw128(k0 + x * KT * 128) + 2 * k, idS, (x | k) != 0);
           ptx::mma_commit(&s_full[sb]);
+          if (pool_writer && !kt.prefix) {   // the slot is refilled only after the store read it
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          }
           ptx::mma_commit(&k_empty[st]);
         }
         if (j >= 1) {  // O += P(j-1) V(j-1)
@@ -310,6 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ptx::mbar_wait(&p_full[pb], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
           if (!ptx::mbar_wait(&v_full[st], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
           ptx::tc_fence_after();
+          const KeyTile vt = key_tile(t_begin + j - 1, b, a.P, a.H);
+          if (pool_writer && !vt.prefix) tma_store_4d(&tmPv, sKV + st * L::STAGE + L::KV_BYTES, 0, vt.srow, b, 0);
           const uint32_t p0 = ptx::smem_u32(sP + pb * L::P_BYTES);
           const uint32_t v0 = ptx::smem_u32(sKV + st * L::STAGE + L::KV_BYTES);
 #pragma unroll
@@ -317,9 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_bf16(tO, ptx::sdesc_sw128(p0) + 2 * k, sdesc_sw128_mn(v0 + k * 2048, KT * 128), idO,
                           (j - 1) > 0 || k > 0);
           ptx::mma_commit(&pv_done[pb]);
+          if (pool_writer && !vt.prefix) {
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+          }
           ptx::mma_commit(&v_empty[st]);
         }
       }
+      if (pool_writer) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // pool writes done
     }
   } else {
     // ---------------- softmax (warps 2..9: TMEM lane quadrant = warp % 4) ----------------
@@ -532,7 +569,7 @@ cudaError_t launch_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaS
     configured = true;
   }
   cudaError_t e = launch_k(kern, dim3((a.Hq * a.H + ROWS - 1) / ROWS, S, a.B), dim3(kThreads), L::TOTAL, s, pdl,
-                           maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], a);
+                           maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], a);
   if (e != cudaSuccess || S == 1) return e;
   const long long warps = (long long)a.B * a.Hq * a.H;
   return launch_k(attn_t5_combine_kernel<DH>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, pdl, a, S);
@@ -582,7 +619,9 @@ long long attn_t5_workspace_floats(const AttnT5Args& a, int S) {
 // maps: [0] Q (3-D over [B*H tokens][Hq][Dh] inside qkv), [1] prefix K, [2] prefix V ([B*P][Dh]),
 //       [3] suffix K, [4] suffix V (2-D over qkv [B*H][ldq]; x offsets k_off / v_off),
 //       [5] the output tile: S > 1 the workspace partials [slot * 128 + row][Dh], S = 1 the
-//           attention output [B][H][Hq][Dh] inside out (row stride ldo)
+//           attention output [B][H][Hq][Dh] inside out (row stride ldo),
+//       [6], [7] a bound pool's suffix slots of K and V: (64 columns, H rows, B samples of
+//           pool_cap rows, Dh/64 boxes) from row P (copies of [1] when no pool is bound)
 cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, int S, CUtensorMap* maps) {
   const int D = a.Dh;
   const cuuint32_t nbox = (cuuint32_t)(D / 64);
@@ -592,15 +631,17 @@ cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, in
   const cuuint32_t qb[4] = {64, (cuuint32_t)a.Hq, (cuuint32_t)(ROWS / a.Hq), nbox};
   cudaError_t e = encode(&maps[0], a.qkv, 4, qd, qs, qb);
   if (e != cudaSuccess) return e;
-  // K / V tiles: (64 columns, rows, Dh/64 boxes), box = one 64-key tile
+  // K / V tiles: box = one 64-key tile of all Dh/64 column boxes.  Prefix: (64 columns, P rows,
+  // B samples ps rows apart -- ps = P, or a pool's capacity -- Dh/64 boxes)
   const cuuint32_t kb[3] = {64, KT, nbox};
-  const long long prow = (long long)a.B * (a.P > 0 ? a.P : 1);
-  const cuuint64_t pd[3] = {64, (cuuint64_t)prow, nbox};
-  const cuuint64_t ps[2] = {(cuuint64_t)D * 2, 128};
+  const cuuint32_t kb4[4] = {64, KT, 1, nbox};
+  const long long prows = a.P > 0 ? a.P : 1, pstride = a.ps > 0 ? a.ps : prows;
+  const cuuint64_t pd[4] = {64, (cuuint64_t)prows, (cuuint64_t)a.B, nbox};
+  const cuuint64_t ps[3] = {(cuuint64_t)D * 2, (cuuint64_t)pstride * D * 2, 128};
   // with no prefix the prefix maps are never used: point them at the suffix rows
-  e = encode(&maps[1], a.P > 0 ? kp : a.qkv, 3, pd, ps, kb);
+  e = encode(&maps[1], a.P > 0 ? kp : a.qkv, 4, pd, ps, kb4);
   if (e != cudaSuccess) return e;
-  e = encode(&maps[2], a.P > 0 ? vp : a.qkv, 3, pd, ps, kb);
+  e = encode(&maps[2], a.P > 0 ? vp : a.qkv, 4, pd, ps, kb4);
   if (e != cudaSuccess) return e;
   const cuuint64_t sd[3] = {64, (cuuint64_t)a.B * a.H, nbox};
   const cuuint64_t ss[2] = {(cuuint64_t)a.ldq * 2, 128};
@@ -608,6 +649,18 @@ cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, in
   if (e != cudaSuccess) return e;
   e = encode(&maps[4], static_cast<const bf16*>(a.qkv) + a.v_off, 3, sd, ss, kb);
   if (e != cudaSuccess) return e;
+  if (a.pool_k) {
+    const cuuint64_t pd4[4] = {64, (cuuint64_t)a.H, (cuuint64_t)a.B, nbox};
+    const cuuint64_t ps4[3] = {(cuuint64_t)D * 2, (cuuint64_t)a.pool_cap * D * 2, 128};
+    const cuuint32_t pb4[4] = {64, KT, 1, nbox};
+    e = encode(&maps[6], static_cast<const bf16*>(a.pool_k) + (long long)a.P * D, 4, pd4, ps4, pb4);
+    if (e != cudaSuccess) return e;
+    e = encode(&maps[7], static_cast<const bf16*>(a.pool_v) + (long long)a.P * D, 4, pd4, ps4, pb4);
+    if (e != cudaSuccess) return e;
+  } else {
+    maps[6] = maps[1];
+    maps[7] = maps[1];
+  }
   if (S > 1) {
     // (64 columns, partial rows, Dh/64 boxes): one 128-row tile per request
     const long long rows = (long long)((a.Hq * a.H + ROWS - 1) / ROWS) * a.B * S * ROWS;

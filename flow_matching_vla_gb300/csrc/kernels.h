@@ -149,6 +149,10 @@ struct AttnT5Args {
   long long ws_floats = 0;
   int* err = nullptr;         // device error word (bounded waits)
   long long wait_limit = 0;
+  int ps = 0;                 // rows per sample of the bound prefix K/V (0: P; a pool: its capacity)
+  void* pool_k = nullptr;     // a bound pool's K and V planes: this step's suffix K/V go to
+  void* pool_v = nullptr;     // rows [P, P + H) of each sample's slot (nullptr: no pool)
+  int pool_cap = 0;
 };
 }  // namespace g3
 #include <cuda.h>
@@ -156,7 +160,7 @@ namespace g3 {
 bool attn_t5_supported(int Dh, int Hq);
 int attn_t5_splits(const AttnT5Args& a, int sm_count, int cap = 0);   // cap > 0: at most cap splits
 long long attn_t5_workspace_floats(const AttnT5Args& a, int S);
-// maps[6]: Q, prefix K, prefix V, suffix K, suffix V, the output tile (S: the key splits)
+// maps[8]: Q, prefix K, prefix V, suffix K, suffix V, the output tile (S: the key splits), pool K, pool V
 cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, int S, CUtensorMap* maps);
 cudaError_t attention_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaStream_t s, bool pdl);
 

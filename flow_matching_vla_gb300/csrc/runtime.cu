@@ -70,6 +70,9 @@ struct gr00t_ctx {
   // state
   bool bound = false, scheduled = false;
   int bB = 0, bP = 0, sT = 0, sB = 0;
+  // a bound paged K/V pool (EXPERT): per-layer base of [2][B][cap][1][Dh]; rows per sample
+  std::vector<void*> pool;
+  int pool_cap = 0;
   std::vector<const void*> host_table;
 
   // graph cache (one entry)
@@ -630,10 +633,18 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         a5.ws = c->gemm_ws; a5.ws_floats = c->gemm_ws_floats;
         a5.err = c->err_flag; a5.wait_limit = c->wait_limit;
         const int splits = attn_t5_splits(a5, c->sm_count, c->opt_attn_splits);
-        CUtensorMap maps[6];
+        if (!c->pool.empty()) {   // prefix rows at stride cap; this step's suffix K/V into slots [P, P + H)
+          a5.ps = c->pool_cap;
+          a5.pool_cap = c->pool_cap;
+          a5.pool_k = c->pool[l];
+          a5.pool_v = (char*)c->pool[l] + (size_t)B * c->pool_cap * c->Dh * es;
+        }
+        CUtensorMap maps[8];
         CK(c, attn_t5_maps(a5, c->host_table[2 * l], c->host_table[2 * l + 1], splits, maps));
         if (splits > 1) ++c->launches;   // the split merge is a second kernel
         CK(c, attention_t5(a5, maps, splits, s, c->opt_pdl != 0));
+      } else if (!c->pool.empty()) {
+        return set_err(c, GR00T_EUNSUPPORTED, "a bound K/V pool needs the tcgen05 attention (bf16, attention path 0 or 3)");
       } else if (c->dt == DT_BF16 && (c->opt_attn == 0 || c->opt_attn == 2) && attn_fold_supported(c->Dh)) {
         AttnFoldArgs af;
         af.qkv = c->qkv; af.ldq = nq; af.k_off = c->qd; af.v_off = c->qd + c->Dh;
@@ -985,6 +996,40 @@ extern "C" int gr00t_bind_prefix_kv(gr00t_ctx* c, int batch, int prefix, const v
   c->bB = batch;
   c->bP = prefix;
   c->bound = true;
+  if (!c->pool.empty()) {   // a plain bind replaces a bound pool
+    c->pool.clear();
+    c->pool_cap = 0;
+    if (c->gexec) {
+      cudaGraphExecDestroy(c->gexec);
+      c->gexec = nullptr;
+    }
+  }
+  return GR00T_OK;
+}
+
+extern "C" int gr00t_bind_kv_pool(gr00t_ctx* c, int batch, int prefix, int capacity, void* const* pools) {
+  if (!c) return GR00T_EINVAL;
+  if (c->g.family != GR00T_FAMILY_EXPERT)
+    return set_err(c, GR00T_EINVAL, "the paged K/V pool is an expert-family binding (one KV head)");
+  if (!pools) return set_err(c, GR00T_EINVAL, "pools is NULL");
+  if (capacity < prefix + c->H || capacity % 128)
+    return set_err(c, GR00T_EINVAL, "capacity %d must be a multiple of 128 holding prefix + horizon = %d", capacity,
+                   prefix + c->H);
+  for (int l = 0; l < c->L; ++l)
+    if (!pools[l]) return set_err(c, GR00T_EINVAL, "layer %d pool is NULL", l);
+  // plane-major: every sample's K slot, then every sample's V slot
+  std::vector<const void*> k(c->L), v(c->L);
+  for (int l = 0; l < c->L; ++l) {
+    k[l] = pools[l];
+    v[l] = (const char*)pools[l] + (size_t)batch * capacity * c->Dh * c->esz;
+  }
+  RC(gr00t_bind_prefix_kv(c, batch, prefix, k.data(), v.data(), nullptr, nullptr, nullptr));
+  c->pool.assign(pools, pools + c->L);
+  c->pool_cap = capacity;
+  if (c->gexec) {   // the attention's tensor maps embed the pool layout
+    cudaGraphExecDestroy(c->gexec);
+    c->gexec = nullptr;
+  }
   return GR00T_OK;
 }
 

@@ -235,6 +235,23 @@ int gr00t_bind_context(gr00t_ctx* ctx, int batch, int prefix, const void* featur
                        const uint8_t* image_mask, const float* state_tokens);
 
 /*
+ * EXPERT: bind the pages' paged K/V pool directly ("pi0.5 Design", Attention
+ * and the K/V pool): per layer one DEVICE buffer [2][batch][capacity][1][head_dim]
+ * in the geometry's dtype, plane-major -- every sample's K slot, then every
+ * sample's V slot (the V plane begins past every slot's K) -- with pages of 128
+ * rows under an identity page table, so a slot is a flat [capacity, head_dim]
+ * region.  Slot rows [0, prefix) hold the prefix K/V (keys rotated by RoPE at
+ * positions 0..prefix-1); every denoise step writes its action tokens' K/V into
+ * rows [prefix, prefix + horizon), as the pages' attention plugin appends them
+ * (after a denoise they hold the last step's).  ``capacity``: a multiple of 128
+ * with capacity >= prefix + horizon (the pages round prefix + horizon up to 256).
+ * The pools are BORROWED and WRITTEN: keep them alive until the next bind or
+ * gr00t_destroy.  Needs the tensor-core attention (bf16, GR00T_OPT_ATTN_PATH 0
+ * or 3); a later gr00t_bind_prefix_kv replaces the pool binding.
+ */
+int gr00t_bind_kv_pool(gr00t_ctx* ctx, int batch, int prefix, int capacity, void* const* pools);
+
+/*
  * Hoist the time conditioning for a step count and batch ("pi0.5 Design",
  * cond component: the time embedder and the AdaRMS Denses leave the
  * per-step graph and are evaluated again only for a new step count or batch;

@@ -245,3 +245,88 @@ def test_bind_context_refused_without_context_dim():
     f = torch.zeros((2, 300, 256), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fmv.Gr00tError, match="ESTATE"):
         loop.bind_context(f)
+
+
+# the pages' plane-major paged K/V pool bound directly: [2, B, capacity, 1, Dh]
+# per layer, prefix in slot rows [0, P), every step's action K/V appended into
+# rows [P, P + H); the filler rows must neither be read nor overwritten
+def _pool_case(capacity=384):
+    import torch
+    case = synth.make_case("small_bf16", batch=2, prefix=200)
+    g = case["geom"]
+    B, P, Dh = g["batch"], g["prefix"], g["head_dim"]
+    pools = []
+    for l in range(g["layers"]):
+        pool = torch.full((2, B, capacity, 1, Dh), 1000.0, dtype=torch.bfloat16, device="cuda")
+        pool[0, :, :P] = torch.from_numpy(case["K"][l]).to(torch.bfloat16).cuda()
+        pool[1, :, :P] = torch.from_numpy(case["V"][l]).to(torch.bfloat16).cuda()
+        pools.append(pool)
+    return case, pools
+
+
+def test_expert_paged_kv_pool_parity():
+    import torch
+    fmv = _fmv()
+    case, pools = _pool_case()
+    g = case["geom"]
+    B, P, H = g["batch"], g["prefix"], g["horizon"]
+    keep = [p.clone() for p in pools]
+    loop = fmv.DenoiseLoop(g, case["weights"])
+    loop.bind_kv_pool(pools, P)
+    loop.set_schedule(g["steps"], B)
+    out = loop.denoise(torch.from_numpy(case["x_noise"]).cuda())
+    torch.cuda.synchronize()
+    e_inf, _ = oracle.error_metrics(out.cpu().numpy(), oracle.denoise(case))
+    assert e_inf <= BF16_CHUNK_ABS, f"final chunk max-abs {e_inf:.3e}"
+    for p, p0 in zip(pools, keep):
+        assert torch.equal(p[:, :, :P], p0[:, :, :P])                 # prefix untouched
+        assert torch.equal(p[:, :, P + H:], p0[:, :, P + H:])         # past the suffix slots untouched
+        assert float(p[:, :, P:P + H].float().abs().max()) < 100.0    # suffix slots written
+
+
+def test_expert_paged_kv_pool_appends_the_step_suffix_kv():
+    # one teacher-forced step from x: layer 0's slots [P, P + H) hold that step's
+    # action-token K (RoPE at positions P + j) and V
+    import torch
+    from oracle.expert import ada_rms
+    fmv = _fmv()
+    case, pools = _pool_case()
+    g = case["geom"]
+    B, P, H, Hq, Dh = g["batch"], g["prefix"], g["horizon"], g["q_heads"], g["head_dim"]
+    loop = fmv.DenoiseLoop(g, case["weights"])
+    loop.bind_kv_pool(pools, P)
+    loop.set_schedule(g["steps"], B)
+    k = 1
+    x = case["x_noise"]
+    loop.denoise_step(k, torch.from_numpy(x).cuda())
+    torch.cuda.synchronize()
+    w = case["weights"]
+    mod = oracle.modulation_table(g, w, g["steps"], B)[k * B:(k + 1) * B]
+    trace = {}
+    oracle.expert_velocity(g, w, x, mod, case["K"], case["V"], trace=trace)
+    for b in range(B):
+        n, _ = ada_rms(trace["h_in"][b], mod[b, 0].astype(np.float64), g["norm_eps"])
+        qkv = n @ w["qkv_w.0"].astype(np.float64).T
+        k_ref = oracle.rope_rotate_half(qkv[:, Hq * Dh:Hq * Dh + Dh], P + np.arange(H), g["rope_theta"])
+        v_ref = qkv[:, Hq * Dh + Dh:Hq * Dh + 2 * Dh]
+        k_got = pools[0][0, b, P:P + H, 0].float().cpu().numpy()
+        v_got = pools[0][1, b, P:P + H, 0].float().cpu().numpy()
+        for got, ref in ((k_got, k_ref), (v_got, v_ref)):
+            _, rel = oracle.error_metrics(got, ref)
+            assert rel <= BF16_VEL_REL, f"sample {b}: suffix slot rel-L2 {rel:.3e}"
+
+
+def test_paged_kv_pool_refusals():
+    import torch
+    fmv = _fmv()
+    case, pools = _pool_case()
+    g = case["geom"]
+    loop = fmv.DenoiseLoop(g, case["weights"])
+    small = [torch.zeros((2, 2, 200, 1, g["head_dim"]), dtype=torch.bfloat16, device="cuda")] * g["layers"]
+    with pytest.raises(fmv.Gr00tError, match="capacity"):
+        loop.bind_kv_pool(small, g["prefix"])   # 200 < prefix + horizon, not a multiple of 128
+    loop.bind_kv_pool(pools, g["prefix"])
+    loop.set_schedule(g["steps"], g["batch"])
+    loop.set_option(fmv.OPT_ATTN_PATH, 1)
+    with pytest.raises(fmv.Gr00tError, match="tcgen05 attention"):
+        loop.denoise(torch.from_numpy(case["x_noise"]).cuda())
