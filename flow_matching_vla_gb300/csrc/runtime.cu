@@ -482,16 +482,19 @@ const CUtensorMap* tmap(gr00t_ctx* c, const void* ptr, long long rows, long long
 }
 
 // The split-K plan of a tensor-core GEMM (E4M3 weights: stages of 128 K elements).
-TcPlan plan_of(gr00t_ctx* c, const GemmArgs& a, bool partial) {
+TcPlan plan_of(gr00t_ctx* c, int M, int N, int K, bool e4m3, bool partial) {
   const int cap = partial ? c->resid_split_cap : c->split_cap;
-  return a.epi.wscale ? tc_plan_e4m3(a.M, a.N, a.K, c->sm_count, cap, partial)
-                      : tc_plan(a.M, a.N, a.K, c->sm_count, cap, partial);
+  return e4m3 ? tc_plan_e4m3(M, N, K, c->sm_count, cap, partial) : tc_plan(M, N, K, c->sm_count, cap, partial);
+}
+TcPlan plan_of(gr00t_ctx* c, const GemmArgs& a, bool partial) {
+  return plan_of(c, a.M, a.N, a.K, a.epi.wscale != nullptr, partial);
 }
 
-bool tc_ok(gr00t_ctx* c, const GemmArgs& a) {
+bool tc_ok(gr00t_ctx* c, int M, int N, int K, bool e4m3) {
   if (c->dt != DT_BF16 || c->opt_gemm != 0) return false;
-  return a.epi.wscale ? tc_supported_e4m3(a.M, a.N, a.K) : tc_supported(a.M, a.N, a.K);
+  return e4m3 ? tc_supported_e4m3(M, N, K) : tc_supported(M, N, K);
 }
+bool tc_ok(gr00t_ctx* c, const GemmArgs& a) { return tc_ok(c, a.M, a.N, a.K, a.epi.wscale != nullptr); }
 
 int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
   ++c->launches;
@@ -1289,16 +1292,12 @@ cudaError_t noalloc_scratch(int dev, float** out) {
 // Scratch (fp32 elements) one GEMM of the step uses when the scratch holds ``cap``
 // elements; mirrors gemm() / gemm_resid().
 long long gemm_scratch(gr00t_ctx* c, int M, int N, int K, bool resid, long long cap, bool e4m3 = false) {
-  GemmArgs a;
-  a.M = M; a.N = N; a.K = K;
-  static const float kAnyScale = 1.f;
-  a.epi.wscale = e4m3 ? &kAnyScale : nullptr;   // selects the E4M3 planner only
-  if (!tc_ok(c, a)) return 0;
+  if (!tc_ok(c, M, N, K, e4m3)) return 0;
   if (resid) {
-    const TcPlan p = plan_of(c, a, true);
+    const TcPlan p = plan_of(c, M, N, K, e4m3, true);
     if (p.S > 1 && (long long)p.S * M * N <= cap) return (long long)p.S * M * N;
   }
-  return tc_workspace_floats(plan_of(c, a, false), M, N);
+  return tc_workspace_floats(plan_of(c, M, N, K, e4m3, false), M, N);
 }
 
 // Largest scratch any kernel of one denoise step needs at the bound (batch, prefix).

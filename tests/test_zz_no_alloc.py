@@ -25,7 +25,7 @@ def _fmv():
     return fmv
 
 
-@pytest.mark.parametrize("name", ["small_bf16", "pi05"])
+@pytest.mark.parametrize("name", ["small_bf16", "pi05", "small_fp8"])
 def test_noalloc_step_matches_regular_step_twice(name):
     fmv = _fmv()
     c = synth.make_case(name)
