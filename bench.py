@@ -103,7 +103,7 @@ KCLASS = {"qkv_gemm": 1, "attention": 2, "o_gemm": 3, "up_gemm": 4, "down_gemm":
 # capture (profiles/pi05_b1_kernels_full.md, profiles/pi05_b32_kernels_full.md),
 # with the SHA-1 prefixes of the sources those kernels were built from: a value
 # is reported only while every listed source is unchanged.
-_GEMM_SRC = {"gemm_tc.cu": "b74dca9bc633c271", "epilogue.cuh": "8f28ff6cb7f33192"}
+_GEMM_SRC = {"gemm_tc.cu": "394de066eb6a04ef", "epilogue.cuh": "8f28ff6cb7f33192"}
 _ATTN_SRC = {"attention_tc5.cu": "a75b1ec94792525a"}
 TRAFFIC = {
     ("pi05", "attention"): (1.28e6 + 3.56e6, _ATTN_SRC),   # attention + split merge

@@ -2,18 +2,22 @@
 // fp32 accumulate in tensor memory (tcgen05.mma, kind::f16), fused epilogues.
 //
 // Shapes are weight-streaming: N (weight rows) is large, M (token rows) is
-// 50..1600.  The weight therefore plays the MMA's M role ("swap-AB"): each
+// 17..1600.  The weight therefore plays the MMA's M role ("swap-AB"): each
 // CTA owns 128 weight rows and BN tokens, D[128, BN] lives in TMEM.
 //
 //  * TMA (cp.async.bulk.tensor, 128-byte swizzle) streams 128x64 weight tiles
 //    (L2 evict-first) and BNx64 activation tiles (L2 evict-last) through a
 //    STAGES-deep mbarrier ring; one thread issues loads, one issues MMAs.
-//  * Split-K across a thread-block cluster (1 x 1 x S, S <= 16): every CTA of
-//    the cluster accumulates a K slice and parks its fp32 partial in an
-//    L2-resident workspace; after one cluster barrier each CTA sums 128/S rows
-//    over the S partials in rank order (deterministic) and applies the
-//    epilogue to them.  Without a split the epilogue runs straight from the
-//    TMEM registers (adjacent lanes swap one value to form output pairs).
+//  * Split-K across a thread-block cluster (1 x 1 x S): for 64/128-token tiles
+//    each CTA parks its fp32 partial in its idle pipeline memory and hands every
+//    peer the 128/S rows that peer reduces with one shared-to-peer bulk copy;
+//    256-token tiles go through an L2-resident workspace; either way the S
+//    partials are summed in rank order (deterministic).  Residual GEMMs may
+//    instead leave their partials for the next norm kernel (EPI_PARTIAL).
+//    Without a split the epilogue runs straight from the TMEM registers
+//    (adjacent lanes swap one value to form output pairs).
+//  * E4M3 weights (WF_E4M3): code tiles are widened into bf16 A tiles held in
+//    tensor memory; the row scales finish the accumulator in the epilogue.
 //  * Programmatic dependent launch: weight tiles (which no earlier kernel
 //    writes) are prefetched before griddepcontrol.wait; activations after.
 //  * Every mbarrier wait is bounded; on timeout the CTA records an error
