@@ -884,19 +884,10 @@ extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, voi
   int rc = validate(g, msg, sizeof msg);
   if (rc != GR00T_OK) return set_err(nullptr, rc, "invalid geometry: %s", msg);
 
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  cudaDeviceProp prop;
-  if (e == cudaSuccess) e = cudaGetDeviceProperties(&prop, dev);
-  if (e != cudaSuccess) return set_err(nullptr, GR00T_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
-  if (!(prop.major == 10 && prop.minor == 3))
-    return set_err(nullptr, GR00T_EUNSUPPORTED, "device %s is sm_%d%d; this library is built for sm_103a",
-                   prop.name, prop.major, prop.minor);
-
+  // host-side checks of the geometry and the weight pointers first: nothing touches the GPU
+  // before they pass
   gr00t_ctx* c = new gr00t_ctx();
   c->g = *g;
-  c->sm_count = prop.multiProcessorCount;
-  c->device = dev;
   c->dt = g->dtype == GR00T_DTYPE_BF16 ? DT_BF16 : DT_F32;
   c->esz = c->dt == DT_BF16 ? 2 : 4;
   c->fp8w = g->weight_format == GR00T_WFMT_FP8;
@@ -917,6 +908,22 @@ extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, voi
     delete c;
     return rc;
   }
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  cudaDeviceProp prop;
+  if (e == cudaSuccess) e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) {
+    delete c;
+    return set_err(nullptr, GR00T_ECUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  }
+  if (!(prop.major == 10 && prop.minor == 3)) {
+    delete c;
+    return set_err(nullptr, GR00T_EUNSUPPORTED, "device %s is sm_%d%d; this library is built for sm_103a",
+                   prop.name, prop.major, prop.minor);
+  }
+  c->sm_count = prop.multiProcessorCount;
+  c->device = dev;
   if (stream) {
     c->stream = (cudaStream_t)stream;
   } else {

@@ -113,6 +113,40 @@ def test_create_refuses_before_touching_cuda(lib):
     assert lib.gr00t_create(ctypes.byref(geo), ctypes.byref(w), None, None) == -1
 
 
+def _dummy_weights(g, skip=()):
+    """A gr00t_weights with every pointer the geometry needs set to a dummy
+    non-NULL value (create checks presence before it touches the GPU)."""
+    from flow_matching_vla_gb300 import _abi
+    w = _abi.Weights()
+    w.location = _abi.MEM_DEVICE
+    one = ctypes.c_void_p(16)
+    for name, _ in _abi.Weights._fields_[1:]:
+        if name in skip:
+            continue
+        if name in ("qkv_w", "o_w", "up_w", "down_w", "qkv_s", "o_s", "up_s", "down_s", "cross_k_w", "cross_v_w"):
+            arr = (ctypes.c_void_p * g["layers"])(*([16] * g["layers"]))
+            setattr(w, name, ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p)))
+            w._keep = getattr(w, "_keep", []) + [arr]
+        else:
+            setattr(w, name, one)
+    return w
+
+
+@pytest.mark.parametrize("cfg,skip,needle", [
+    ("pi05_fp8", ("qkv_s",), b"scale"),
+    ("gr00t_ctx", ("cross_v_w",), b"cross"),
+    ("pi05", ("cond_w",), b"cond_w"),
+])
+def test_create_checks_weight_pointers_before_touching_cuda(lib, cfg, skip, needle):
+    import flow_matching_vla_gb300 as fmv
+    g = synth.config(cfg)
+    ctx = ctypes.c_void_p(1)
+    rc = lib.gr00t_create(ctypes.byref(fmv._geometry(g)), ctypes.byref(_dummy_weights(g, skip)), None,
+                          ctypes.byref(ctx))
+    assert rc == -1 and ctx.value is None
+    assert needle in lib.gr00t_last_error(None)
+
+
 def test_null_context_calls_are_einval(lib):
     assert lib.gr00t_set_schedule(None, 1, 1) == -1
     assert lib.gr00t_denoise(None, None, None) == -1
