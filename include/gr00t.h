@@ -16,6 +16,12 @@
  *       cross-attention into the VL context and self-attention over the
  *       state + action tokens.
  *
+ * Inputs of a request are bound once before the loop: per-layer prefix K/V
+ * (gr00t_bind_prefix_kv), the pages' paged K/V pool (gr00t_bind_kv_pool,
+ * EXPERT), or VL features whose cross K/V the library projects itself
+ * (gr00t_bind_context, DIT).  The per-layer projections may be streamed as
+ * E4M3 codes with row scales (GR00T_WFMT_FP8).
+ *
  * Conventions shared by every call:
  *   - Every function returns GR00T_OK (0) or a negative GR00T_E* status.
  *     gr00t_last_error() gives a one-line text for the context's last error.
@@ -25,7 +31,8 @@
  *   - Matrices are row-major.  Weights use the nn.Linear layout [out, in].
  *   - "bf16" tensors are raw IEEE bfloat16 bit patterns (uint16_t).
  *   - Nothing here allocates on a call except gr00t_create (and graph
- *     instantiation on the first denoise of a new (steps, batch, prefix)).
+ *     instantiation on the first denoise of a new (steps, batch, prefix) or
+ *     binding layout).
  *   - No call ever falls back to the CPU.  Without a usable sm_103a device
  *     gr00t_create returns GR00T_ECUDA.
  */
