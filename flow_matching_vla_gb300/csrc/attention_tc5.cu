@@ -5,23 +5,28 @@
 // mask; vla.cpp Eq. (2) per row), on the 5th-generation tensor cores:
 //
 //  * a CTA owns 128 folded rows (r = t * Hq + h) and a range of 64-key tiles;
-//    the prefix tiles come from the bound per-layer K/V, the suffix tiles from
-//    this step's QKV projection;
-//  * warps 0 and 6 issue TMA: Q once through a 3-D map over [tokens][heads][Dh]
+//    the prefix tiles come from the bound per-layer K/V (a flat [B, P] region or
+//    a paged pool's slots, through a per-sample map: rows past P read as zeros),
+//    the suffix tiles from this step's QKV projection;
+//  * warps 0 and 10 issue TMA: Q once through a 4-D map over [tokens][heads][Dh]
 //    whose box lands exactly in folded-row order; K and V tiles through
 //    separate 2-slot rings (128-byte swizzle, 64-element boxes), a K slot
 //    freed as soon as S = QK^T read it, a V slot when P V did;
 //  * warp 1 issues tcgen05.mma: S = Q K^T into one of two TMEM buffers
 //    (kind::f16, K-major operands), and O += P V into a TMEM accumulator with
-//    V read MN-major straight from its [key][dim] tile;
-//  * warps 2..5 (one thread per row, the TMEM lane) run the softmax in
-//    registers: exp2 of scaled scores against a running maximum that is only
-//    raised -- and O rescaled in TMEM -- when a tile's maximum exceeds it by
-//    more than 8 (2^8 headroom, exact arithmetic otherwise), write P (bf16)
-//    into shared memory in the MMA's swizzled K-major layout and hand it to
-//    the MMA warp;
-//  * with S key splits each split CTA writes its partial (O / sum as bf16, and
-//    (max, sum)) to the workspace; a warp-per-row kernel merges the S splits.
+//    V read MN-major straight from its [key][dim] tile; with a paged pool bound,
+//    the first row tile's CTAs also store the suffix K/V tiles into the pool's
+//    slots [P, P + H);
+//  * warps 2..9 (two per TMEM lane quadrant: one thread per row for each half
+//    of a tile's keys and of O's columns) run the softmax in registers: exp2 of
+//    scaled scores against a running maximum that is only raised -- and O
+//    rescaled in TMEM -- when a tile's maximum exceeds it by more than 8 (2^8
+//    headroom, exact arithmetic otherwise), write P (bf16) into shared memory
+//    in the MMA's swizzled K-major layout and hand it to the MMA warp;
+//  * the output tile (O / sum, bf16) is staged in the idle Q buffer and written
+//    with one tensor store: to the attention output, or with S key splits as a
+//    partial (with (max, sum)) to the workspace, where a warp-per-row kernel
+//    merges the S splits.
 // All mbarrier waits are bounded (error flag, drained copies, freed TMEM).
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -616,8 +621,9 @@ long long attn_t5_workspace_floats(const AttnT5Args& a, int S) {
   return (bytes + 3) / 4;
 }
 
-// maps: [0] Q (3-D over [B*H tokens][Hq][Dh] inside qkv), [1] prefix K, [2] prefix V ([B*P][Dh]),
-//       [3] suffix K, [4] suffix V (2-D over qkv [B*H][ldq]; x offsets k_off / v_off),
+// maps: [0] Q (4-D: 64 columns, Hq heads, B*H tokens, Dh/64 boxes inside qkv), [1] prefix K, [2] prefix V
+//       (4-D per sample, rows [0, P) at the sample stride),
+//       [3] suffix K, [4] suffix V (3-D: 64 columns, B*H rows of qkv, Dh/64 boxes; based at k_off / v_off),
 //       [5] the output tile: S > 1 the workspace partials [slot * 128 + row][Dh], S = 1 the
 //           attention output [B][H][Hq][Dh] inside out (row stride ldo),
 //       [6], [7] a bound pool's suffix slots of K and V: (64 columns, H rows, B samples of
