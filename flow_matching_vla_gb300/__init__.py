@@ -27,12 +27,12 @@ import numpy as np
 
 from . import _abi
 from ._abi import (DTYPE_BF16, DTYPE_FP32, FAMILY_DIT, FAMILY_EXPERT, MLP_GEGLU, MLP_GELU,
-                   OPT_ATTN_PATH, OPT_GEMM_PATH, OPT_TIME_KERNEL, OPT_USE_GRAPH, OPT_WAIT_LIMIT,
+                   OPT_ATTN_PATH, OPT_GEMM_PATH, OPT_TIME_KERNELS, OPT_USE_GRAPH, OPT_WAIT_LIMIT,
                    OPT_SPLIT_CAP, OPT_RESID_SPLIT_CAP, OPT_PERSISTENT_GEMM, OPT_L2_PREFETCH, OPT_NOALLOC_LIMIT,
-                   OPT_ATTN_SPLIT_CAP,
+                   OPT_ATTN_SPLIT_CAP, OPT_TEST_STALL, ETIMEOUT,
                    INFO_DEVICE_BYTES, INFO_ERROR_FLAG, INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES,
                    KCLASS_ATTENTION, KCLASS_DOWN_GEMM, KCLASS_NORM, KCLASS_O_GEMM, KCLASS_QKV_GEMM,
-                   KCLASS_UP_GEMM, WFMT_NATIVE, WFMT_FP8)
+                   KCLASS_UP_GEMM, KCLASS_OTHER, KCLASS_NAMES, WFMT_NATIVE, WFMT_FP8)
 
 __all__ = ["DenoiseLoop", "Gr00tError", "validate_geometry", "load_library", "FAMILY_EXPERT",
            "FAMILY_DIT", "DTYPE_FP32", "DTYPE_BF16", "MLP_GELU", "MLP_GEGLU"]
@@ -297,11 +297,31 @@ class DenoiseLoop:
         self._check(self._lib.gr00t_set_option(self._ctx, int(option), int(value)))
 
     def kernel_times(self, max_count: int = 1 << 16):
-        """Durations (ms) of the launches bracketed by OPT_TIME_KERNEL in the last denoise."""
+        """(durations in us, kernel classes) of every launch of the last denoise run with
+        OPT_TIME_KERNELS = 1, each launch charged its share of the launch chain."""
         buf = (ctypes.c_float * max_count)()
+        cls = (ctypes.c_int * max_count)()
         n = ctypes.c_int()
-        self._check(self._lib.gr00t_kernel_times(self._ctx, buf, max_count, ctypes.byref(n)))
-        return list(buf[:n.value])
+        self._check(self._lib.gr00t_kernel_times(self._ctx, buf, cls, max_count, ctypes.byref(n)))
+        return list(buf[:n.value]), list(cls[:n.value])
+
+    def sync(self):
+        """gr00t_sync: wait for the stream; raise Gr00tError(ETIMEOUT) if a bounded device wait gave up."""
+        self._check(self._lib.gr00t_sync(self._ctx))
+
+    def debug_dump(self, k: int, x_in, layer: int, h_out=None):
+        """gr00t_debug_dump: residual stream [B, tokens, hidden] (fp32) after block ``layer``
+        (-1: after the input projection) of velocity evaluation k from ``x_in``."""
+        torch = _torch()
+        x_in = self._chunk(x_in)
+        if h_out is None:
+            tok = int(self.geom["horizon"]) + int(self.geom.get("state_tokens", 0))
+            h_out = torch.empty((x_in.shape[0], tok, int(self.geom["hidden"])), dtype=torch.float32,
+                                device=x_in.device)
+        if not (h_out.is_cuda and h_out.dtype == torch.float32 and h_out.is_contiguous()):
+            raise ValueError("h_out must be a contiguous CUDA float32 tensor")
+        self._check(self._lib.gr00t_debug_dump(self._ctx, int(k), _ptr(x_in), int(layer), _ptr(h_out)))
+        return h_out
 
     def info(self, what: int) -> int:
         v = ctypes.c_int64()

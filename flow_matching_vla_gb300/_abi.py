@@ -14,18 +14,22 @@ ROOT = os.path.dirname(PKG)
 HEADER = os.path.join(ROOT, "include", "gr00t.h")
 LIB_PATH = os.path.join(PKG, "libgr00t.so")
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 WFMT_NATIVE, WFMT_FP8 = 0, 1
 OK, EINVAL, ENOMEM, ECUDA, ESTATE, EUNSUPPORTED, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 FAMILY_EXPERT, FAMILY_DIT = 0, 1
 DTYPE_FP32, DTYPE_BF16 = 0, 1
 MLP_GELU, MLP_GEGLU = 0, 1
 MEM_HOST, MEM_DEVICE = 0, 1
-OPT_USE_GRAPH, OPT_GEMM_PATH, OPT_WAIT_LIMIT, OPT_ATTN_PATH, OPT_TIME_KERNEL = 1, 2, 3, 4, 5
+OPT_USE_GRAPH, OPT_GEMM_PATH, OPT_WAIT_LIMIT, OPT_ATTN_PATH, OPT_TIME_KERNELS = 1, 2, 3, 4, 5
 OPT_SPLIT_CAP, OPT_RESID_SPLIT_CAP, OPT_PERSISTENT_GEMM, OPT_L2_PREFETCH = 6, 7, 8, 9
 OPT_ATTN_SPLIT_CAP = 11
+OPT_TEST_STALL = 12
 OPT_NOALLOC_LIMIT = 10
 KCLASS_QKV_GEMM, KCLASS_ATTENTION, KCLASS_O_GEMM, KCLASS_UP_GEMM, KCLASS_DOWN_GEMM, KCLASS_NORM = 1, 2, 3, 4, 5, 6
+KCLASS_OTHER = 7
+KCLASS_NAMES = {1: "qkv_gemm", 2: "attention", 3: "o_gemm", 4: "up_gemm", 5: "down_gemm", 6: "norm",
+                7: "other"}
 INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES, INFO_DEVICE_BYTES, INFO_ERROR_FLAG = 1, 2, 3, 4
 
 STATUS_NAMES = {OK: "OK", EINVAL: "EINVAL", ENOMEM: "ENOMEM", ECUDA: "ECUDA", ESTATE: "ESTATE",
@@ -70,8 +74,10 @@ SIGNATURES = {
     "gr00t_last_error": (ctypes.c_char_p, [_VP]),
     "gr00t_set_option": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int64]),
     "gr00t_get_info": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]),
-    "gr00t_kernel_times": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_float), ctypes.c_int,
-                                          ctypes.POINTER(ctypes.c_int)]),
+    "gr00t_kernel_times": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int),
+                                          ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
+    "gr00t_sync": (ctypes.c_int, [_VP]),
+    "gr00t_debug_dump": (ctypes.c_int, [_VP, ctypes.c_int, _VP, ctypes.c_int, _VP]),
 }
 
 _lib = None

@@ -68,6 +68,7 @@ __global__ void __launch_bounds__(64) attn_dit_kernel(AttnArgs a) {
   const bf16* Vp = a.v_slot >= 0 ? (const bf16*)a.table[a.v_slot] : nullptr;
   const uint8_t* mask = a.mask_slot >= 0 ? (const uint8_t*)a.table[a.mask_slot] : nullptr;
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(a.ts);
 
   // queries: rows t < Tq of (b, head)
   for (int i = tid; i < QROWS * CH; i += 64) {

@@ -25,6 +25,7 @@ template <typename T>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   ptx::pdl_launch_dependents();
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(a.ts);
   const int lane = threadIdx.x & 31;
   const long long w = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
   const long long total = (long long)a.B * a.Tq * a.Hq;

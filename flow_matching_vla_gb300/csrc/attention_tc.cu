@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(128) attn_fold_kernel(AttnFoldArgs a) {
   const int first = nsub < RING ? nsub : RING;
   for (int i = 0; i < first; ++i) issue_kv(k_begin + i * KT, 0, i);
   ptx::pdl_wait();
+  if (tid == 0) kstamp(a.ts);
 
   // Q tile: folded row r = t * Hq + h -> qkv[(b*H + t) * ldq + h * DH]
   for (int i = tid; i < ROWS * CH; i += 128) {

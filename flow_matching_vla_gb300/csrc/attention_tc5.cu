@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!key_tile(t_begin + pre, b, a.P, a.H).prefix) break;
       for (int i = 0; i < pre; ++i) load(i, i);
       ptx::pdl_wait();
+      if (is_k) kstamp(a.ts);
       if (is_k) {
         ptx::mbar_arrive_expect_tx(q_full, L::Q_BYTES);
         const int tokens_per_tile = ROWS / a.Hq;
@@ -518,6 +519,7 @@ __global__ void __launch_bounds__(256) attn_t5_combine_kernel(AttnT5Args a, int 
   const int tiles_x = (nrows + ROWS - 1) / ROWS;
   const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);   // b * nrows + gr
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(a.ts2);
   if (gw >= (long long)a.B * nrows) return;
   const int b = (int)(gw / nrows), gr = (int)(gw % nrows);
   const long long tiles = (long long)tiles_x * a.B;

@@ -77,4 +77,17 @@ template <typename T> __device__ __forceinline__ float gelu_act(float x);
 template <> __device__ __forceinline__ float gelu_act<float>(float x) { return gelu_tanhf(x); }
 template <> __device__ __forceinline__ float gelu_act<bf16>(float x) { return gelu_tanh_fast(x); }
 
+// Dependency-release stamp for timing a launch inside the step's chain: the
+// global timer (ns) at the moment this grid's programmatic dependency wait
+// returned, i.e. when the previous kernel of the stream had completed.  One
+// store by the calling thread of the first CTA; ``ts`` null (the default):
+// nothing.  Call it from one thread, right after griddepcontrol.wait.
+__device__ __forceinline__ void kstamp(unsigned long long* ts) {
+  if (ts != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    *ts = t;
+  }
+}
+
 }  // namespace g3

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const T* __restrict__ A,
                                                         int N, int K, Epi e) {
   ptx::pdl_launch_dependents();
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(e.ts);
   __shared__ float As[BK][BM + 4];
   __shared__ float Ws[BK][BN + 4];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;

@@ -510,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every thread but the producer (which waited before its activation loads)
   // waits for the previous kernel before touching activation memory
   if (TA || threadIdx.x != 0) ptx::pdl_wait();
+  if (threadIdx.x == 96) kstamp(e.ts);   // warp 3 has no main-loop role on either weight path
 
   if (!ptx::mbar_wait(done, 0, wait_limit)) {
     atomicExch(abort_flag, 1);
@@ -784,6 +785,7 @@ __global__ void __launch_bounds__(kPersThreads, 1)
     }
   } else {
     ptx::pdl_wait();
+    if (threadIdx.x == 64) kstamp(e.ts);
     const int ew = warp - 2;
     const int quad = warp & 3;
     const int c_begin = (ew >> 2) * (BN / 2), c_end = c_begin + BN / 2;

@@ -44,6 +44,8 @@ struct Epi {
   // E4M3 weights: fp32 scale of weight row n (output column n); the tensor-core
   // E4M3 GEMM multiplies each accumulator row by it before the epilogue
   const float* wscale = nullptr;
+  // dependency-release stamp of this launch (nullable; see kstamp in common.cuh)
+  unsigned long long* ts = nullptr;
 };
 
 struct GemmArgs {
@@ -77,6 +79,7 @@ struct NormArgs {
   long long mod_bstride = 0;
   int scale_off = 0, shift_off = 0;   // offsets of scale and shift inside the row
   int tok = 1;                   // token rows per sample
+  unsigned long long* ts = nullptr;   // dependency-release stamp (nullable)
 };
 
 // out[m] = norm(h[m]) * (1 + scale) + shift for m < M (mod == nullptr: plain norm)
@@ -98,7 +101,7 @@ cudaError_t out_euler(DType dt, float* h, int D, int M, int H, int ro, const voi
 // state tokens copied into the residual rows (b * tok + j, j < ns) from state [B][ns][D].
 cudaError_t dit_in(DType dt, const float* x, int A, const void* w1, const float* b1, void* a_out,
                    int D, int M, const float* state, int ns, int tok, int B, float* h,
-                   cudaStream_t s, bool pdl);
+                   cudaStream_t s, bool pdl, unsigned long long* ts = nullptr);
 
 // ---- attention ----------------------------------------------------------------
 struct AttnArgs {
@@ -114,6 +117,7 @@ struct AttnArgs {
   int S = 0;                // suffix keys per sample
   void* out = nullptr;      // output of (b, t, head): out + (b*Tq + t)*ldo + head*Dh
   int ldo = 0;
+  unsigned long long* ts = nullptr;   // dependency-release stamp (nullable)
 };
 cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s, bool pdl);
 
@@ -132,6 +136,7 @@ struct AttnFoldArgs {
   int ldo = 0;
   float* ws = nullptr;         // split partials (L2-resident scratch)
   long long ws_floats = 0;
+  unsigned long long* ts = nullptr;   // dependency-release stamp (nullable)
 };
 bool attn_fold_supported(int Dh);
 long long attn_fold_workspace_floats(const AttnFoldArgs& a, int S);
@@ -153,6 +158,8 @@ struct AttnT5Args {
   void* pool_k = nullptr;     // a bound pool's K and V planes: this step's suffix K/V go to
   void* pool_v = nullptr;     // rows [P, P + H) of each sample's slot (nullptr: no pool)
   int pool_cap = 0;
+  unsigned long long* ts = nullptr;    // dependency-release stamp of the main kernel (nullable)
+  unsigned long long* ts2 = nullptr;   // ... and of the split merge (nullable)
 };
 }  // namespace g3
 #include <cuda.h>
@@ -179,5 +186,12 @@ cudaError_t permute_rows(const void* src, void* dst, int rows, int row_bytes, in
 cudaError_t permute_floats(const float* src, float* dst, int rows, int mode, int p0, int p1, cudaStream_t s);
 // dst[i] = float(src[i]) for a DType source
 cudaError_t to_f32(DType dt, const void* src, float* dst, long long n, cudaStream_t s);
+
+// One thread waits up to ``limit`` polls for *never to become nonzero; when the
+// limit passes it sets *err = 1 and returns (the bounded-wait error path).
+cudaError_t bounded_wait_probe(const int* never, int* err, long long limit, cudaStream_t s);
+// A one-thread kernel that writes its dependency-release stamp into *ts: placed
+// after the loop's last launch, it closes that launch's interval.
+cudaError_t stamp_tail(unsigned long long* ts, cudaStream_t s, bool pdl);
 
 }  // namespace g3

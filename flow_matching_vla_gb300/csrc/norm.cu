@@ -95,6 +95,7 @@ template <typename T>
 __global__ void adanorm_kernel(float* __restrict__ h, int D, T* __restrict__ out, NormArgs na) {
   ptx::pdl_launch_dependents();
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(na.ts);
   extern __shared__ float sm[];
   float* row = sm;
   float* red = sm + D;
@@ -111,6 +112,7 @@ __global__ void expert_in_kernel(const float* __restrict__ x, int A, const T* __
                                  T* __restrict__ out, NormArgs na) {
   ptx::pdl_launch_dependents();
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(na.ts);
   extern __shared__ float sm[];
   float* row = sm;
   float* red = sm + D;
@@ -140,6 +142,7 @@ __global__ void out_euler_kernel(float* __restrict__ h, int D, int H, int ro, in
                                  float* __restrict__ v_out) {
   ptx::pdl_launch_dependents();
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(na.ts);
   extern __shared__ float sm[];
   float* row = sm;
   float* red = sm + D;
@@ -166,9 +169,10 @@ template <typename T>
 __global__ void dit_in_kernel(const float* __restrict__ x, int A, const T* __restrict__ w1,
                               const float* __restrict__ b1, T* __restrict__ a_out, int D, int M,
                               const float* __restrict__ state, int ns, int tok,
-                              float* __restrict__ h) {
+                              float* __restrict__ h, unsigned long long* ts) {
   ptx::pdl_launch_dependents();
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(ts);
   extern __shared__ float xs[];
   const int blk = blockIdx.x;
   if (blk >= M) {  // state-token rows: copy the bound embedding into the residual stream
@@ -356,6 +360,7 @@ __global__ void __launch_bounds__(32 * kNormRowsPerCta) adanorm_rows_kernel(floa
   typename RawQuad<T>::type sc[NQ], sh[NQ];
   if (m < M) warp_load_mod<T, NQ>(na, m, nq, lane, sc, sh);
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(na.ts);
   if (m >= M) return;
   float4 x[NQ];
   warp_load_residual<T, NS, NQ>(h, m, nq, lane, na, x, D, true);
@@ -386,6 +391,7 @@ __global__ void __launch_bounds__(512) adanorm_cta_kernel(float* __restrict__ h,
   }
   if (na.part && na.gate) gq = RQ::load((const T*)na.gate + mrow + i);
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(na.ts);
   float* hr = h + (long long)m * D + i;
   float4 x = ld4(hr);
   if (na.part) {
@@ -464,6 +470,7 @@ __global__ void __launch_bounds__(256) expert_in_rows_kernel(const float* __rest
       sh[r] = RQ::load(mod + na.shift_off + f0);
     }
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(na.ts);
   for (int i = t; i < kInRows * A; i += blockDim.x) {
     const int r = i / A, a = i % A;
     xs[r][a] = m0 + r < M ? x[(long long)(m0 + r) * A + a] : 0.f;
@@ -551,6 +558,7 @@ __global__ void __launch_bounds__(32 * kNormRowsPerCta) out_euler_rows_kernel(
   typename RawQuad<T>::type sc[NQ], sh[NQ];
   if (m < M) warp_load_mod<T, NQ>(na, row, nq, lane, sc, sh);
   ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(na.ts);
   if (m >= M) return;
   float4 y[NQ];
   warp_load_residual<T, NS, NQ>(h, row, nq, lane, na, y, D, false);
@@ -687,15 +695,15 @@ cudaError_t out_euler(DType dt, float* h, int D, int M, int H, int ro, const voi
 
 cudaError_t dit_in(DType dt, const float* x, int A, const void* w1, const float* b1, void* a_out,
                    int D, int M, const float* state, int ns, int tok, int B, float* h,
-                   cudaStream_t s, bool pdl) {
+                   cudaStream_t s, bool pdl, unsigned long long* ts) {
   const int blocks = M + (state ? B * ns : 0);
   if (blocks <= 0) return cudaSuccess;
   const size_t smem = A * sizeof(float);
   if (dt == DT_F32)
     return launch_k(dit_in_kernel<float>, blocks, threads_for(D), smem, s, pdl, x, A, (const float*)w1, b1,
-                    (float*)a_out, D, M, state, ns, tok, h);
+                    (float*)a_out, D, M, state, ns, tok, h, ts);
   return launch_k(dit_in_kernel<bf16>, blocks, threads_for(D), smem, s, pdl, x, A, (const bf16*)w1, b1,
-                  (bf16*)a_out, D, M, state, ns, tok, h);
+                  (bf16*)a_out, D, M, state, ns, tok, h, ts);
 }
 
 }  // namespace g3

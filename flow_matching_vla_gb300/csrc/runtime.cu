@@ -21,6 +21,10 @@
 
 // Size (fp32 elements) of the fixed scratch array of the allocation-free step.
 #define G3_NOALLOC_SCRATCH_FLOATS (3 << 20)
+// Descriptor slots the allocation-free step uses instead of the descriptor cache
+// (a launch takes at most this many descriptors from tmap(); they are copied into
+// the kernel parameters at launch).
+constexpr int kSpillMaps = 4;
 
 using namespace g3;
 
@@ -105,16 +109,34 @@ struct gr00t_ctx {
     const void* gate = nullptr;
   } pending;
 
-  // per-kernel timing: event pairs around every launch of one kernel class
-  int time_class = 0;
-  std::vector<cudaEvent_t> tev;
-  int tev_used = 0;
-  bool capturing = false;
+  // launch stamps (GR00T_OPT_TIME_KERNELS): one device slot per launch of the loop
+  int stamp_on = 0;
+  unsigned long long* stamps = nullptr;
+  int stamp_cap = 0, stamp_used = 0;
+  bool in_loop = false;         // stamps are taken by the launches of the whole loop only
+  std::vector<int> stamp_cls;   // kernel class of each stamped launch
+
+  // the allocation-free step: its fixed scratch array (device address looked up at
+  // create) and descriptor slots that stand in for the descriptor cache
+  float* noalloc_addr = nullptr;
+  bool no_host_alloc = false;
+  CUtensorMap tmap_spill[kSpillMaps];
+  unsigned tmap_spill_next = 0;
+
+  // test hooks: a bounded wait on a word nothing writes (GR00T_OPT_TEST_STALL);
+  // the residual stream of one block copied out (gr00t_debug_dump)
+  int opt_stall = 0;           // polls of the probe's bounded wait (0: no probe)
+  int* never_set = nullptr;
+  int* err_host = nullptr;   // page-locked copy of the device error word (synchronous calls)
+  float* dump_out = nullptr;
+  int dump_layer = -2;
 };
 
 namespace {
 
 thread_local std::string g_create_err;
+
+cudaError_t noalloc_scratch(int dev, float** out);
 
 int set_err(gr00t_ctx* c, int code, const char* fmt, ...) {
   char buf[512];
@@ -300,6 +322,7 @@ void plan_buffers(gr00t_ctx* c, Plan& pl) {
   c->gemm_ws_floats = (long long)(c->sm_count + c->sm_count / 16 + 1) * 256 * 128;
   pl.add((void**)&c->gemm_ws, (size_t)c->gemm_ws_floats * 4);
   pl.add((void**)&c->err_flag, 64);
+  pl.add((void**)&c->never_set, 64);
 }
 
 // Copy one weight matrix [rows][cols] into library memory, re-laid-out by ``mode``.
@@ -457,15 +480,14 @@ int upload_weights(gr00t_ctx* c, const gr00t_weights* w) {
 
 // ---- the step ------------------------------------------------------------------
 
-// Timing brackets: with GR00T_OPT_TIME_KERNEL set to a class, every launch of
-// that class sits between two events (event-record nodes when captured).
-void tmark(gr00t_ctx* c, int cls) {
-  if (!c->time_class || cls != c->time_class || c->tev_used >= (int)c->tev.size()) return;
-  cudaEvent_t ev = c->tev[c->tev_used++];
-  if (c->capturing)
-    cudaEventRecordWithFlags(ev, c->stream, cudaEventRecordExternal);
-  else
-    cudaEventRecord(ev, c->stream);
+// Launch stamps: with GR00T_OPT_TIME_KERNELS set, every kernel launch of the
+// loop gets its own slot of a device array into which it writes the global
+// timer when its dependency wait returns (kstamp); consecutive stamps bound
+// each launch's share of the chain without changing the launches themselves.
+unsigned long long* next_ts(gr00t_ctx* c, int cls) {
+  if (!c->stamp_on || !c->in_loop || !c->stamps || c->stamp_used >= c->stamp_cap) return nullptr;
+  c->stamp_cls.push_back(cls);
+  return c->stamps + c->stamp_used++;
 }
 
 const CUtensorMap* tmap(gr00t_ctx* c, const void* ptr, long long rows, long long cols, long long ld,
@@ -478,6 +500,13 @@ const CUtensorMap* tmap(gr00t_ctx* c, const void* ptr, long long rows, long long
   const cudaError_t e = box_rows < 0 ? tc_make_map_e4m3(&m, ptr, rows, cols, ld)
                                      : tc_make_map(&m, ptr, rows, cols, ld, box_rows);
   if (e != cudaSuccess) return nullptr;
+  if (c->no_host_alloc) {
+    // the allocation-free step adds nothing to the cache: the descriptor goes to
+    // a fixed slot of the context (kernels take descriptors by value at launch)
+    CUtensorMap* slot = &c->tmap_spill[c->tmap_spill_next++ % kSpillMaps];
+    *slot = m;
+    return slot;
+  }
   return &c->tmaps.emplace(key, m).first->second;
 }
 
@@ -496,9 +525,9 @@ bool tc_ok(gr00t_ctx* c, int M, int N, int K, bool e4m3) {
 }
 bool tc_ok(gr00t_ctx* c, const GemmArgs& a) { return tc_ok(c, a.M, a.N, a.K, a.epi.wscale != nullptr); }
 
-int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
+int gemm(gr00t_ctx* c, GemmArgs a, int cls = GR00T_KCLASS_OTHER) {
   ++c->launches;
-  tmark(c, cls);
+  a.epi.ts = next_ts(c, cls);
   if (a.epi.wscale) {   // E4M3 weights: the tensor-core path is the only one
     if (!tc_ok(c, a))
       return set_err(c, GR00T_EUNSUPPORTED, "FP8 weights need the tensor-core GEMM (GEMM path 0, K %% 128 == 0)");
@@ -508,7 +537,6 @@ int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
     if (!tw || !tx) return set_err(c, GR00T_ECUDA, "TMA descriptor encode failed (alignment?)");
     CK(c, gemm_tc_e4m3(*tw, *tx, a, p, c->gemm_ws, c->gemm_ws_floats, c->err_flag, c->wait_limit, c->stream,
                        c->opt_pdl != 0));
-    tmark(c, cls);
     return GR00T_OK;
   }
   if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
@@ -526,7 +554,6 @@ int gemm(gr00t_ctx* c, const GemmArgs& a, int cls = 0) {
   } else {
     CK(c, gemm_simt(c->dt, a, c->stream, c->opt_pdl != 0));
   }
-  tmark(c, cls);
   return GR00T_OK;
 }
 
@@ -546,7 +573,9 @@ int gemm_resid(gr00t_ctx* c, GemmArgs a, int cls) {
       a.epi.ldo = a.N;
     }
   }
-  return gemm(c, a, cls);
+  const int rc = gemm(c, a, cls);
+  if (rc != GR00T_OK) c->pending = gr00t_ctx::Pending();   // nothing was enqueued to fold
+  return rc;
 }
 
 // Attach (and clear) pending partials to the next norm's arguments.
@@ -569,10 +598,29 @@ inline const char* ptr_at(const void* p, long long elems, size_t esz) {
   return (const char*)p + elems * (long long)esz;
 }
 
+// Test hook (GR00T_OPT_TEST_STALL): a bounded wait on a word nothing writes,
+// enqueued ahead of a step, so the bounded-wait error path can be exercised
+// without any copy or tensor-core operation in flight.
+int stall_probe(gr00t_ctx* c) {
+  if (!c->opt_stall) return GR00T_OK;
+  ++c->launches;
+  CK(c, bounded_wait_probe(c->never_set, c->err_flag, c->opt_stall, c->stream));
+  return GR00T_OK;
+}
+
+// Residual stream after block ``layer`` into the dump target (gr00t_debug_dump).
+int dump_h(gr00t_ctx* c, int layer) {
+  if (!c->dump_out || layer != c->dump_layer) return GR00T_OK;
+  CK(c, cudaMemcpyAsync(c->dump_out, c->h, (size_t)c->bB * c->tok * c->D * sizeof(float),
+                        cudaMemcpyDeviceToDevice, c->stream));
+  return GR00T_OK;
+}
+
 // Enqueue one denoise step k on the stream: x (fp32 [B][H][A]) in; v_out
 // (nullable) receives the velocity; with do_euler x += dt_k * v.
 int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   c->launches = 0;
+  c->pending = gr00t_ctx::Pending();   // partials of an earlier, failed enqueue are not this step's
   const int B = c->bB, P = c->bP, D = c->D, L = c->L, H = c->H, tok = c->tok;
   const int M = B * tok, MA = B * H, R = c->R;
   const long long bstride = (long long)c->S * R;
@@ -580,17 +628,24 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   const char* mod_k = ptr_at(c->mod, (long long)k * B * bstride, es);
   const bool dit = c->g.family == GR00T_FAMILY_DIT;
   cudaStream_t s = c->stream;
+  RC(stall_probe(c));
 
   auto site = [&](int si) { return (const void*)(mod_k + (long long)si * R * es); };
   // Kernels read the modulation table before their programmatic-launch wait.
   // The table is written when the schedule is set, so the head of step 0 is
   // launched without the early-launch attribute: it (and so every later
   // kernel) starts only once that write has completed.
-  const bool pdl_head = c->opt_pdl != 0 && k > 0;
+  const bool pdl_head = c->opt_pdl != 0 && k > 0 && !c->opt_stall;
   NormArgs base;
   base.eps = c->g.norm_eps;
   base.mod_bstride = bstride;
   base.tok = tok;
+  auto norm = [&](NormArgs na) -> int {
+    ++c->launches;
+    na.ts = next_ts(c, GR00T_KCLASS_NORM);
+    CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, na), s, c->opt_pdl != 0));
+    return GR00T_OK;
+  };
 
   if (!dit) {
     NormArgs na = base;
@@ -599,9 +654,12 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     na.scale_off = 0;
     na.shift_off = D;
     ++c->launches;
-    tmark(c, GR00T_KCLASS_NORM);
-    CK(c, expert_in(c->dt, x, c->A, c->w_in, c->b_in, c->h, D, M, c->n, na, s, pdl_head));
-    tmark(c, GR00T_KCLASS_NORM);
+    {
+      NormArgs nh = na;
+      nh.ts = next_ts(c, GR00T_KCLASS_NORM);
+      CK(c, expert_in(c->dt, x, c->A, c->w_in, c->b_in, c->h, D, M, c->n, nh, s, pdl_head));
+    }
+    RC(dump_h(c, -1));
     const int nq = c->nqkv[0];
     for (int l = 0; l < L; ++l) {
       GemmArgs g;
@@ -610,11 +668,13 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       g.epi.kind = EPI_ROPE; g.epi.out = c->qkv; g.epi.ldo = nq;
       g.epi.rope_cols = (c->Hq + 1) * c->Dh; g.epi.hd = c->Dh; g.epi.rope_tab = c->rope_tab;
       g.epi.tok_rope = tok;
-      if (c->opt_l2_ahead) {  // pull the next layer's weights and prefix K/V into L2 meanwhile
+      if (c->opt_l2_ahead) {  // pull the next layer's weights (and flat prefix K/V) into L2 meanwhile
         const int ln = (l + 1) % L;
         g.l2[0].p = c->w_qkv[ln];
         g.l2[0].bytes = ((const char*)c->w_down[ln] + (size_t)D * c->F * es) - (const char*)c->w_qkv[ln];
-        if (P > 0) {
+        // a bound pool keeps samples ``capacity`` rows apart: a contiguous range would
+        // prefetch mostly other rows, so only flat prefix K/V is prefetched
+        if (P > 0 && c->pool.empty()) {
           g.l2[1].p = c->host_table[2 * ln];
           g.l2[1].bytes = (long long)B * P * c->Dh * es;
           g.l2[2].p = c->host_table[2 * ln + 1];
@@ -624,7 +684,6 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       RC(gemm(c, g, GR00T_KCLASS_QKV_GEMM));
 
       ++c->launches;
-      tmark(c, GR00T_KCLASS_ATTENTION);
       // bf16: the tcgen05 kernel (key splits merged by a second kernel when the
       // row tiles alone do not fill the GPU); the mma.sync and CUDA-core
       // kernels remain selectable
@@ -644,7 +703,11 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         }
         CUtensorMap maps[8];
         CK(c, attn_t5_maps(a5, c->host_table[2 * l], c->host_table[2 * l + 1], splits, maps));
-        if (splits > 1) ++c->launches;   // the split merge is a second kernel
+        a5.ts = next_ts(c, GR00T_KCLASS_ATTENTION);
+        if (splits > 1) {   // the split merge is a second kernel
+          ++c->launches;
+          a5.ts2 = next_ts(c, GR00T_KCLASS_ATTENTION);
+        }
         CK(c, attention_t5(a5, maps, splits, s, c->opt_pdl != 0));
       } else if (!c->pool.empty()) {
         return set_err(c, GR00T_EUNSUPPORTED, "a bound K/V pool needs the tcgen05 attention (bf16, attention path 0 or 3)");
@@ -655,6 +718,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         af.table = c->table; af.k_slot = 2 * l; af.v_slot = 2 * l + 1;
         af.out = c->att; af.ldo = c->qd;
         af.ws = c->gemm_ws; af.ws_floats = c->gemm_ws_floats;   // kernels run in order: one scratch
+        af.ts = next_ts(c, GR00T_KCLASS_ATTENTION);
         CK(c, attention_fold(af, attn_fold_splits(af, c->sm_count), s, c->opt_pdl != 0));
       } else {
         AttnArgs at;
@@ -662,9 +726,9 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         at.table = c->table; at.k_slot = 2 * l; at.v_slot = 2 * l + 1; at.P = P;
         at.ks = ptr_at(c->qkv, (long long)c->qd, es); at.vs = ptr_at(c->qkv, (long long)c->qd + c->Dh, es);
         at.lds = nq; at.S = tok; at.out = c->att; at.ldo = c->qd;
+        at.ts = next_ts(c, GR00T_KCLASS_ATTENTION);
         CK(c, attention_simt(c->dt, at, s, c->opt_pdl != 0));
       }
-      tmark(c, GR00T_KCLASS_ATTENTION);
 
       GemmArgs go;
       go.A = c->att; go.lda = c->qd; go.W = c->w_o[l]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
@@ -675,10 +739,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
 
       NormArgs n2 = na;
       n2.mod = site(2 * l + 1);
-      ++c->launches;
-      tmark(c, GR00T_KCLASS_NORM);
-      CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, n2), s, c->opt_pdl != 0));
-      tmark(c, GR00T_KCLASS_NORM);
+      RC(norm(n2));
 
       GemmArgs gu;
       gu.A = c->n; gu.lda = D; gu.W = c->w_up[l]; gu.ldw = D; gu.M = M; gu.K = D;
@@ -701,30 +762,32 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       if (l + 1 < L) {
         NormArgs n3 = na;
         n3.mod = site(2 * l + 2);
-        ++c->launches;
-        tmark(c, GR00T_KCLASS_NORM);
-        CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, n3), s, c->opt_pdl != 0));
-        tmark(c, GR00T_KCLASS_NORM);
+        RC(norm(n3));   // folds this layer's down partials into h
+        RC(dump_h(c, l));
       }
     }
     NormArgs nf = na;
     nf.mod = site(2 * L);
+    if (c->dump_out && c->dump_layer == L - 1) {
+      // dump of the last layer: fold its partials into h first (the step tail folds
+      // them without writing h back)
+      NormArgs nd = na;
+      nd.mod = nullptr;
+      RC(norm(nd));
+      RC(dump_h(c, L - 1));
+    }
     ++c->launches;
-    tmark(c, GR00T_KCLASS_NORM);
+    nf.ts = next_ts(c, GR00T_KCLASS_NORM);
     CK(c, out_euler(c->dt, c->h, D, MA, H, 0, c->w_out, c->b_out, c->A, take_pending(c, nf), x, c->dts, k,
-                    do_euler,
-                    v_out, s, c->opt_pdl != 0));
-    tmark(c, GR00T_KCLASS_NORM);
+                    do_euler, v_out, s, c->opt_pdl != 0));
     return GR00T_OK;
   }
 
   // ---- DiT family ----
   const int E = c->E, Ns = c->Ns;
   ++c->launches;
-  tmark(c, GR00T_KCLASS_NORM);
   CK(c, dit_in(c->dt, x, c->A, c->w_enc1, c->b_enc1, c->a_enc, D, MA, (const float*)c->host_table[2 * L + 2],
-               Ns, tok, B, c->h, s, pdl_head));
-  tmark(c, GR00T_KCLASS_NORM);
+               Ns, tok, B, c->h, s, pdl_head, next_ts(c, GR00T_KCLASS_NORM)));
   {
     GemmArgs g;  // e = swish(a W2[:, :D]^T + atb_k), atb_k holds W2's time half and b2
     g.A = c->a_enc; g.lda = D; g.W = c->w_enc2; g.ldw = D + E; g.M = MA; g.N = D; g.K = D;
@@ -737,6 +800,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     g3a.epi.ldo = D; g3a.epi.rg = H; g3a.epi.rs = tok; g3a.epi.ro = Ns;
     RC(gemm(c, g3a));
   }
+  RC(dump_h(c, -1));
   NormArgs na = base;
   na.kind = NORM_LN;
   na.scale_off = 0;
@@ -744,10 +808,8 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   for (int i = 0; i < L; ++i) {
     NormArgs n1 = na;
     n1.mod = site(i);
-    ++c->launches;
-    tmark(c, GR00T_KCLASS_NORM);
-    CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, n1), s, c->opt_pdl != 0));
-    tmark(c, GR00T_KCLASS_NORM);
+    RC(norm(n1));   // folds block i-1's down partials into h
+    RC(dump_h(c, i - 1));
     const int nq = c->nqkv[i];
     GemmArgs g;
     g.A = c->n; g.lda = D; g.W = c->w_qkv[i]; g.ldw = D; g.M = M; g.N = nq; g.K = D;
@@ -767,12 +829,11 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       at.lds = nq; at.S = tok;
     }
     ++c->launches;
-    tmark(c, GR00T_KCLASS_ATTENTION);
+    at.ts = next_ts(c, GR00T_KCLASS_ATTENTION);
     if (c->dt == DT_BF16 && c->opt_attn == 0 && attn_dit_supported(at))
       CK(c, attention_dit(at, s, c->opt_pdl != 0));
     else
       CK(c, attention_simt(c->dt, at, s, c->opt_pdl != 0));
-    tmark(c, GR00T_KCLASS_ATTENTION);
     GemmArgs go;
     go.A = c->att; go.lda = c->qd; go.W = c->w_o[i]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
     go.epi.wscale = c->fp8w ? c->s_o[i] : nullptr;
@@ -780,10 +841,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     RC(gemm_resid(c, go, GR00T_KCLASS_O_GEMM));
     NormArgs n3 = na;
     n3.mod = nullptr;
-    ++c->launches;
-    tmark(c, GR00T_KCLASS_NORM);
-    CK(c, adanorm(c->dt, c->h, D, M, c->n, take_pending(c, n3), s, c->opt_pdl != 0));
-    tmark(c, GR00T_KCLASS_NORM);
+    RC(norm(n3));
     GemmArgs gu;
     gu.A = c->n; gu.lda = D; gu.W = c->w_up[i]; gu.ldw = D; gu.M = M; gu.N = c->F; gu.K = D;
     gu.epi.wscale = c->fp8w ? c->s_up[i] : nullptr;
@@ -799,13 +857,30 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   nf.mod = site(L);
   nf.scale_off = D;  // final row splits (shift, scale)
   nf.shift_off = 0;
+  if (c->dump_out && c->dump_layer == L - 1) {
+    NormArgs nd = na;
+    nd.mod = nullptr;
+    RC(norm(nd));
+    RC(dump_h(c, L - 1));
+  }
   ++c->launches;
-  tmark(c, GR00T_KCLASS_NORM);
+  nf.ts = next_ts(c, GR00T_KCLASS_NORM);
   CK(c, out_euler(c->dt, c->h, D, MA, H, Ns, c->w_out, c->b_out, c->A, take_pending(c, nf), x, c->dts, k,
-                  do_euler,
-                  v_out, s, c->opt_pdl != 0));
-  tmark(c, GR00T_KCLASS_NORM);
+                  do_euler, v_out, s, c->opt_pdl != 0));
   return GR00T_OK;
+}
+
+// Enqueue the T steps of the loop (the tail stamp closes the last launch's interval).
+int enqueue_loop(gr00t_ctx* c) {
+  c->stamp_used = 0;
+  c->stamp_cls.clear();
+  c->in_loop = true;
+  int rc = GR00T_OK;
+  for (int k = 0; k < c->sT && rc == GR00T_OK; ++k) rc = enqueue_step(c, k, c->x, nullptr, 1);
+  unsigned long long* ts = rc == GR00T_OK ? next_ts(c, 0) : nullptr;
+  c->in_loop = false;
+  if (ts) CK(c, stamp_tail(ts, c->stream, c->opt_pdl != 0));
+  return rc;
 }
 
 int ensure_graph(gr00t_ctx* c) {
@@ -816,11 +891,7 @@ int ensure_graph(gr00t_ctx* c) {
   }
   cudaGraph_t graph = nullptr;
   CK(c, cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-  c->capturing = true;
-  c->tev_used = 0;
-  int rc = GR00T_OK;
-  for (int k = 0; k < c->sT && rc == GR00T_OK; ++k) rc = enqueue_step(c, k, c->x, nullptr, 1);
-  c->capturing = false;
+  const int rc = enqueue_loop(c);
   cudaError_t e = cudaStreamEndCapture(c->stream, &graph);
   if (rc != GR00T_OK) {
     if (graph) cudaGraphDestroy(graph);
@@ -852,8 +923,23 @@ int run_loop(gr00t_ctx* c) {
     RC(ensure_graph(c));
     CK(c, cudaGraphLaunch(c->gexec, c->stream));
   } else {
-    c->tev_used = 0;
-    for (int k = 0; k < c->sT; ++k) RC(enqueue_step(c, k, c->x, nullptr, 1));
+    RC(enqueue_loop(c));
+  }
+  return GR00T_OK;
+}
+
+// Synchronise the stream and turn a set device error word into GR00T_ETIMEOUT
+// (the word is cleared, so the context stays usable).
+int sync_and_check(gr00t_ctx* c) {
+  CK(c, cudaMemcpyAsync(c->err_host, c->err_flag, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+  CK(c, cudaStreamSynchronize(c->stream));
+  const int f = *(volatile int*)c->err_host;
+  if (f != 0) {
+    CK(c, cudaMemsetAsync(c->err_flag, 0, sizeof(int), c->stream));
+    CK(c, cudaStreamSynchronize(c->stream));
+    return set_err(c, GR00T_ETIMEOUT,
+                   "a bounded device wait gave up (error word %d): the results of the work enqueued since the "
+                   "last check are not valid", f);
   }
   return GR00T_OK;
 }
@@ -862,12 +948,12 @@ void free_ctx(gr00t_ctx* c) {
   if (!c) return;
   if (c->stream) cudaStreamSynchronize(c->stream);
   if (c->gexec) cudaGraphExecDestroy(c->gexec);
-  for (cudaEvent_t e : c->tev) cudaEventDestroy(e);
+  if (c->stamps) cudaFree(c->stamps);
+  if (c->err_host) cudaFreeHost(c->err_host);
   if (c->arena) cudaFree(c->arena);
   if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
   delete c;
 }
-
 }  // namespace
 
 // ---- exported ------------------------------------------------------------------
@@ -934,6 +1020,17 @@ extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, voi
     }
     c->own_stream = true;
   }
+  // the allocation-free step's fixed scratch array: the module holding it is loaded
+  // (and the array placed on the device) here, so that step itself never is the first
+  // to touch it
+  e = noalloc_scratch(dev, &c->noalloc_addr);
+  if (e == cudaSuccess) e = cudaMallocHost((void**)&c->err_host, 64);
+  if (e != cudaSuccess) {
+    set_err(nullptr, GR00T_ECUDA, "set-up failed: %s", cudaGetErrorString(e));
+    free_ctx(c);
+    return GR00T_ECUDA;
+  }
+  *c->err_host = 0;
   Plan pl;
   plan_buffers(c, pl);
   c->arena_bytes = pl.total();
@@ -952,6 +1049,7 @@ extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, voi
   rc = upload_weights(c, w);
   if (rc == GR00T_OK) {
     e = cudaMemsetAsync(c->err_flag, 0, 64, c->stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->never_set, 0, 64, c->stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(c->table, 0, (2 * c->L + 3) * sizeof(void*), c->stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
     if (e != cudaSuccess) rc = set_err(c, GR00T_ECUDA, "init failed: %s", cudaGetErrorString(e));
@@ -1133,8 +1231,7 @@ extern "C" int gr00t_denoise_host(gr00t_ctx* c, const float* x_noise_host, float
   CK(c, cudaMemcpyAsync(c->x, x_noise_host, bytes, cudaMemcpyHostToDevice, c->stream));
   RC(run_loop(c));
   CK(c, cudaMemcpyAsync(actions_host, c->x, bytes, cudaMemcpyDeviceToHost, c->stream));
-  CK(c, cudaStreamSynchronize(c->stream));
-  return GR00T_OK;
+  return sync_and_check(c);
 }
 
 extern "C" int gr00t_denoise_step(gr00t_ctx* c, int k, const float* x_in, float* v_out) {
@@ -1196,17 +1293,24 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
       if (value < 1 || value > 16 || (value & (value - 1))) return set_err(c, GR00T_EINVAL, "split cap: 1, 2, 4, 8 or 16");
       (option == GR00T_OPT_SPLIT_CAP ? c->split_cap : c->resid_split_cap) = (int)value;
       break;
-    case GR00T_OPT_TIME_KERNEL: {
-      if (value < 0 || value > GR00T_KCLASS_NORM) return set_err(c, GR00T_EINVAL, "unknown kernel class");
-      c->time_class = (int)value;
-      const size_t need = value ? (size_t)2 * c->g.max_steps * (2 * c->L + 4) : 0;
-      while (c->tev.size() < need) {
-        cudaEvent_t e;
-        CK(c, cudaEventCreate(&e));
-        c->tev.push_back(e);
+    case GR00T_OPT_TIME_KERNELS: {
+      if (value != 0 && value != 1) return set_err(c, GR00T_EINVAL, "launch stamps: 0 or 1");
+      c->stamp_on = (int)value;
+      // one slot per launch of a whole loop at max_steps, plus the tail stamp
+      const int need = value ? c->g.max_steps * (8 * c->L + 16) + 1 : 0;
+      if (need > c->stamp_cap) {
+        if (c->stamps) CK(c, cudaFree(c->stamps));
+        c->stamps = nullptr;
+        c->stamp_cap = 0;
+        CK(c, cudaMalloc((void**)&c->stamps, (size_t)need * sizeof(unsigned long long)));
+        c->stamp_cap = need;
       }
       break;
     }
+    case GR00T_OPT_TEST_STALL:
+      if (value < 0 || value > (1 << 24)) return set_err(c, GR00T_EINVAL, "test stall: 0 .. 2^24 polls");
+      c->opt_stall = (int)value;
+      break;
     default:
       return set_err(c, GR00T_EINVAL, "unknown option %d", option);
   }
@@ -1254,18 +1358,42 @@ extern "C" int gr00t_get_info(gr00t_ctx* c, int what, int64_t* value) {
   }
 }
 
-extern "C" int gr00t_kernel_times(gr00t_ctx* c, float* ms, int max, int* count) {
-  if (!c || !count || (max > 0 && !ms)) return GR00T_EINVAL;
+extern "C" int gr00t_kernel_times(gr00t_ctx* c, float* us, int* kclass, int max, int* count) {
+  if (!c || !count || (max > 0 && !us)) return GR00T_EINVAL;
+  *count = 0;
   CK(c, cudaStreamSynchronize(c->stream));
-  const int pairs = c->tev_used / 2;
-  int n = 0;
-  for (int i = 0; i < pairs && n < max; ++i) {
-    float t = 0.f;
-    CK(c, cudaEventElapsedTime(&t, c->tev[2 * i], c->tev[2 * i + 1]));
-    ms[n++] = t;
+  const int n = c->stamp_used;
+  if (!c->stamp_on || n < 2) return GR00T_OK;
+  std::vector<unsigned long long> t(n);
+  CK(c, cudaMemcpy(t.data(), c->stamps, (size_t)n * sizeof(unsigned long long), cudaMemcpyDeviceToHost));
+  int m = 0;
+  for (int i = 0; i + 1 < n && m < max; ++i, ++m) {
+    us[m] = (float)((double)(long long)(t[i + 1] - t[i]) * 1e-3);
+    if (kclass) kclass[m] = c->stamp_cls[i];
   }
-  *count = n;
+  *count = m;
   return GR00T_OK;
+}
+
+extern "C" int gr00t_sync(gr00t_ctx* c) {
+  if (!c) return GR00T_EINVAL;
+  return sync_and_check(c);
+}
+
+extern "C" int gr00t_debug_dump(gr00t_ctx* c, int k, const float* x_in, int layer, float* h_out) {
+  if (!c) return GR00T_EINVAL;
+  if (!x_in || !h_out) return set_err(c, GR00T_EINVAL, "x_in/h_out is NULL");
+  RC(check_ready(c));
+  if (k < 0 || k >= c->sT) return set_err(c, GR00T_EINVAL, "step %d outside [0, %d)", k, c->sT);
+  if (layer < -1 || layer >= c->L) return set_err(c, GR00T_EINVAL, "layer %d outside [-1, %d)", layer, c->L);
+  const size_t bytes = (size_t)c->bB * c->H * c->A * sizeof(float);
+  CK(c, cudaMemcpyAsync(c->xtmp, x_in, bytes, cudaMemcpyDeviceToDevice, c->stream));
+  c->dump_out = h_out;
+  c->dump_layer = layer;
+  const int rc = enqueue_step(c, k, c->xtmp, nullptr, 0);
+  c->dump_out = nullptr;
+  c->dump_layer = -2;
+  return rc;
 }
 
 // ---- allocation-free step ------------------------------------------------------
@@ -1359,16 +1487,20 @@ extern "C" int gr00t_denoise_step_noalloc(gr00t_ctx* c, int k, const float* x_in
                    "this step needs %lld floats of scratch at batch %d, prefix %d; the no-alloc bound is %lld of "
                    "the fixed array's %lld (use gr00t_denoise_step)", need, c->bB, c->bP, cap,
                    (long long)G3_NOALLOC_SCRATCH_FLOATS);
-  float* scratch = nullptr;
-  CK(c, noalloc_scratch(dev, &scratch));
+  // the array's device address was looked up by gr00t_create on this device
+  float* const scratch = c->noalloc_addr;
+  if (!scratch) return set_err(c, GR00T_ESTATE, "the fixed scratch array was not set up on this device");
   const size_t bytes = (size_t)c->bB * c->H * c->A * sizeof(float);
   CK(c, cudaMemcpyAsync(c->xtmp, x_in, bytes, cudaMemcpyDeviceToDevice, c->stream));
-  // same launch sequence as gr00t_denoise_step, scratch taken from the fixed array
+  // same launch sequence as gr00t_denoise_step, scratch taken from the fixed array and
+  // tensor-map descriptors from fixed slots of the context instead of its cache
   float* const own = c->gemm_ws;
   const long long own_floats = c->gemm_ws_floats;
   c->gemm_ws = scratch;
   c->gemm_ws_floats = cap;
+  c->no_host_alloc = true;
   const int rc = enqueue_step(c, k, c->xtmp, v_out, 0);
+  c->no_host_alloc = false;
   c->gemm_ws = own;
   c->gemm_ws_floats = own_floats;
   return rc;

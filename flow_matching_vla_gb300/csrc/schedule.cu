@@ -4,6 +4,8 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.cuh"
+#include "tc_ptx.cuh"
 
 namespace g3 {
 
@@ -116,6 +118,33 @@ cudaError_t to_f32(DType dt, const void* src, float* dst, long long n, cudaStrea
   else
     to_f32_kernel<bf16><<<blocks, 256, 0, s>>>((const bf16*)src, dst, n);
   return cudaGetLastError();
+}
+
+
+namespace {
+
+__global__ void bounded_wait_probe_kernel(const volatile int* never, int* err, long long limit) {
+  if (threadIdx.x != 0) return;
+  for (long long i = 0; i < limit; ++i)
+    if (*never != 0) return;
+  atomicExch(err, 1);
+}
+
+__global__ void stamp_tail_kernel(unsigned long long* ts) {
+  ptx::pdl_launch_dependents();
+  ptx::pdl_wait();
+  if (threadIdx.x == 0) kstamp(ts);
+}
+
+}  // namespace
+
+cudaError_t bounded_wait_probe(const int* never, int* err, long long limit, cudaStream_t s) {
+  bounded_wait_probe_kernel<<<1, 32, 0, s>>>(never, err, limit);
+  return cudaGetLastError();
+}
+
+cudaError_t stamp_tail(unsigned long long* ts, cudaStream_t s, bool pdl) {
+  return launch_k(stamp_tail_kernel, dim3(1), dim3(32), 0, s, pdl, ts);
 }
 
 }  // namespace g3

@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define GR00T_ABI_VERSION 2
+#define GR00T_ABI_VERSION 3
 
 /* ---- status codes ------------------------------------------------------ */
 #define GR00T_OK 0
@@ -297,24 +297,27 @@ int gr00t_denoise_host(gr00t_ctx* ctx, const float* x_noise_host, float* actions
 int gr00t_denoise_step(gr00t_ctx* ctx, int k, const float* x_in, float* v_out);
 
 /*
- * gr00t_denoise_step with no allocation of any kind and no use of the
- * context's scratch workspace.  (No counterpart in the source pages: this is
- * an interface addition of this library.)
+ * gr00t_denoise_step with no allocation and no use of the context's scratch
+ * workspace.  (No counterpart in the source pages: this is an interface
+ * addition of this library.)
  *
  * Who it is for: callers that are not allowed to allocate device memory at
  * the point where they run a step -- e.g. a controller that fixed its device
  * memory budget at start-up and treats any later allocation as an error, or a
  * host program that lends this library a context and forbids it from taking
  * memory of its own.  This call never calls cudaMalloc, cudaFree or any other
- * allocating routine; the scratch that the tensor-core GEMMs (split-K
- * partials) and the attention (per-split partials) need comes from a fixed
- * array compiled into the library: 12 MiB of fp32 (3 * 2^20 floats) in the device
- * image of every GPU that loads the library, held until the process exits.
+ * allocating routine (device or host): the scratch that the tensor-core GEMMs
+ * (split-K partials) and the attention (per-split partials) need comes from a
+ * fixed array compiled into the library -- 12 MiB of fp32 (3 * 2^20 floats) in
+ * the device image of every GPU that loads the library, held until the process
+ * exits -- and its TMA descriptors are encoded into fixed slots of the context
+ * rather than added to the context's descriptor cache.
  *
  * Same arguments, inputs, outputs and results as gr00t_denoise_step.
- * Set-up: the first call on a device looks up the array's device address
- * (with that device current -- it must be the context's device); make that
- * first call before any stream capture.  The call runs gr00t_denoise_step's
+ * Set-up: gr00t_create looks up the array's device address on the context's
+ * device (which loads the library's device code there and places the array),
+ * so this call only reads the cached address; it must run with the context's
+ * device current.  The call runs gr00t_denoise_step's
  * own launch sequence; a step whose scratch need in that sequence, at the
  * bound (batch, prefix), exceeds the array returns GR00T_EINVAL with the need
  * in gr00t_last_error, before anything is enqueued.  All calls in the process
@@ -339,8 +342,10 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
 #define GR00T_OPT_ATTN_PATH 4     /* expert family: 0 (default): tcgen05/TMEM kernel for bf16 (its key splits
                                      merged by a second kernel), else CUDA cores; 1: CUDA-core kernel;
                                      2: mma.sync head-folded kernel; 3: tcgen05/TMEM kernel */
-#define GR00T_OPT_TIME_KERNEL 5   /* bracket every launch of one kernel class with timing events
-                                     (GR00T_KCLASS_*, 0 = off); read with gr00t_kernel_times */
+#define GR00T_OPT_TIME_KERNELS 5  /* 1: every kernel launch of the loop records the global timer (ns)
+                                     when its dependency wait returns -- one store by one thread, the
+                                     launches and their programmatic-launch chain unchanged; read with
+                                     gr00t_kernel_times.  0 (default): off */
 #define GR00T_OPT_SPLIT_CAP 6     /* largest split-K factor of GEMMs that reduce in-kernel (1..16, power of 2; default 4) */
 #define GR00T_OPT_RESID_SPLIT_CAP 7 /* same for residual GEMMs whose partials the next kernel folds in (default 8) */
 #define GR00T_OPT_PERSISTENT_GEMM 8 /* 1 (default): persistent tensor-core GEMM for unsplit shapes with > 64 tokens */
@@ -352,6 +357,10 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
                                       limit is how the refusal is exercised */
 #define GR00T_OPT_ATTN_SPLIT_CAP 11 /* expert family, tcgen05 attention: at most this many key splits
                                        (1 .. 32; 0 = automatic: as many as fill the SMs, up to 32) */
+#define GR00T_OPT_TEST_STALL 12   /* test hook: > 0 enqueues ahead of every step a one-thread kernel
+                                     that waits this many polls for a device word nothing writes, then
+                                     sets the device error word -- the bounded-wait error path with no
+                                     copy or tensor-core operation in flight (0 = off, the default) */
 int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
 
 #define GR00T_INFO_KERNELS_PER_STEP 1   /* kernel launches of one denoise step            */
@@ -360,22 +369,50 @@ int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
 #define GR00T_INFO_ERROR_FLAG 4         /* device error word (bounded waits), 0 if clean  */
 int gr00t_get_info(gr00t_ctx* ctx, int what, int64_t* value);
 
-/* Kernel classes of one denoise step, for GR00T_OPT_TIME_KERNEL. */
+/* Kernel classes of one denoise step (gr00t_kernel_times). */
 #define GR00T_KCLASS_QKV_GEMM 1    /* fused Q/K/V projection (+ RoPE epilogue)          */
 #define GR00T_KCLASS_ATTENTION 2   /* attention over prefix ++ suffix K/V                */
 #define GR00T_KCLASS_O_GEMM 3      /* output projection + (gated) residual               */
 #define GR00T_KCLASS_UP_GEMM 4     /* MLP gate/up projection + GeGLU / GeLU              */
 #define GR00T_KCLASS_DOWN_GEMM 5   /* MLP down projection + (gated) residual             */
 #define GR00T_KCLASS_NORM 6        /* adaptive norms, step head and tail                 */
+#define GR00T_KCLASS_OTHER 7       /* DiT action-encoder GEMMs                           */
 
 /*
- * Durations in milliseconds of the launches bracketed under
- * GR00T_OPT_TIME_KERNEL during the most recent gr00t_denoise (CUDA events on
- * the context's stream, recorded inside the captured graph).  Writes at most
- * ``max`` values to ``ms`` and their number to ``*count``.  Synchronises the
- * stream.
+ * Per-launch durations of the most recent gr00t_denoise run with
+ * GR00T_OPT_TIME_KERNELS = 1, in launch order: us[i] = stamp[i + 1] - stamp[i]
+ * in microseconds, where stamp[i] is the global timer when launch i's
+ * dependency wait returned (the previous kernel had completed) and a
+ * one-thread tail kernel closes the last interval.  Each launch is thus
+ * charged its share of the programmatic-launch chain, including its release
+ * gap, and the durations of one loop add up to the loop's device time (less
+ * the first launch's start-up).  ``kclass`` (nullable) receives each launch's
+ * GR00T_KCLASS_*.  Writes at most ``max`` entries and their number to
+ * ``*count`` (0 when stamps are off).  Synchronises the stream.
  */
-int gr00t_kernel_times(gr00t_ctx* ctx, float* ms, int max, int* count);
+int gr00t_kernel_times(gr00t_ctx* ctx, float* us, int* kclass, int max, int* count);
+
+/*
+ * Synchronise the context's stream and report the outcome of the bounded
+ * device waits of everything enqueued since the last check: GR00T_ETIMEOUT
+ * when one gave up (the device error word was set; the outputs of that work
+ * are not valid), GR00T_OK otherwise.  The word is cleared, so the context
+ * stays usable.  gr00t_denoise_host performs the same check before it returns;
+ * the asynchronous calls cannot, so call this after them where the outcome
+ * matters.
+ */
+int gr00t_sync(gr00t_ctx* ctx);
+
+/*
+ * Test-only: one velocity evaluation at step k from ``x_in`` (as
+ * gr00t_denoise_step, the velocity discarded) with the fp32 residual stream
+ * after block ``layer`` copied into ``h_out`` -- DEVICE fp32 [batch, tokens,
+ * hidden], tokens = state_tokens + horizon; layer -1 gives the stream after
+ * the step's input projection.  Intermediate tensors localise where two
+ * implementations diverge (vla.cpp, Section III-E).  0 <= k < steps,
+ * -1 <= layer < layers.  Asynchronous on the stream.
+ */
+int gr00t_debug_dump(gr00t_ctx* ctx, int k, const float* x_in, int layer, float* h_out);
 
 #ifdef __cplusplus
 }

@@ -56,7 +56,7 @@ def action_time_bias(g, w, steps, dtype=np.float64):
     return out
 
 
-def dit_velocity(g, w, x, mod_k, atb_k, K, V, text_mask, image_mask, state, dtype=np.float64):
+def dit_velocity(g, w, x, mod_k, atb_k, K, V, text_mask, image_mask, state, dtype=np.float64, trace=None):
     """Velocity of the DiT head ("GR00T N1.7", action component).
 
     ``x``: [B, H, A]; ``mod_k``: [B, L+1, 2D]; ``atb_k``: [D]; ``K``/``V``:
@@ -74,6 +74,9 @@ def dit_velocity(g, w, x, mod_k, atb_k, K, V, text_mask, image_mask, state, dtyp
                 h += gelu(LN(h) W_1^T) W_2^T     (reading S9: plain FF)
       final:    n = LN(h) (1 + scale) + shift, row L split (shift, scale)
                 v = n[Ns:] W_out^T + b_out
+
+    ``trace`` (a dict, optional) receives per sample the residual stream after
+    the encoder ("h_in") and after every block i ("h.<i>"), [Ns + H, D] each.
     """
     B, H, A = x.shape
     D, L, Hq, Dh = g["hidden"], g["layers"], g["q_heads"], g["head_dim"]
@@ -88,6 +91,8 @@ def dit_velocity(g, w, x, mod_k, atb_k, K, V, text_mask, image_mask, state, dtyp
         tok = e @ _w(w, "enc_w3", dtype).T + _w(w, "enc_b3", dtype)
         h = np.concatenate([state[b].astype(dtype), tok], axis=0) if Ns else tok
         T = h.shape[0]
+        if trace is not None:
+            trace.setdefault("h_in", []).append(h.copy())
         for i in range(L):
             row = mod_k[b, i].astype(dtype)
             scale, shift = row[:D], row[D:2 * D]
@@ -110,6 +115,8 @@ def dit_velocity(g, w, x, mod_k, atb_k, K, V, text_mask, image_mask, state, dtyp
             h = h + o @ _w(w, f"o_w.{i}", dtype).T
             f = gelu_tanh(layer_norm(h, eps) @ _w(w, f"up_w.{i}", dtype).T)
             h = h + f @ _w(w, f"down_w.{i}", dtype).T
+            if trace is not None:
+                trace.setdefault(f"h.{i}", []).append(h.copy())
         row = mod_k[b, L].astype(dtype)
         shift, scale = row[:D], row[D:2 * D]
         n = layer_norm(h, eps) * (1.0 + scale) + shift

@@ -163,29 +163,37 @@ def test_binding_fails_loudly_without_library(tmp_path):
 
 
 def test_bench_work_accounting_matches_weight_shapes():
+    """The bench's algorithmic bytes are the weights, the prefix K/V and the modulation
+    rows read once per denoise step (641.1 MB for the pi0.5 expert at batch 1)."""
     import bench
     g = synth.config("pi05")
     w = bench.kernel_work(g, 1, 968)
     gemm_weight_bytes = sum(2 * int(np.prod(s)) for k, s in synth.weight_shapes(g).items() if "." in k)
-    # every weight byte of the 18 layers is read exactly once per denoise step
-    M = 50
-    act = 0
-    for name in ("qkv_gemm", "o_gemm", "up_gemm", "down_gemm"):
-        n, by, fl = w[name]
-        assert n == 18
+    for name in ("qkv_gemm", "o_gemm", "up_gemm", "down_gemm", "attention"):
+        assert w[name][0] == 18
     total_w = sum(w[k][0] * w[k][1] for k in ("qkv_gemm", "o_gemm", "up_gemm", "down_gemm"))
-    assert gemm_weight_bytes < total_w < gemm_weight_bytes * 1.08   # + activations
-    kv = w["attention"][0] * w["attention"][1]
-    assert kv > 18 * 968 * 256 * 2 * 2
+    assert total_w == gemm_weight_bytes
+    assert w["attention"][0] * w["attention"][1] == 18 * 968 * 256 * 2 * 2
+    by, fl = bench.step_work(g, 1, 968)
+    assert abs(by / 1e6 - 641.1) < 0.2, by
+    assert abs(fl / 1e9 - 38.65) < 0.1, fl
+    by32, fl32 = bench.step_work(synth.config("pi05_b32"), 32, 968)
+    assert abs(by32 / 1e9 - 1.201) < 0.002 and abs(fl32 / 1e9 - 1237) < 2, (by32, fl32)
 
 
-def test_bench_traffic_needs_unchanged_sources(monkeypatch):
+def test_bench_traffic_needs_unchanged_sources(monkeypatch, tmp_path):
     import bench
-    assert bench.measured_traffic("no_such_workload", "attention") is None
-    for (w, k), (nbytes, srcs) in bench.TRAFFIC.items():
-        assert nbytes > 0 and srcs and k in bench.KCLASS
-    # a digest that no longer matches the source hides the number
-    key = next(iter(bench.TRAFFIC))
-    nbytes, srcs = bench.TRAFFIC[key]
-    monkeypatch.setitem(bench.TRAFFIC, key, (nbytes, {name: "0" * 16 for name in srcs}))
-    assert bench.measured_traffic(*key) is None
+    f = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.measured_traffic("pi05_b32", "attention") is None      # nothing recorded
+    csv = tmp_path / "cap.csv"
+    csv.write_text('"ID","Kernel Name","Metric Name","Metric Unit","Metric Value"\n'
+                   '"0","k","dram__bytes_read.sum","Mbyte","10.5"\n'
+                   '"0","k","dram__bytes_write.sum","Mbyte","1.5"\n'
+                   '"1","k","dram__bytes_read.sum","Mbyte","11.5"\n'
+                   '"1","k","dram__bytes_write.sum","Mbyte","0.5"\n')
+    bench.record_traffic(str(csv), "pi05_b32", "attention", "ncu ...")
+    assert bench.measured_traffic("pi05_b32", "attention") == pytest.approx(12e6)
+    # a digest that no longer matches the kernel sources hides the number
+    monkeypatch.setattr(bench, "source_digest", lambda: "0" * 16)
+    assert bench.measured_traffic("pi05_b32", "attention") is None

@@ -71,6 +71,9 @@ def check_case(case, steps=None, samples=None, options=()):
     torch.cuda.synchronize()
     got = out.cpu().numpy()[idx]
     e_inf, e_rel = oracle.error_metrics(got, xT)
+    # the margins, for the log: worst per-step velocity rel-L2 and the chunk errors
+    print(f"parity {g.get('name', '?')} B={g['batch']} P={g['prefix']} T={T} samples={len(idx)}: "
+          f"worst step rel-L2 {worst:.3e} (gate {vel_tol:g}), chunk max-abs {e_inf:.3e}, chunk rel-L2 {e_rel:.3e}")
     if chunk_rel is not None:
         assert e_rel <= chunk_rel, f"final chunk rel-L2 {e_rel:.3e}"
     else:
@@ -139,12 +142,30 @@ def test_gr00t_full_size():
     check_case(synth.make_case("gr00t"))
 
 
-def test_pi05_batch32_sampled():
-    check_case(synth.make_case("pi05_b32"), samples=[0, 31])
+def _straddling_samples(B, H, tiles=(128, 256)):
+    """Samples whose token rows [b H, (b + 1) H) cross a 128- or 256-row tile
+    boundary of the GEMMs, plus the first and the last sample."""
+    out = {0, B - 1}
+    for b in range(B):
+        lo, hi = b * H, (b + 1) * H
+        if any((lo // t) != ((hi - 1) // t) for t in tiles):
+            out.add(b)
+    return sorted(out)
 
 
-def test_pi05_long_prefix_sampled():
-    check_case(synth.make_case("pi05_long"), samples=[0, 7])
+def test_straddling_sample_choice():
+    # pi0.5 at batch 32: rows of sample 2 (100..149) cross 128, sample 5 (250..299) crosses 256
+    s = _straddling_samples(32, 50)
+    assert {0, 2, 5, 7, 10, 12, 15, 17, 20, 23, 25, 28, 30, 31} <= set(s)
+
+
+def test_pi05_batch32_straddling_samples():
+    g = synth.config("pi05_b32")
+    check_case(synth.make_case("pi05_b32"), samples=_straddling_samples(g["batch"], g["horizon"]))
+
+
+def test_pi05_long_prefix_every_sample():
+    check_case(synth.make_case("pi05_long"))
 
 
 # every attention kernel of the expert family on the same small cases: 1 = CUDA

@@ -136,3 +136,91 @@ def test_no_bounded_wait_timed_out(name):
     x0 = torch.from_numpy(c["x_noise"]).cuda()
     loop.denoise(x0)
     assert loop.info(fmv.INFO_ERROR_FLAG) == 0
+
+
+def test_launch_stamps_cover_every_launch_of_the_loop():
+    """gr00t_kernel_times: one interval per launch of the captured loop, classes of
+    every kind, intervals that add up to the loop's device time."""
+    fmv = _fmv()
+    c = synth.make_case("small_bf16")
+    g = c["geom"]
+    loop, held = fmv.from_case(c)
+    x0 = torch.from_numpy(c["x_noise"]).cuda()
+    ref = loop.denoise(x0).clone()
+    per_step = loop.info(fmv.INFO_KERNELS_PER_STEP)
+    loop.set_option(fmv.OPT_TIME_KERNELS, 1)
+    got = loop.denoise(x0).clone()
+    loop.denoise(x0)
+    us, cls = loop.kernel_times()
+    assert len(us) == per_step * g["steps"]
+    assert set(cls) >= {fmv.KCLASS_QKV_GEMM, fmv.KCLASS_ATTENTION, fmv.KCLASS_O_GEMM, fmv.KCLASS_UP_GEMM,
+                        fmv.KCLASS_DOWN_GEMM, fmv.KCLASS_NORM}
+    assert all(u >= 0 for u in us) and sum(us) > 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    loop.denoise(x0)
+    b.record()
+    b.synchronize()
+    loop_us = a.elapsed_time(b) * 1000.0
+    us2, _ = loop.kernel_times()
+    print(f"stamped loop {sum(us2):.1f} us, event-timed loop {loop_us:.1f} us")
+    assert sum(us2) <= loop_us * 1.05 + 5.0
+    assert torch.equal(got, ref), "the stamps changed the results"
+    loop.set_option(fmv.OPT_TIME_KERNELS, 0)
+    assert loop.kernel_times() == ([], [])
+
+
+def test_bounded_wait_timeout_is_reported_and_the_context_recovers():
+    """A bounded device wait that runs out (on a word nothing writes) sets the error
+    word; the synchronous calls return GR00T_ETIMEOUT, clear it, and the next call
+    runs clean with the same results as before."""
+    fmv = _fmv()
+    c = synth.make_case("small_bf16")
+    loop, held = fmv.from_case(c)
+    xh = torch.from_numpy(c["x_noise"]).pin_memory()
+    clean = torch.empty_like(xh).pin_memory()
+    loop.denoise_host(xh, clean)
+    loop.set_option(fmv.OPT_TEST_STALL, 2000)
+    oh = torch.empty_like(xh).pin_memory()
+    with pytest.raises(fmv.Gr00tError) as ei:
+        loop.denoise_host(xh, oh)
+    assert ei.value.status == fmv.ETIMEOUT and "bounded device wait" in str(ei.value)
+    assert loop.info(fmv.INFO_ERROR_FLAG) == 0          # cleared by the report
+    loop.denoise_step(0, torch.from_numpy(c["x_noise"]).cuda())   # asynchronous: reported by sync
+    with pytest.raises(fmv.Gr00tError) as ei:
+        loop.sync()
+    assert ei.value.status == fmv.ETIMEOUT
+    loop.set_option(fmv.OPT_TEST_STALL, 0)
+    loop.sync()
+    again = torch.empty_like(xh).pin_memory()
+    loop.denoise_host(xh, again)
+    assert torch.equal(again, clean)
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "small_dit"])
+def test_debug_dump_matches_the_oracle_trace(name):
+    """gr00t_debug_dump: the residual stream after every block (and after the input
+    projection) against the oracle's trace of the same velocity evaluation."""
+    fmv = _fmv()
+    c = synth.make_case(name)
+    g, w = c["geom"], c["weights"]
+    B, L, k = g["batch"], g["layers"], 1
+    loop, held = fmv.from_case(c)
+    x = c["x_noise"]
+    mod = oracle.modulation_table(g, w, g["steps"], B)[k * B:(k + 1) * B]
+    trace = {}
+    if g["family"] == synth.FAMILY_EXPERT:
+        oracle.expert_velocity(g, w, x, mod, c["K"], c["V"], trace=trace)
+    else:
+        atb = oracle.action_time_bias(g, w, g["steps"])[k]
+        oracle.dit_velocity(g, w, x, mod, atb, c["K"], c["V"], c["text_mask"], c["image_mask"], c["state"],
+                            trace=trace)
+    xd = torch.from_numpy(x).cuda()
+    worst = 0.0
+    for layer in range(-1, L):
+        h = loop.debug_dump(k, xd, layer).cpu().numpy()
+        ref = np.stack(trace["h_in" if layer < 0 else f"h.{layer}"])
+        _, rel = oracle.error_metrics(h, ref)
+        worst = max(worst, rel)
+        assert rel <= 1e-2, f"block {layer}: residual rel-L2 {rel:.3e}"
+    print(f"debug dump {name}: worst residual rel-L2 {worst:.3e} over {L + 1} dumps")
