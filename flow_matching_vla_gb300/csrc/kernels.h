@@ -121,9 +121,13 @@ struct AttnArgs {
 };
 cudaError_t attention_simt(DType dt, const AttnArgs& a, cudaStream_t s, bool pdl);
 
-// Tensor-core attention of the DiT head (bf16, Dh 48 or 64, <= 32 query tokens, masks).
-bool attn_dit_supported(const AttnArgs& a);
-cudaError_t attention_dit(const AttnArgs& a, cudaStream_t s, bool pdl);
+// Attention of the DiT head (bf16, Dh 48 or 64, <= 32 query tokens, masks): K/V tiles
+// staged by TMA, mma.sync per head, key groups merged on chip.  Either cross-attention
+// (a.P > 0, a.S == 0; kp / vp = the bound context's K / V, the host's copies of the
+// table entries) or self-attention (a.P == 0, a.S == a.Tq <= 64; kp / vp unused).
+bool attn_dit_supported(const AttnArgs& a, const void* kp, const void* vp);
+cudaError_t attention_dit(const AttnArgs& a, const void* kp, const void* vp, int* err, long long wait_limit,
+                          cudaStream_t s, bool pdl);
 
 // Tensor-core attention of the expert family (one KV head, heads folded into rows).
 struct AttnFoldArgs {

@@ -830,8 +830,10 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     }
     ++c->launches;
     at.ts = next_ts(c, GR00T_KCLASS_ATTENTION);
-    if (c->dt == DT_BF16 && c->opt_attn == 0 && attn_dit_supported(at))
-      CK(c, attention_dit(at, s, c->opt_pdl != 0));
+    const void* kp = i % 2 == 0 ? c->host_table[2 * i] : nullptr;
+    const void* vp = i % 2 == 0 ? c->host_table[2 * i + 1] : nullptr;
+    if (c->dt == DT_BF16 && c->opt_attn == 0 && attn_dit_supported(at, kp, vp))
+      CK(c, attention_dit(at, kp, vp, c->err_flag, c->wait_limit, s, c->opt_pdl != 0));
     else
       CK(c, attention_simt(c->dt, at, s, c->opt_pdl != 0));
     GemmArgs go;

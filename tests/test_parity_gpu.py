@@ -110,6 +110,16 @@ def test_dit_random_masks():
     check_case(c)
 
 
+def test_dit_long_context_ring_and_fully_masked_rows():
+    # 1000 context tokens: 16 key tiles through the attention's 6-slot TMA ring; sample 0
+    # sees no text token at all, so the text-mask blocks' rows of that sample are 0
+    c = synth.make_case("small_dit", prefix=1000)
+    tm, im = synth.make_masks(c["geom"], 0, kind="random")
+    tm[0] = 0
+    c["text_mask"], c["image_mask"] = tm, im
+    check_case(c)
+
+
 def test_expert_empty_prefix_and_single_token():
     check_case(synth.make_case("small_bf16", prefix=0, horizon=1, batch=2))
 
