@@ -32,7 +32,7 @@ from .ops import (gelu_tanh, swish, rms_norm, layer_norm, rope_rotate_half, e4m3
                   attention, error_metrics)
 from .schedule import schedule, euler, time_embedding, time_condition, modulation_table
 from .expert import expert_velocity, expert_denoise
-from .dit import dit_velocity, dit_denoise, action_time_bias, project_context
+from .dit import dit_velocity, dit_denoise, action_time_bias, project_context, encode_state
 from .denoise import denoise, velocity
 
 __all__ = [
@@ -40,5 +40,5 @@ __all__ = [
     "attention", "error_metrics", "schedule", "time_embedding",
     "time_condition", "modulation_table", "expert_velocity", "expert_denoise",
     "dit_velocity", "dit_denoise", "action_time_bias", "denoise", "velocity",
-    "euler", "e4m3_decode", "dequantize_rows", "project_context",
+    "euler", "e4m3_decode", "dequantize_rows", "project_context", "encode_state",
 ]

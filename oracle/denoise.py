@@ -6,7 +6,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .dit import action_time_bias, dit_denoise, dit_velocity, project_context
+from .dit import action_time_bias, dit_denoise, dit_velocity, encode_state, project_context
 from .expert import expert_denoise, expert_velocity
 from .schedule import euler, modulation_table
 
@@ -20,6 +20,13 @@ def _kv(case, dtype):
     return case["K"], case["V"]
 
 
+def _state(case, dtype):
+    """The case's state tokens, or (DiT with a raw robot state) their encoding."""
+    if case.get("state_raw") is not None:
+        return encode_state(case["geom"], case["weights"], case["state_raw"], dtype)
+    return case["state"]
+
+
 def denoise(case, steps=None, dtype=np.float64, record=False):
     """Full denoise loop for a ``synth.make_case`` dictionary."""
     g, w = case["geom"], case["weights"]
@@ -28,7 +35,7 @@ def denoise(case, steps=None, dtype=np.float64, record=False):
         return expert_denoise(g, w, case["x_noise"], case["K"], case["V"], T, dtype, record)
     K, V = _kv(case, dtype)
     return dit_denoise(g, w, case["x_noise"], K, V, T, case["text_mask"],
-                       case["image_mask"], case["state"], dtype, record)
+                       case["image_mask"], _state(case, dtype), dtype, record)
 
 
 def velocity(case, x, k, steps=None, dtype=np.float64, mod=None, atb=None):
@@ -45,4 +52,4 @@ def velocity(case, x, k, steps=None, dtype=np.float64, mod=None, atb=None):
         atb = action_time_bias(g, w, T, dtype)
     K, V = _kv(case, dtype)
     return dit_velocity(g, w, x, rows, atb[k], K, V, case["text_mask"],
-                        case["image_mask"], case["state"], dtype)
+                        case["image_mask"], _state(case, dtype), dtype)

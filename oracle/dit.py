@@ -38,6 +38,23 @@ def project_context(g, w, features, dtype=np.float64):
     return K, V
 
 
+def encode_state(g, w, state_raw, dtype=np.float64):
+    """Robot-state token(s) from the raw state ("GR00T N1.7", action: the action
+    component takes the robot state [B, 1, state_dim] beside the noisy actions,
+    and the checkpoint's state encoder is one of the per-embodiment modules
+    resolved at build time).  The page names the module, not its layers; the
+    reading taken here (S18) is a two-layer MLP in the style of the action
+    encoder: s_tok = W_s2 swish(W_s1 s + b_s1) + b_s2, hidden width D.  The state
+    does not change across the denoise steps of a request, so it is embedded
+    once, when the request's inputs are bound.
+
+    ``state_raw``: [B, Ns, state_dim]; returns [B, Ns, D].
+    """
+    s = state_raw.astype(dtype, copy=False)
+    hid = swish(s @ _w(w, "state_w1", dtype).T + _w(w, "state_b1", dtype))
+    return hid @ _w(w, "state_w2", dtype).T + _w(w, "state_b2", dtype)
+
+
 def action_time_bias(g, w, steps, dtype=np.float64):
     """Hoisted action_time_bias [steps, D] ("GR00T N1.7", Build-time constants).
 

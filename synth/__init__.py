@@ -47,7 +47,7 @@ _BASE = dict(
     kv_heads=1, head_dim=64, mlp_dim=1024, mlp_kind=MLP_GELU, horizon=16,
     action_dim=8, state_tokens=0, batch=1, prefix=64, steps=4,
     time_dim=256, time_mlp=0, rope_theta=10000.0, norm_eps=1e-6,
-    direction=-1, weight_format=WFMT_NATIVE, context_dim=0,
+    direction=-1, weight_format=WFMT_NATIVE, context_dim=0, state_dim=0,
 )
 
 
@@ -106,6 +106,13 @@ CONFIGS = {
                         action_dim=32, state_tokens=1, batch=2, prefix=300,
                         steps=4, time_dim=384, time_mlp=1, direction=+1,
                         context_dim=256),
+    # DiT with the robot state encoded at bind time: raw state [B, Ns, state_dim]
+    "gr00t_state": _g(**dict(_GR00T, state_dim=132)),
+    "small_dit_state": _g(family=FAMILY_DIT, layers=4, hidden=384, q_heads=8,
+                          kv_heads=8, head_dim=48, mlp_dim=1536, horizon=16,
+                          action_dim=32, state_tokens=1, batch=2, prefix=300,
+                          steps=4, time_dim=384, time_mlp=1, direction=+1,
+                          state_dim=40),
     "small_dit_fp32": _g(family=FAMILY_DIT, dtype=DTYPE_FP32, layers=2,
                          hidden=192, q_heads=4, kv_heads=4, head_dim=48,
                          mlp_dim=768, horizon=16, action_dim=32,
@@ -186,6 +193,12 @@ def weight_shapes(g: dict) -> dict:
         sh[f"o_w.{l}"] = (D, qd)
         sh[f"up_w.{l}"] = (up_rows(g), D)
         sh[f"down_w.{l}"] = (D, g["mlp_dim"])
+    Ds = g.get("state_dim", 0)
+    if g["family"] == FAMILY_DIT and Ds > 0:   # the state encoder: state_dim -> D -> D
+        sh["state_w1"] = (D, Ds)
+        sh["state_b1"] = (D,)
+        sh["state_w2"] = (D, D)
+        sh["state_b2"] = (D,)
     Dc = g.get("context_dim", 0)
     if g["family"] == FAMILY_DIT and Dc > 0:   # cross K/V projections of the even blocks
         kd = g["kv_heads"] * g["head_dim"]
@@ -340,6 +353,16 @@ def make_state_tokens(g: dict, seed: int = 0, batch: int | None = None):
     return _rng(seed, "state").standard_normal(size=(B, g["state_tokens"], g["hidden"]), dtype=np.float32)
 
 
+def make_raw_state(g: dict, seed: int = 0, batch: int | None = None):
+    """DiT family with state_dim > 0: the raw robot state ~N(0,1), float32
+    [B, n_state, state_dim] (bf16-rounded for bf16 workloads), the input of the
+    bind-time state encoder."""
+    if g["state_tokens"] == 0 or g.get("state_dim", 0) == 0:
+        return None
+    B = g["batch"] if batch is None else batch
+    return _normal(seed, "state_raw", (B, g["state_tokens"], g["state_dim"]), 1.0, g["dtype"] == DTYPE_BF16)
+
+
 def make_masks(g: dict, seed: int = 0, batch: int | None = None, kind: str = "ones"):
     """DiT family: (text_mask, image_mask), uint8 [B, P], 1 = visible.
 
@@ -373,6 +396,8 @@ def make_case(name_or_geom, seed: int = 0, **overrides) -> dict:
 
     DiT workloads with ``context_dim`` > 0 carry VL ``features`` instead of
     bound K/V (K and V are lists of None): the cross K/V are projected from them.
+    DiT workloads with ``state_dim`` > 0 carry the raw robot state ``state_raw``
+    instead of the embedded ``state`` tokens (None): the state encoder embeds it.
     """
     g = config(name_or_geom, **overrides) if isinstance(name_or_geom, str) else dict(name_or_geom)
     tm, im = make_masks(g, seed)
@@ -382,5 +407,7 @@ def make_case(name_or_geom, seed: int = 0, **overrides) -> dict:
         K, V = [None] * g["layers"], [None] * g["layers"]
     else:
         K, V = make_prefix_kv(g, seed)
+    raw = make_raw_state(g, seed) if g["family"] == FAMILY_DIT else None
+    state = None if raw is not None else make_state_tokens(g, seed)
     return dict(geom=g, weights=make_weights(g, seed), K=K, V=V, x_noise=make_noise(g, seed),
-                state=make_state_tokens(g, seed), text_mask=tm, image_mask=im, features=feats, seed=seed)
+                state=state, state_raw=raw, text_mask=tm, image_mask=im, features=feats, seed=seed)

@@ -608,3 +608,78 @@ def test_context_case_equals_bound_projections():
     K, V = oracle.project_context(c["geom"], c["weights"], c["features"])
     bound = dict(c, features=None, K=K, V=V)
     assert np.array_equal(oracle.denoise(c), oracle.denoise(bound))
+
+
+# ---------------------------------------------------------------------------
+# bind-time state encoder (DiT with a raw robot state)
+# ---------------------------------------------------------------------------
+
+def test_encode_state_matches_torch_mlp():
+    c = synth.make_case("small_dit_state")
+    g, w = c["geom"], c["weights"]
+    s = c["state_raw"]
+    assert s.shape == (g["batch"], g["state_tokens"], g["state_dim"])
+    got = oracle.encode_state(g, w, s)
+    ref = F.linear(F.silu(F.linear(t64(s), t64(w["state_w1"]), t64(w["state_b1"]))),
+                   t64(w["state_w2"]), t64(w["state_b2"])).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_encode_state_closed_forms():
+    # zero first layer: every state maps to W_s2 swish(b_s1) + b_s2; zero second
+    # layer: the bias alone; and the first layer sees the state, not its transpose
+    c = synth.make_case("small_dit_state")
+    g, w = c["geom"], dict(c["weights"])
+    D = g["hidden"]
+    w0 = dict(w, state_w1=np.zeros_like(w["state_w1"]))
+    const = w["state_w2"].astype(np.float64) @ oracle.swish(w["state_b1"].astype(np.float64)) + w["state_b2"]
+    got = oracle.encode_state(g, w0, c["state_raw"])
+    np.testing.assert_allclose(got, np.broadcast_to(const, got.shape), rtol=1e-13, atol=1e-13)
+    wz = dict(w, state_w2=np.zeros_like(w["state_w2"]))
+    np.testing.assert_array_equal(oracle.encode_state(g, wz, c["state_raw"]),
+                                  np.broadcast_to(w["state_b2"].astype(np.float64), (g["batch"], 1, D)))
+    # a one-hot state picks one column of W_s1
+    e = np.zeros((1, 1, g["state_dim"]))
+    e[0, 0, 5] = 1.0
+    wi = dict(w, state_w2=np.eye(D), state_b2=np.zeros(D), state_b1=np.zeros(D))
+    np.testing.assert_allclose(oracle.encode_state(g, wi, e)[0, 0],
+                               oracle.swish(w["state_w1"][:, 5].astype(np.float64)), rtol=1e-14, atol=1e-15)
+
+
+def test_state_case_equals_bound_state_tokens():
+    c = synth.make_case("small_dit_state")
+    assert c["state"] is None and c["state_raw"] is not None
+    tokens = oracle.encode_state(c["geom"], c["weights"], c["state_raw"])
+    bound = dict(c, state_raw=None, state=tokens)
+    assert np.array_equal(oracle.denoise(c), oracle.denoise(bound))
+
+
+def test_residual_traces_end_in_the_velocity():
+    # the last traced residual, through the final norm and output projection, is the
+    # velocity; the first is the step's input embedding (the debug-dump reference)
+    for name in ("small_bf16", "small_dit"):
+        c = synth.make_case(name)
+        g, w = c["geom"], c["weights"]
+        B, L, D, k = g["batch"], g["layers"], g["hidden"], 1
+        mod = oracle.modulation_table(g, w, g["steps"], B)[k * B:(k + 1) * B]
+        tr = {}
+        if g["family"] == synth.FAMILY_EXPERT:
+            v = expert_velocity(g, w, c["x_noise"], mod, c["K"], c["V"], trace=tr)
+            for b in range(B):
+                n, _ = ada_rms(tr[f"h.{L - 1}"][b], mod[b, 2 * L].astype(np.float64), g["norm_eps"])
+                np.testing.assert_allclose(n @ w["action_out_w"].astype(np.float64).T + w["action_out_b"], v[b],
+                                           rtol=1e-12, atol=1e-12)
+                h0 = c["x_noise"][b].astype(np.float64) @ w["action_in_w"].astype(np.float64).T + w["action_in_b"]
+                np.testing.assert_allclose(tr["h_in"][b], h0, rtol=1e-13, atol=1e-13)
+        else:
+            atb = oracle.action_time_bias(g, w, g["steps"])[k]
+            v = dit_velocity(g, w, c["x_noise"], mod, atb, c["K"], c["V"], c["text_mask"], c["image_mask"],
+                             c["state"], trace=tr)
+            Ns = g["state_tokens"]
+            for b in range(B):
+                row = mod[b, L].astype(np.float64)
+                n = oracle.layer_norm(tr[f"h.{L - 1}"][b], g["norm_eps"]) * (1 + row[D:2 * D]) + row[:D]
+                np.testing.assert_allclose(n[Ns:] @ w["action_out_w"].astype(np.float64).T + w["action_out_b"],
+                                           v[b], rtol=1e-12, atol=1e-12)
+                np.testing.assert_array_equal(tr["h_in"][b][:Ns], c["state"][b])
+        assert len([k_ for k_ in tr if k_.startswith("h.")]) == L
