@@ -276,7 +276,7 @@ def oracle_rate(case, budget_s: float = 15.0, max_evals: int | None = None):
     sub["x_noise"] = case["x_noise"][:1]
     sub["K"] = [None if k is None else k[:1] for k in case["K"]]
     sub["V"] = [None if v is None else v[:1] for v in case["V"]]
-    for key in ("text_mask", "image_mask", "state"):
+    for key in ("text_mask", "image_mask", "state", "state_raw", "features"):
         if case.get(key) is not None:
             sub[key] = case[key][:1]
     sub["geom"] = dict(g, batch=1)

@@ -39,7 +39,7 @@ __all__ = ["DenoiseLoop", "Gr00tError", "validate_geometry", "load_library", "FA
 
 _SINGLE = ("time_mlp_in_w", "time_mlp_in_b", "time_mlp_out_w", "time_mlp_out_b", "cond_w", "cond_b",
            "action_in_w", "action_in_b", "enc_w1", "enc_b1", "enc_w2", "enc_b2", "enc_w3", "enc_b3",
-           "action_out_w", "action_out_b")
+           "action_out_w", "action_out_b", "state_w1", "state_b1", "state_w2", "state_b2")
 _LAYERED = ("qkv_w", "o_w", "up_w", "down_w")
 
 
@@ -67,6 +67,7 @@ def _geometry(g: dict) -> _abi.Geometry:
     s.norm_eps = float(g.get("norm_eps", 1e-6))
     s.weight_format = int(g.get("weight_format", WFMT_NATIVE))
     s.context_dim = int(g.get("context_dim", 0))
+    s.state_dim = int(g.get("state_dim", 0))
     return s
 
 
@@ -348,7 +349,8 @@ def from_case(case: dict, stream=None, steps=None, device_weights=False, **geom_
 
     tm = dev(case.get("text_mask"), torch.uint8)
     im = dev(case.get("image_mask"), torch.uint8)
-    st = dev(case.get("state"), torch.float32)
+    # the embedded state tokens, or (state_dim > 0) the raw robot state the bind encodes
+    st = dev(case.get("state") if case.get("state_raw") is None else case["state_raw"], torch.float32)
     if case.get("features") is not None:   # cross K/V projected on the GPU at bind time
         feats = dev(case["features"], dt)
         torch.cuda.synchronize()

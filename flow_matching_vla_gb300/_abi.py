@@ -42,7 +42,7 @@ class Geometry(ctypes.Structure):
         "mlp_dim", "mlp_kind", "horizon", "action_dim", "state_tokens", "time_dim", "time_mlp",
         "direction", "max_batch", "max_prefix", "max_steps")] + [
         ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float), ("weight_format", ctypes.c_int32),
-        ("context_dim", ctypes.c_int32)]
+        ("context_dim", ctypes.c_int32), ("state_dim", ctypes.c_int32)]
 
 
 _VP = ctypes.c_void_p
@@ -54,7 +54,8 @@ class Weights(ctypes.Structure):
         "time_mlp_in_w", "time_mlp_in_b", "time_mlp_out_w", "time_mlp_out_b", "cond_w", "cond_b",
         "action_in_w", "action_in_b", "enc_w1", "enc_b1", "enc_w2", "enc_b2", "enc_w3", "enc_b3",
         "action_out_w", "action_out_b")] + [(n, _VPP) for n in (
-        "qkv_w", "o_w", "up_w", "down_w", "qkv_s", "o_s", "up_s", "down_s", "cross_k_w", "cross_v_w")]
+        "qkv_w", "o_w", "up_w", "down_w", "qkv_s", "o_s", "up_s", "down_s", "cross_k_w", "cross_v_w")] + [
+        (n, _VP) for n in ("state_w1", "state_b1", "state_w2", "state_b2")]
 
 
 # exported symbol -> (restype, argtypes)

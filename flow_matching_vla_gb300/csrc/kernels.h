@@ -190,6 +190,9 @@ cudaError_t permute_rows(const void* src, void* dst, int rows, int row_bytes, in
 cudaError_t permute_floats(const float* src, float* dst, int rows, int mode, int p0, int p1, cudaStream_t s);
 // dst[i] = float(src[i]) for a DType source
 cudaError_t to_f32(DType dt, const void* src, float* dst, long long n, cudaStream_t s);
+// dst[m][k] = (DType) src[m][k] for k < K, 0 for K <= k < Kp: fp32 rows [M][K] into
+// activation rows [M][Kp] (the state encoder's input, K padded for the tensor cores)
+cudaError_t state_rows(DType dt, const float* src, int M, int K, void* dst, int Kp, cudaStream_t s);
 
 // One thread waits up to ``limit`` polls for *never to become nonzero; when the
 // limit passes it sets *err = 1 and returns (the bounded-wait error path).

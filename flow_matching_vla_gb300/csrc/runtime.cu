@@ -57,6 +57,11 @@ struct gr00t_ctx {
   void* ctx_feat = nullptr;
   void *w_tin = nullptr, *w_tout = nullptr, *w_cond = nullptr, *w_in = nullptr, *w_out = nullptr;
   void *w_enc1 = nullptr, *w_enc2 = nullptr, *w_enc3 = nullptr;
+  // DiT state encoder (state_dim > 0): W_s1 with its K padded to Ks (a multiple of 64),
+  // its input rows, hidden rows and the encoded state tokens
+  int Ks = 0;
+  void *w_s1 = nullptr, *w_s2 = nullptr, *state_in = nullptr, *state_hid = nullptr;
+  float *b_s1 = nullptr, *b_s2 = nullptr, *state_tok = nullptr;
   float *b_tin = nullptr, *b_tout = nullptr, *b_cond = nullptr, *b_in = nullptr, *b_out = nullptr;
   float *b_enc1 = nullptr, *b_enc2 = nullptr, *b_enc3 = nullptr;
 
@@ -199,6 +204,9 @@ int validate(const gr00t_geometry* g, char* msg, size_t len) {
     return bad(GR00T_EINVAL, "context_dim must be 0 or a multiple of 64 up to 16384");
   if (g->context_dim > 0 && g->family != GR00T_FAMILY_DIT)
     return bad(GR00T_EINVAL, "context_dim (bind-time cross K/V projection) is a DiT-family field");
+  if (g->state_dim < 0 || g->state_dim > 4096) return bad(GR00T_EINVAL, "state_dim must be in [0, 4096]");
+  if (g->state_dim > 0 && (g->family != GR00T_FAMILY_DIT || g->state_tokens < 1))
+    return bad(GR00T_EINVAL, "state_dim (bind-time state encoder) needs the DiT family with state_tokens >= 1");
   if (g->family == GR00T_FAMILY_EXPERT) {
     if (g->kv_heads != 1)
       return bad(GR00T_EINVAL, "expert family needs kv_heads == 1 (the head fold is exact only with one KV head)");
@@ -276,6 +284,16 @@ void plan_buffers(gr00t_ctx* c, Plan& pl) {
   }
   pl.add(&c->w_out, (size_t)c->A * D * es);
   pl.add((void**)&c->b_out, (size_t)c->A * 4);
+  if (dit && c->g.state_dim > 0) {
+    const size_t rows = (size_t)c->g.max_batch * c->Ns;
+    pl.add(&c->w_s1, (size_t)D * c->Ks * es);
+    pl.add((void**)&c->b_s1, (size_t)D * 4);
+    pl.add(&c->w_s2, (size_t)D * D * es);
+    pl.add((void**)&c->b_s2, (size_t)D * 4);
+    pl.add(&c->state_in, rows * c->Ks * es);
+    pl.add(&c->state_hid, rows * D * es);
+    pl.add((void**)&c->state_tok, rows * D * 4);
+  }
   c->w_ck.assign(L, nullptr);
   c->w_cv.assign(L, nullptr);
   c->ctx_k.assign(L, nullptr);
@@ -396,6 +414,8 @@ int check_weights(gr00t_ctx* c, const gr00t_weights* w) {
     for (int l = 0; l < c->L; l += 2)
       if (!w->cross_k_w[l] || !w->cross_v_w[l]) return set_err(c, GR00T_EINVAL, "block %d has a NULL cross weight", l);
   }
+  if (c->g.state_dim > 0 && (!w->state_w1 || !w->state_b1 || !w->state_w2 || !w->state_b2))
+    return set_err(c, GR00T_EINVAL, "state_dim set: the state encoder weights state_w1..state_b2 are required");
   if (c->fp8w) {
     if (!w->qkv_s || !w->o_s || !w->up_s || !w->down_s)
       return set_err(c, GR00T_EINVAL, "FP8 weights need the per-layer scale arrays qkv_s/o_s/up_s/down_s");
@@ -464,6 +484,18 @@ int upload_weights(gr00t_ctx* c, const gr00t_weights* w) {
   }
   M(w->action_out_w, c->w_out, c->A, D, PERM_NONE, 0, 0);
   Bv(w->action_out_b, c->b_out, c->A);
+  if (dit && c->g.state_dim > 0 && rc == GR00T_OK) {
+    // W_s1 [D][state_dim] into [D][Ks], zero columns past state_dim (the tensor-core GEMM's K)
+    cudaError_t e = cudaMemsetAsync(c->w_s1, 0, (size_t)D * c->Ks * c->esz, c->stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(c->w_s1, (size_t)c->Ks * c->esz, w->state_w1, (size_t)c->g.state_dim * c->esz,
+                            (size_t)c->g.state_dim * c->esz, D, on_dev ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                            c->stream);
+    if (e != cudaSuccess) rc = set_err(c, GR00T_ECUDA, "state encoder upload failed: %s", cudaGetErrorString(e));
+    M(w->state_w2, c->w_s2, D, D, PERM_NONE, 0, 0);
+    Bv(w->state_b1, c->b_s1, D);
+    Bv(w->state_b2, c->b_s2, D);
+  }
   if (dit && c->g.context_dim > 0)
     for (int l = 0; l < c->L; l += 2) {
       M(w->cross_k_w[l], c->w_ck[l], c->Hkv * c->Dh, c->g.context_dim, PERM_NONE, 0, 0);
@@ -983,6 +1015,7 @@ extern "C" int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, voi
   c->F = g->mlp_dim; c->H = g->horizon; c->A = g->action_dim; c->Ns = g->state_tokens; c->E = g->time_dim;
   c->tok = c->H + c->Ns;
   c->qd = c->Hq * c->Dh;
+  c->Ks = (g->state_dim + 63) / 64 * 64;
   const bool dit = g->family == GR00T_FAMILY_DIT;
   c->S = dit ? c->L + 1 : 2 * c->L + 1;
   c->R = (dit ? 2 : 3) * c->D;
@@ -1080,6 +1113,22 @@ extern "C" int gr00t_bind_prefix_kv(gr00t_ctx* c, int batch, int prefix, const v
   if (!dit && state_tokens) return set_err(c, GR00T_EINVAL, "the expert family has no state tokens");
   if (dit && c->Ns > 0 && !state_tokens) return set_err(c, GR00T_EINVAL, "state_tokens required");
   if (prefix > 0 && (!k || !v)) return set_err(c, GR00T_EINVAL, "k/v pointer arrays are NULL");
+  if (dit && c->g.state_dim > 0 && state_tokens) {
+    // the raw robot state [batch, Ns, state_dim] -> the library's state tokens [batch, Ns, D]
+    const int M = batch * c->Ns, D = c->D;
+    CK(c, state_rows(c->dt, state_tokens, M, c->g.state_dim, c->state_in, c->Ks, c->stream));
+    c->launches = 0;
+    GemmArgs g1;
+    g1.A = c->state_in; g1.lda = c->Ks; g1.W = c->w_s1; g1.ldw = c->Ks; g1.M = M; g1.N = D; g1.K = c->Ks;
+    g1.epi.kind = EPI_STORE; g1.epi.act = ACT_SWISH; g1.epi.bias = c->b_s1; g1.epi.out = c->state_hid;
+    g1.epi.ldo = D;
+    RC(gemm(c, g1));
+    GemmArgs g2;
+    g2.A = c->state_hid; g2.lda = D; g2.W = c->w_s2; g2.ldw = D; g2.M = M; g2.N = D; g2.K = D;
+    g2.epi.kind = EPI_STORE; g2.epi.out_f32 = 1; g2.epi.bias = c->b_s2; g2.epi.out = c->state_tok; g2.epi.ldo = D;
+    RC(gemm(c, g2));
+    state_tokens = c->state_tok;
+  }
   std::vector<const void*> t(2 * c->L + 3, nullptr);
   for (int l = 0; l < c->L; ++l) {
     if (dit && l % 2 == 1) continue;

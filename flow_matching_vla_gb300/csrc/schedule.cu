@@ -123,6 +123,29 @@ cudaError_t to_f32(DType dt, const void* src, float* dst, long long n, cudaStrea
 
 namespace {
 
+template <typename T>
+__global__ void state_rows_kernel(const float* __restrict__ src, int M, int K, T* __restrict__ dst, int Kp) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)M * Kp) return;
+  const int m = (int)(i / Kp), k = (int)(i % Kp);
+  dst[i] = from_f<T>(k < K ? src[(long long)m * K + k] : 0.f);
+}
+
+}  // namespace
+
+cudaError_t state_rows(DType dt, const float* src, int M, int K, void* dst, int Kp, cudaStream_t s) {
+  const long long n = (long long)M * Kp;
+  if (n <= 0) return cudaSuccess;
+  const unsigned blocks = (unsigned)((n + 255) / 256);
+  if (dt == DT_F32)
+    state_rows_kernel<float><<<blocks, 256, 0, s>>>(src, M, K, (float*)dst, Kp);
+  else
+    state_rows_kernel<bf16><<<blocks, 256, 0, s>>>(src, M, K, (bf16*)dst, Kp);
+  return cudaGetLastError();
+}
+
+namespace {
+
 __global__ void bounded_wait_probe_kernel(const volatile int* never, int* err, long long limit) {
   if (threadIdx.x != 0) return;
   for (long long i = 0; i < limit; ++i)

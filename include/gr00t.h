@@ -108,6 +108,8 @@ typedef struct gr00t_geometry {
   int32_t weight_format; /* GR00T_WFMT_*: storage of the per-layer projections */
   int32_t context_dim;   /* DIT: width of the VL features gr00t_bind_context projects
                             into the cross K/V (multiple of 64); 0: K/V bound directly */
+  int32_t state_dim;     /* DIT: width of the raw robot state the binds embed with the
+                            state encoder (<= 4096); 0: state tokens bound already embedded */
 } gr00t_geometry;
 
 /* Storage of the per-layer projections (qkv_w, o_w, up_w, down_w).  FP8: each
@@ -134,6 +136,9 @@ typedef struct gr00t_geometry {
  *   DIT:    enc_w1 [D, A], enc_b1 [D], enc_w2 [D, D+E] acting on
  *           concat(W1 x + b1, temb(tau)), enc_b2 [D], enc_w3 [D, D], enc_b3 [D]
  *   action_out_w [A, D], action_out_b [A]
+ *   DIT with state_dim > 0: the state encoder state_w1 [D, state_dim],
+ *           state_b1 [D], state_w2 [D, D], state_b2 [D]:
+ *           s_tok = state_w2 swish(state_w1 s + state_b1) + state_b2
  *   per layer l (arrays of ``layers`` pointers; with GR00T_WFMT_FP8 these four
  *   are uint8 E4M3 codes and qkv_s .. down_s their fp32 row scales):
  *     qkv_w[l]  EXPERT: [Hq*Dh + 2*Dh, D] rows (q heads, k, v)
@@ -175,6 +180,11 @@ typedef struct gr00t_weights {
    * NULL), in the geometry's dtype, no bias */
   const void* const* cross_k_w;
   const void* const* cross_v_w;
+  /* DIT with state_dim > 0 (else NULL): the state encoder, in the geometry's dtype */
+  const void* state_w1;
+  const void* state_b1;
+  const void* state_w2;
+  const void* state_b2;
 } gr00t_weights;
 
 typedef struct gr00t_ctx gr00t_ctx;
@@ -214,7 +224,13 @@ int gr00t_create(const gr00t_geometry* g, const gr00t_weights* w, void* stream, 
  * mask otherwise ("GR00T N1.7", action).  NULL = all visible.  Must be NULL
  * for EXPERT (its head fold needs the all-ones mask).
  * ``state_tokens``: DIT only, DEVICE fp32 [batch, state_tokens, hidden], the
- * embedded robot state placed ahead of the action tokens; borrowed.
+ * embedded robot state placed ahead of the action tokens; borrowed.  With
+ * state_dim > 0 it is instead the RAW robot state [batch, state_tokens,
+ * state_dim] (fp32), which this call embeds with the state encoder into
+ * library-owned tokens on the tensor cores ("GR00T N1.7", action: the robot
+ * state enters beside the noisy actions and its encoder is one of the
+ * per-embodiment modules; it does not change across a request's denoise
+ * steps, so it is embedded once, here); read on the stream, not borrowed.
  * 1 <= batch <= max_batch; 0 <= prefix <= max_prefix (EXPERT), 1 <= prefix
  * (DIT).  Enqueues a small copy on the stream.
  */

@@ -89,6 +89,17 @@ def test_context_dim_rules(lib):
     assert rc == -1 and "context_dim" in msg
 
 
+def test_state_dim_rules(lib):
+    import flow_matching_vla_gb300 as fmv
+    assert fmv.validate_geometry(synth.config("gr00t_state"))[0] == 0
+    rc, msg = fmv.validate_geometry(synth.config("pi05", state_dim=32))
+    assert rc == -1 and "state_dim" in msg
+    rc, msg = fmv.validate_geometry(synth.config("gr00t_state", state_tokens=0))
+    assert rc == -1 and "state_dim" in msg
+    rc, msg = fmv.validate_geometry(synth.config("gr00t_state", state_dim=5000))
+    assert rc == -1 and "state_dim" in msg
+
+
 def test_dit_geometry_rules(lib):
     import flow_matching_vla_gb300 as fmv
     g = synth.config("gr00t")
@@ -136,6 +147,7 @@ def _dummy_weights(g, skip=()):
     ("pi05_fp8", ("qkv_s",), b"scale"),
     ("gr00t_ctx", ("cross_v_w",), b"cross"),
     ("pi05", ("cond_w",), b"cond_w"),
+    ("gr00t_state", ("state_b2",), b"state encoder"),
 ])
 def test_create_checks_weight_pointers_before_touching_cuda(lib, cfg, skip, needle):
     import flow_matching_vla_gb300 as fmv

@@ -87,7 +87,7 @@ def _subcase(case, idx):
     c["x_noise"] = case["x_noise"][idx]
     c["K"] = [None if k is None else k[idx] for k in case["K"]]
     c["V"] = [None if v is None else v[idx] for v in case["V"]]
-    for key in ("text_mask", "image_mask", "state", "features"):
+    for key in ("text_mask", "image_mask", "state", "state_raw", "features"):
         if case.get(key) is not None:
             c[key] = case[key][idx]
     c["geom"] = dict(case["geom"], batch=len(idx))
@@ -267,6 +267,20 @@ def test_dit_context_projection_small():
 
 def test_gr00t_context_projection_full_size():
     check_case(synth.make_case("gr00t_ctx"))
+
+
+# DiT robot state embedded at bind time by the state encoder (raw state [B, Ns, state_dim],
+# state_dim 40 and the pages' 132, padded to the tensor cores' K on the device)
+def test_dit_state_encoder_small():
+    check_case(synth.make_case("small_dit_state"))
+
+
+def test_gr00t_state_encoder_full_size():
+    check_case(synth.make_case("gr00t_state"))
+
+
+def test_gr00t_state_encoder_with_context_projection():
+    check_case(synth.make_case("small_dit_state", context_dim=256, batch=3))
 
 
 def test_bind_context_refused_without_context_dim():

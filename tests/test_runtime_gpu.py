@@ -197,10 +197,11 @@ def test_bounded_wait_timeout_is_reported_and_the_context_recovers():
     assert torch.equal(again, clean)
 
 
-@pytest.mark.parametrize("name", ["small_bf16", "small_dit"])
+@pytest.mark.parametrize("name", ["small_bf16", "small_dit", "small_dit_state"])
 def test_debug_dump_matches_the_oracle_trace(name):
     """gr00t_debug_dump: the residual stream after every block (and after the input
-    projection) against the oracle's trace of the same velocity evaluation."""
+    projection, whose state rows are the bound -- or bind-time encoded -- state
+    tokens) against the oracle's trace of the same velocity evaluation."""
     fmv = _fmv()
     c = synth.make_case(name)
     g, w = c["geom"], c["weights"]
@@ -213,7 +214,8 @@ def test_debug_dump_matches_the_oracle_trace(name):
         oracle.expert_velocity(g, w, x, mod, c["K"], c["V"], trace=trace)
     else:
         atb = oracle.action_time_bias(g, w, g["steps"])[k]
-        oracle.dit_velocity(g, w, x, mod, atb, c["K"], c["V"], c["text_mask"], c["image_mask"], c["state"],
+        state = c["state"] if c.get("state_raw") is None else oracle.encode_state(g, w, c["state_raw"])
+        oracle.dit_velocity(g, w, x, mod, atb, c["K"], c["V"], c["text_mask"], c["image_mask"], state,
                             trace=trace)
     xd = torch.from_numpy(x).cuda()
     worst = 0.0
