@@ -10,19 +10,25 @@
 //    the suffix tiles from this step's QKV projection;
 //  * warps 0 and 10 issue TMA: Q once through a 4-D map over [tokens][heads][Dh]
 //    whose box lands exactly in folded-row order; K and V tiles through
-//    separate 2-slot rings (128-byte swizzle, 64-element boxes), a K slot
-//    freed as soon as S = QK^T read it, a V slot when P V did;
+//    separate rings (128-byte swizzle, 64-element boxes; for Dh = 256 three K
+//    slots and two V slots), a K slot freed as soon as S = QK^T read it, a V
+//    slot when P V did.  The row tiles of one sample (and split) read the same
+//    key tiles, so they run as a cluster: each CTA loads 1/CT of every K and V
+//    tile (CT = row tiles, 2 or 4) and multicasts it into all CT CTAs, and a
+//    slot is refilled once every CTA's MMA released it -- a tile is fetched
+//    once per sample, and each SM issues a quarter of the requests;
 //  * warp 1 issues tcgen05.mma: S = Q K^T into one of two TMEM buffers
 //    (kind::f16, K-major operands), and O += P V into a TMEM accumulator with
 //    V read MN-major straight from its [key][dim] tile; with a paged pool bound,
 //    the first row tile's CTAs also store the suffix K/V tiles into the pool's
 //    slots [P, P + H);
-//  * warps 2..9 (two per TMEM lane quadrant: one thread per row for each half
-//    of a tile's keys and of O's columns) run the softmax in registers: exp2 of
-//    scaled scores against a running maximum that is only raised -- and O
-//    rescaled in TMEM -- when a tile's maximum exceeds it by more than 8 (2^8
-//    headroom, exact arithmetic otherwise), write P (bf16) into shared memory
-//    in the MMA's swizzled K-major layout and hand it to the MMA warp;
+//  * warps 2..5 (one per TMEM lane quadrant, one thread per row, all keys of a
+//    tile) run the softmax in registers: exp2 of scaled scores against a
+//    running maximum that is only raised -- and O rescaled in TMEM -- when a
+//    tile's maximum exceeds it by more than 8 (2^8 headroom, exact arithmetic
+//    otherwise), and write P (bf16 pairs) into one of two TMEM buffers, from
+//    which the P V MMA reads its A operand (no shared-memory round trip, no
+//    exchange between threads of a row); warps 6..9 join for the output tile;
 //  * the output tile (O / sum, bf16) is staged in the idle Q buffer and written
 //    with one tensor store: to the attention output, or with S key splits as a
 //    partial (with (max, sum)) to the workspace, where a warp-per-row kernel
@@ -45,26 +51,29 @@ namespace {
 
 constexpr int ROWS = 128;   // folded query rows per CTA (MMA M)
 constexpr int KT = 64;      // keys per tile (MMA N of S, K of PV)
-// warp 0: K loads, 1: MMA, 2..9: softmax (two warps per TMEM lane quadrant, one per
-// half of the keys of a tile and of O's columns), 10: V loads
+// warp 0: K loads, 1: MMA, 2..5: softmax (one warp per TMEM lane quadrant, a thread
+// per row), 6..9 with 2..5: the output tile (half of O's columns each), 10: V loads
 constexpr int kThreads = 352;
 constexpr int kSlack = 256;   // alignment slack of the dynamic shared memory (checked)
 constexpr int kMaxSplits = 32;   // key splits (a lane of the merge kernel's warp per split)
+constexpr long long kDrainPolls = 1LL << 22;   // bounded wait for this CTA's own copies after an abort
 
 template <int DH>
 struct T5Smem {
   static constexpr int BOXES = DH / 64;          // 64-element column boxes per row block
   static constexpr int Q_BYTES = ROWS * DH * 2;
   static constexpr int KV_BYTES = KT * DH * 2;   // one K (or V) tile
-  static constexpr int STAGE = 2 * KV_BYTES;     // K tile then V tile of one ring slot
-  static constexpr int P_BYTES = ROWS * KT * 2;   // one of two P buffers
+  static constexpr int NK = DH == 256 ? 3 : 4;   // K ring slots
+  static constexpr int NV = DH == 256 ? 2 : 4;   // V ring slots
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + 2 * STAGE;
-  static constexpr int OFF_X = OFF_P + 2 * P_BYTES;   // row-maximum exchange [2 parities][2 halves][ROWS]
-  static constexpr int OFF_BAR = OFF_X + 2 * 2 * ROWS * 4;
-  static constexpr int NBAR = 1 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 2 + 8;
+  static constexpr int OFF_K = Q_BYTES;
+  static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
+  static constexpr int OFF_X = OFF_V + NV * KV_BYTES;   // per row: (sum, max) handed to the staging warps
+  static constexpr int OFF_BAR = OFF_X + 2 * ROWS * 4;
+  static constexpr int NBAR = 1 + 2 * NK + 3 + 3 + 2 + 2 + 2 * NV;
   static constexpr int TOTAL = OFF_BAR + NBAR * 8 + 16 + kSlack;
+  static_assert(TOTAL <= 232448, "shared memory of the tcgen05 attention");
+  static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0 && KV_BYTES % 1024 == 0, "128-byte-swizzled tiles");
 };
 
 // MN-major (V) descriptor: 64-element rows of 128 bytes along N in groups of 8 K-rows
@@ -120,6 +129,25 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
       "[%2];" ::"r"(ptx::smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+// Multicast variants: the box lands at the same offset in every CTA of ``mask``,
+// completing on the mbarrier at the same offset in each.
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z,
+                                               uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(ptx::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z), "h"(mask), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_mc(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z,
+                                               int w, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%3, %4, %5, %6}], [%2], %7, %8;" ::"r"(ptx::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(ptx::smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask),
+      "l"(policy)
       : "memory");
 }
 // Tensor stores of a shared-memory tile (bulk-group completion).
@@ -194,20 +222,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicExch(a.err, 1);
     return;
   }
+  constexpr int NK = L::NK, NV = L::NV;
   uint8_t* sQ = smem + L::OFF_Q;
-  uint8_t* sKV = smem + L::OFF_KV;
-  uint8_t* sP = smem + L::OFF_P;
+  uint8_t* sK = smem + L::OFF_K;
+  uint8_t* sV = smem + L::OFF_V;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;    // [2] K tile of ring slot landed
-  uint64_t* k_empty = bars + 3;   // [2] S = QK^T read it
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_empty = bars + 7;   // [2]
-  uint64_t* p_full = bars + 9;    // [2] P buffer b written
-  uint64_t* pv_done = bars + 11;  // [2] the PV reading P buffer b completed
-  uint64_t* v_full = bars + 13;   // [2] V tile of ring slot landed
-  uint64_t* v_empty = bars + 15;  // [2] PV read it
-  uint64_t* x_bar = bars + 17;    // [4 quadrants][2 parities] the two halves of a row exchanged
+  uint64_t* k_full = bars + 1;           // [NK] K tile of ring slot landed
+  uint64_t* k_empty = k_full + NK;       // [NK] S = QK^T read it
+  uint64_t* s_full = k_empty + NK;       // [3] S buffer b computed
+  uint64_t* s_empty = s_full + 3;        // [3] the softmax read it
+  uint64_t* p_full = s_empty + 3;        // [2] P buffer b written
+  uint64_t* pv_done = p_full + 2;        // [2] the PV reading P buffer b completed
+  uint64_t* v_full = pv_done + 2;        // [NV] V tile of ring slot landed
+  uint64_t* v_empty = v_full + NV;       // [NV] PV read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::NBAR);
   float* xm = reinterpret_cast<float*>(smem + L::OFF_X);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -227,22 +255,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // a bound K/V pool takes this step's suffix K/V into its slots [P, P + H): the CTAs of
   // the first row tile own the suffix tiles of their key range and store them from shared memory
   const bool pool_writer = a.pool_k != nullptr && blockIdx.x == 0;
+  const int CT = a.ct > 1 ? a.ct : 1;                 // CTAs of the cluster (row tiles of the sample)
+  const int crank = CT > 1 ? (int)(blockIdx.x % CT) : 0;
+  const uint16_t cmask = (uint16_t)((1u << CT) - 1);
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NK; ++i) {
       ptx::mbar_init(&k_full[i], 1);
-      ptx::mbar_init(&k_empty[i], 1);
+      ptx::mbar_init(&k_empty[i], CT);   // every CTA of the cluster releases a multicast slot
+    }
+    for (int i = 0; i < NV; ++i) {
       ptx::mbar_init(&v_full[i], 1);
-      ptx::mbar_init(&v_empty[i], 1);
+      ptx::mbar_init(&v_empty[i], CT);
+    }
+    for (int i = 0; i < 3; ++i) {
       ptx::mbar_init(&s_full[i], 1);
-      ptx::mbar_init(&s_empty[i], 8);
+      ptx::mbar_init(&s_empty[i], 4);   // the four softmax warps read S
     }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&p_full[i], 8);
+      ptx::mbar_init(&p_full[i], 4);    // the four softmax warps wrote P
       ptx::mbar_init(&pv_done[i], 1);
     }
-    for (int i = 0; i < 8; ++i) ptx::mbar_init(&x_bar[i], 64);
     *abort_flag = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmQ);
@@ -256,38 +290,108 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  if (CT > 1) ptx::cluster_sync_all();   // the peers' barriers exist before any copy or release targets them
   const uint32_t tmem = *tmem_slot;
   const uint32_t tO = tmem;              // O: DH columns
-  const uint32_t tS = tmem + 256;        // S buffers: 2 x 64 columns
+  const uint32_t tS = tmem + 256;        // S buffers: 3 x 64 columns (S runs two tiles ahead of P V)
+  const uint32_t tP = tmem + 448;        // P buffers: 2 x 32 columns of bf16 pairs (lane = row)
   ptx::pdl_launch_dependents();
   auto fail = [&]() {
     *abort_flag = 1;
     atomicExch(a.err, 1);
   };
 
+  constexpr uint32_t idS = ptx::idesc_bf16(ROWS, KT);
+  constexpr uint32_t idO = ptx::idesc_bf16(ROWS, DH) | (1u << 16);   // B (V) MN-major
+  // S(j) = Q K(j)^T into S buffer j % 3
+  auto issue_s = [&](int j) -> bool {
+    const int st = j % NK, sb = j % 3;
+    if (!ptx::mbar_wait(&k_full[st], (j / NK) & 1, lim)) return false;
+    if (j >= 3 && !ptx::mbar_wait(&s_empty[sb], ((j / 3) - 1) & 1, lim)) return false;
+    ptx::tc_fence_after();
+    const KeyTile kt = key_tile(t_begin + j, b, a.P, a.H);
+    if (pool_writer && !kt.prefix)   // rows past H fall outside the pool map
+      tma_store_4d(&tmPk, sK + st * L::KV_BYTES, 0, kt.srow, b, 0);
+    const uint32_t q0 = ptx::smem_u32(sQ), k0 = ptx::smem_u32(sK + st * L::KV_BYTES);
+#pragma unroll
+    for (int x = 0; x < L::BOXES; ++x)
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        ptx::mma_bf16(tS + sb * KT, ptx::sdesc_sw128(q0 + x * ROWS * 128) + 2 * k,
+                      ptx::sdesc_sw128(k0 + x * KT * 128) + 2 * k, idS, (x | k) != 0);
+    ptx::mma_commit(&s_full[sb]);
+    if (pool_writer && !kt.prefix) {   // the slot is refilled only after the store read it
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
+    if (CT == 1)
+      ptx::mma_commit(&k_empty[st]);
+    else
+      ptx::mma_commit_mc(&k_empty[st], cmask);
+    return true;
+  };
+  // O += P(j) V(j), P from TMEM buffer j & 1
+  auto issue_pv = [&](int j) -> bool {
+    const int st = j % NV, pb = j & 1;
+    if (!ptx::mbar_wait(&p_full[pb], (j >> 1) & 1, lim)) return false;
+    if (!ptx::mbar_wait(&v_full[st], (j / NV) & 1, lim)) return false;
+    ptx::tc_fence_after();
+    const KeyTile vt = key_tile(t_begin + j, b, a.P, a.H);
+    if (pool_writer && !vt.prefix) tma_store_4d(&tmPv, sV + st * L::KV_BYTES, 0, vt.srow, b, 0);
+    const uint32_t v0 = ptx::smem_u32(sV + st * L::KV_BYTES);
+#pragma unroll
+    for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 8 P columns; 2 K-row groups of 1024 bytes of V
+      ptx::mma_bf16_tmem_a(tO, tP + pb * (KT / 2) + 8 * k, sdesc_sw128_mn(v0 + k * 2048, KT * 128), idO,
+                           j > 0 || k > 0);
+    ptx::mma_commit(&pv_done[pb]);
+    if (pool_writer && !vt.prefix) {
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    }
+    if (CT == 1)
+      ptx::mma_commit(&v_empty[st]);
+    else
+      ptx::mma_commit_mc(&v_empty[st], cmask);
+    return true;
+  };
   if (warp == 0 || warp == 10) {
     // ---------------- TMA producers: warp 0 streams K tiles, warp 10 V tiles ----------------
     if (lane == 0) {
       const bool is_k = warp == 0;
+      const int NS = is_k ? NK : NV;
       uint64_t* full = is_k ? k_full : v_full;
       uint64_t* empty = is_k ? k_empty : v_empty;
-      auto load = [&](int i, int st) {
+      uint8_t* ring = is_k ? sK : sV;
+      const CUtensorMap* pmap = is_k ? &tmKp : &tmVp;
+      auto load = [&](int i) {
+        const int st = i % NS;
         const KeyTile kt = key_tile(t_begin + i, b, a.P, a.H);
-        uint8_t* dst = sKV + st * L::STAGE + (is_k ? 0 : L::KV_BYTES);
-        ptx::mbar_arrive_expect_tx(&full[st], L::KV_BYTES);
+        uint8_t* dst = ring + st * L::KV_BYTES;
+        ptx::mbar_arrive_expect_tx(&full[st], L::KV_BYTES);   // the whole tile lands here (all CT parts)
         // [Dh/64 boxes][KT rows][64 columns] in one request; prefix: 4-D map (columns, rows
         // [0, P) of the sample, samples, boxes) so rows past P read as zeros, never as a
-        // neighbour's rows or a pool's other slots
-        if (kt.prefix)
-          tma_load_4d_hint(dst, is_k ? &tmKp : &tmVp, &full[st], 0, kt.row, b, 0, ptx::policy_evict_first());
-        else
-          tma_load_3d_hint(dst, is_k ? &tmKs : &tmVs, &full[st], 0, kt.row, 0, ptx::policy_evict_last());
+        // neighbour's rows or a pool's other slots.  In a cluster this CTA loads boxes
+        // [crank * part, (crank + 1) * part) and multicasts them
+        const int part = L::BOXES / CT;
+        if (CT == 1) {
+          if (kt.prefix)
+            tma_load_4d_hint(dst, pmap, &full[st], 0, kt.row, b, 0, ptx::policy_evict_first());
+          else
+            tma_load_3d_hint(dst, is_k ? &tmKs : &tmVs, &full[st], 0, kt.row, 0, ptx::policy_evict_last());
+        } else {
+          uint8_t* dpart = dst + crank * part * KT * 128;
+          if (kt.prefix)
+            tma_load_4d_mc(dpart, pmap, &full[st], 0, kt.row, b, crank * part, cmask, ptx::policy_evict_first());
+          else
+            tma_load_3d_mc(dpart, is_k ? &tmKs : &tmVs, &full[st], 0, kt.row, crank * part, cmask,
+                           ptx::policy_evict_last());
+        }
       };
       // bound prefix tiles do not depend on the previous kernel: stage them first
       int pre = 0;
-      for (; pre < 2 && pre < nt; ++pre)
+      for (; pre < NS && pre < nt; ++pre)
         if (!key_tile(t_begin + pre, b, a.P, a.H).prefix) break;
-      for (int i = 0; i < pre; ++i) load(i, i);
+      for (int i = 0; i < pre; ++i) load(i);
       ptx::pdl_wait();
       if (is_k) kstamp(a.ts);
       if (is_k) {
@@ -298,157 +402,115 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int loaded = pre;
       for (int i = pre; i < nt && !*abort_flag; ++i) {
-        const int st = i & 1;
-        if (i >= 2 && !ptx::mbar_wait(&empty[st], ((i >> 1) & 1) ^ 1, lim)) {
+        const int st = i % NS;
+        if (i >= NS && !ptx::mbar_wait(&empty[st], ((i / NS) & 1) ^ 1, lim)) {
           fail();
           break;
         }
-        load(i, st);
+        load(i);
         loaded = i + 1;
       }
-      if (*abort_flag) {  // drain this thread's in-flight copies (bounded) before the CTA can exit
-        if (is_k) ptx::mbar_wait(q_full, 0, lim);
-        for (int i = loaded - 1; i >= 0 && i >= loaded - 2; --i) ptx::mbar_wait(&full[i & 1], (i >> 1) & 1, lim);
+      const long long drain = lim > kDrainPolls ? lim : kDrainPolls;
+      if (*abort_flag) {  // drain this thread's in-flight copies before the CTA can exit
+        if (is_k) ptx::mbar_wait(q_full, 0, drain);
+        for (int i = loaded - 1; i >= 0 && i >= loaded - NS; --i)
+          ptx::mbar_wait(&full[i % NS], (i / NS) & 1, drain);
       }
+      if (CT > 1)   // every CTA's release of this ring has arrived: no MMA warp signals it any more
+        for (int i = loaded - 1; i >= 0 && i >= loaded - NS; --i)
+          ptx::mbar_wait(&empty[i % NS], (i / NS) & 1, drain);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer (lane 0; the other lanes idle until the end) ----------------
+    // order on the tensor pipe: S(0), S(1), then S(j + 2) ahead of P(j) V(j), so the
+    // softmax of tile j has two S batches of time before its P V is due
     if (lane == 0) {
-      constexpr uint32_t idS = ptx::idesc_bf16(ROWS, KT);
-      constexpr uint32_t idO = ptx::idesc_bf16(ROWS, DH) | (1u << 16);   // B (V) MN-major
       bool ok = ptx::mbar_wait(q_full, 0, lim);
-      if (!ok) fail();
-      for (int j = 0; ok && j <= nt; ++j) {
-        if (j < nt) {  // S(j) = Q K(j)^T
-          const int st = j & 1, sb = j & 1;
-          if (!ptx::mbar_wait(&k_full[st], (j >> 1) & 1, lim)) { fail(); break; }
-          if (j >= 2 && !ptx::mbar_wait(&s_empty[sb], ((j >> 1) & 1) ^ 1, lim)) { fail(); break; }
-          ptx::tc_fence_after();
-          const KeyTile kt = key_tile(t_begin + j, b, a.P, a.H);
-          if (pool_writer && !kt.prefix)   // rows past H fall outside the pool map
-            tma_store_4d(&tmPk, sKV + st * L::STAGE, 0, kt.srow, b, 0);
-          const uint32_t q0 = ptx::smem_u32(sQ), k0 = ptx::smem_u32(sKV + st * L::STAGE);
-#pragma unroll
-          for (int x = 0; x < L::BOXES; ++x)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              ptx::mma_bf16(tS + sb * KT, ptx::sdesc_sw128(q0 + x * ROWS * 128) + 2 * k,
-                            ptx::sdesc_sw128(k0 + x * KT * 128) + 2 * k, idS, (x | k) != 0);
-          ptx::mma_commit(&s_full[sb]);
-          if (pool_writer && !kt.prefix) {   // the slot is refilled only after the store read it
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-          }
-          ptx::mma_commit(&k_empty[st]);
-        }
-        if (j >= 1) {  // O += P(j-1) V(j-1)
-          const int st = (j - 1) & 1, pb = (j - 1) & 1;
-          if (!ptx::mbar_wait(&p_full[pb], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
-          if (!ptx::mbar_wait(&v_full[st], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
-          ptx::tc_fence_after();
-          const KeyTile vt = key_tile(t_begin + j - 1, b, a.P, a.H);
-          if (pool_writer && !vt.prefix) tma_store_4d(&tmPv, sKV + st * L::STAGE + L::KV_BYTES, 0, vt.srow, b, 0);
-          const uint32_t p0 = ptx::smem_u32(sP + pb * L::P_BYTES);
-          const uint32_t v0 = ptx::smem_u32(sKV + st * L::STAGE + L::KV_BYTES);
-#pragma unroll
-          for (int k = 0; k < KT / 16; ++k)   // 16 keys per MMA: 2 K-row groups of 1024 bytes of V
-            ptx::mma_bf16(tO, ptx::sdesc_sw128(p0) + 2 * k, sdesc_sw128_mn(v0 + k * 2048, KT * 128), idO,
-                          (j - 1) > 0 || k > 0);
-          ptx::mma_commit(&pv_done[pb]);
-          if (pool_writer && !vt.prefix) {
-            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-          }
-          ptx::mma_commit(&v_empty[st]);
-        }
+      for (int j = 0; ok && j < 2 && j < nt; ++j) ok = issue_s(j);
+      for (int j = 0; ok && j < nt; ++j) {
+        if (j + 2 < nt) ok = issue_s(j + 2);
+        if (ok) ok = issue_pv(j);
       }
+      if (!ok) fail();
       if (pool_writer) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // pool writes done
     }
   } else {
-    // ---------------- softmax (warps 2..9: TMEM lane quadrant = warp % 4) ----------------
-    const int quad = warp & 3, g = (warp - 2) >> 2;   // g: which half of the keys / of O's columns
+    // ---------------- softmax (warps 2..5, a thread per row) and the output tile (2..9) ----------------
+    const int quad = warp & 3, g = (warp - 2) >> 2;   // g: which half of O's columns the warp stages
     const int row = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     constexpr int OH = DH / 2;                          // O columns per half
     const float sl2 = rsqrtf((float)DH) * 1.4426950408889634f;
-    // the two threads of a row swap a value through shared memory; exchange e
-    // uses parity e & 1 of this quadrant's barrier pair (64 arrivals, bounded wait)
-    auto exchange = [&](int e, float mine) -> float {
-      const int par = e & 1;
-      xm[(par * 2 + g) * ROWS + row] = mine;
-      ptx::mbar_arrive(&x_bar[quad * 2 + par]);
-      if (!ptx::mbar_wait(&x_bar[quad * 2 + par], (e >> 1) & 1, lim)) fail();
-      return xm[(par * 2 + (g ^ 1)) * ROWS + row];
-    };
     ptx::pdl_wait();
-    float m_used = -INFINITY, l = 0.f;   // l: this thread's half of the row sum
-    for (int j = 0; j < nt; ++j) {
-      const int sb = j & 1;
-      if (!ptx::mbar_wait(&s_full[sb], (j >> 1) & 1, lim)) { fail(); break; }
-      ptx::tc_fence_after();
-      float sv[32];
-      ptx::tmem_ld32(tS + sb * KT + 32 * g + lane_off, sv);
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s_empty[sb]);
-      const int valid = key_tile(t_begin + j, b, a.P, a.H).valid - 32 * g;   // keys of this half in range
-      // half-tile maximum of the raw scores (4 independent chains); keys past the tile end masked
-      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    float m_used = -INFINITY, l = 0.f;
+    if (g == 0) {
+      for (int j = 0; j < nt; ++j) {
+        const int sb = j % 3;
+        if (!ptx::mbar_wait(&s_full[sb], (j / 3) & 1, lim)) { fail(); break; }
+        ptx::tc_fence_after();
+        float sv[KT];
+        ptx::tmem_ld32(tS + sb * KT + lane_off, *reinterpret_cast<float(*)[32]>(sv));
+        ptx::tmem_ld32(tS + sb * KT + 32 + lane_off, *reinterpret_cast<float(*)[32]>(sv + 32));
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&s_empty[sb]);
+        const int valid = key_tile(t_begin + j, b, a.P, a.H).valid;   // keys of the tile in range
+        // tile maximum of the raw scores (4 independent chains); keys past the tile end masked
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        if (c >= valid) sv[c] = -INFINITY;
-        mq[c & 3] = fmaxf(mq[c & 3], sv[c]);
-      }
-      const float mh = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
-      const float mt = fmaxf(mh, exchange(j, mh));
-      // raise the running maximum only when this tile exceeds it by more than 2^8
-      const bool raise = mt > m_used + 8.f;
-      const float m_new = raise ? mt : m_used;
-      const float corr = raise ? ex2_approx(m_used - m_new) : 1.f;   // 0 on the first tile
-      float pq[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        // p = 2^(s * log2e / sqrt(d) - m): the scale folded into one fma
-        const float p0 = ex2_approx(fmaf(sv[c], sl2, -m_new));
-        const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, -m_new));
-        pq[(c >> 1) & 3] += p0 + p1;
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-        pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h2);
-      }
-      l = l * corr + ((pq[0] + pq[1]) + (pq[2] + pq[3]));
-      const int pb = j & 1;
-      // P buffer pb is free once PV(j-2) has completed
-      if (j >= 2 && !ptx::mbar_wait(&pv_done[pb], ((j - 2) >> 1) & 1, lim)) { fail(); break; }
-      const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);   // same in both warps of the rows
-      // O is stable once PV(j-1) has completed: needed only to rescale it
-      if (rescale && !ptx::mbar_wait(&pv_done[pb ^ 1], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
-      ptx::tc_fence_after();
-      if (rescale) {  // rescale this warp's half of its O rows in TMEM
-#pragma unroll 1
-        for (int c0 = g * OH; c0 < g * OH + OH; c0 += 32) {
-          float o[32];
-          ptx::tmem_ld32(tO + c0 + lane_off, o);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] *= corr;
-          tmem_st32(tO + c0 + lane_off, o);
+        for (int c = 0; c < KT; ++c) {
+          if (c >= valid) sv[c] = -INFINITY;
+          mq[c & 3] = fmaxf(mq[c & 3], sv[c]);
         }
-      }
-      m_used = m_new;
-      // this half of the P row -> shared memory, K-major 128-byte swizzled (chunk c at c ^ (row % 8))
-      uint4* prow = reinterpret_cast<uint4*>(sP + pb * L::P_BYTES + row * 128);
+        const float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
+        // raise the running maximum only when this tile exceeds it by more than 2^8
+        const bool raise = mt > m_used + 8.f;
+        const float m_new = raise ? mt : m_used;
+        const float corr = raise ? ex2_approx(m_used - m_new) : 1.f;   // 0 on the first tile
+        float pq[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pk[KT / 2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        prow[(4 * g + c) ^ (row & 7)] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&p_full[pb]);
+        for (int c = 0; c < KT; c += 2) {
+          // p = 2^(s * log2e / sqrt(d) - m): the scale folded into one fma
+          const float p0 = ex2_approx(fmaf(sv[c], sl2, -m_new));
+          const float p1 = ex2_approx(fmaf(sv[c + 1], sl2, -m_new));
+          pq[(c >> 1) & 3] += p0 + p1;
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);   // key c in the low half
+          pk[c >> 1] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        l = l * corr + ((pq[0] + pq[1]) + (pq[2] + pq[3]));
+        const int pb = j & 1;
+        // P buffer pb is free once PV(j-2) has completed
+        if (j >= 2 && !ptx::mbar_wait(&pv_done[pb], ((j - 2) >> 1) & 1, lim)) { fail(); break; }
+        const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
+        // O is stable once PV(j-1) has completed: needed only to rescale it
+        if (rescale && !ptx::mbar_wait(&pv_done[pb ^ 1], ((j - 1) >> 1) & 1, lim)) { fail(); break; }
+        ptx::tc_fence_after();
+        if (rescale) {  // rescale this thread's O row in TMEM (corr = 1 on rows that did not raise)
+#pragma unroll 1
+          for (int c0 = 0; c0 < DH; c0 += 32) {
+            float o[32];
+            ptx::tmem_ld32(tO + c0 + lane_off, o);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] *= corr;
+            tmem_st32(tO + c0 + lane_off, o);
+          }
+        }
+        m_used = m_new;
+        ptx::tmem_st32u(tP + pb * (KT / 2) + lane_off, pk);   // P row: column c = keys 2c, 2c + 1
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&p_full[pb]);
+      }
+      // the last PV (it follows every earlier one on the tensor pipe)
+      if (nt > 0 && !*abort_flag && !ptx::mbar_wait(&pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, lim)) fail();
+      xm[row] = l;
+      xm[ROWS + row] = m_used;
     }
-    // the last PV (it follows every earlier one on the tensor pipe)
-    if (nt > 0 && !*abort_flag && !ptx::mbar_wait(&pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, lim)) fail();
+    asm volatile("bar.sync 1, 256;" ::: "memory");   // the rows' (sum, max) are in shared memory
     ptx::tc_fence_after();
-    l += exchange(nt, l);   // the whole row's sum (both halves add the same two numbers)
+    l = xm[row];
+    m_used = xm[ROWS + row];
     const bool aborted = *abort_flag != 0;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     long long slot = 0;
@@ -500,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (CT > 1) ptx::cluster_sync_all();   // no copy or release targets a CTA that has left
   if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
@@ -575,8 +638,22 @@ cudaError_t launch_t5(const AttnT5Args& a, const CUtensorMap* maps, int S, cudaS
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  cudaError_t e = launch_k(kern, dim3((a.Hq * a.H + ROWS - 1) / ROWS, S, a.B), dim3(kThreads), L::TOTAL, s, pdl,
-                           maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7], a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((a.Hq * a.H + ROWS - 1) / ROWS, S, a.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::TOTAL;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = a.ct > 1 ? a.ct : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.ct > 1 ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
+                                     maps[7], a);
   if (e != cudaSuccess || S == 1) return e;
   const long long warps = (long long)a.B * a.Hq * a.H;
   return launch_k(attn_t5_combine_kernel<DH>, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s, pdl, a, S);
@@ -602,6 +679,14 @@ cudaError_t encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* 
 }  // namespace
 
 bool attn_t5_supported(int Dh, int Hq) { return (Dh == 64 || Dh == 128 || Dh == 256) && Hq > 0 && ROWS % Hq == 0; }
+
+int attn_t5_cluster(const AttnT5Args& a) {
+  // the row tiles of a sample as one cluster when there are 2 or 4 of them and the
+  // Dh/64 column boxes of a key tile split evenly between them
+  const int tiles_x = (a.Hq * a.H + ROWS - 1) / ROWS;
+  const int boxes = a.Dh / 64;
+  return (tiles_x == 2 || tiles_x == 4) && boxes % tiles_x == 0 ? tiles_x : 1;
+}
 
 int attn_t5_splits(const AttnT5Args& a, int sm_count, int cap) {
   // at most one CTA per SM and kMaxSplits (or cap) splits; then as few splits as keep
@@ -639,10 +724,12 @@ cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, in
   const cuuint32_t qb[4] = {64, (cuuint32_t)a.Hq, (cuuint32_t)(ROWS / a.Hq), nbox};
   cudaError_t e = encode(&maps[0], a.qkv, 4, qd, qs, qb);
   if (e != cudaSuccess) return e;
-  // K / V tiles: box = one 64-key tile of all Dh/64 column boxes.  Prefix: (64 columns, P rows,
-  // B samples ps rows apart -- ps = P, or a pool's capacity -- Dh/64 boxes)
-  const cuuint32_t kb[3] = {64, KT, nbox};
-  const cuuint32_t kb4[4] = {64, KT, 1, nbox};
+  // K / V tiles: box = one 64-key tile of all Dh/64 column boxes (in a cluster of ct row
+  // tiles: 1/ct of them, each CTA's part).  Prefix: (64 columns, P rows, B samples ps rows
+  // apart -- ps = P, or a pool's capacity -- Dh/64 boxes)
+  const cuuint32_t part = nbox / (cuuint32_t)(a.ct > 1 ? a.ct : 1);
+  const cuuint32_t kb[3] = {64, KT, part};
+  const cuuint32_t kb4[4] = {64, KT, 1, part};
   const long long prows = a.P > 0 ? a.P : 1, pstride = a.ps > 0 ? a.ps : prows;
   const cuuint64_t pd[4] = {64, (cuuint64_t)prows, (cuuint64_t)a.B, nbox};
   const cuuint64_t ps[3] = {(cuuint64_t)D * 2, (cuuint64_t)pstride * D * 2, 128};

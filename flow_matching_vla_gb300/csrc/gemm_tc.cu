@@ -211,7 +211,8 @@ __device__ __forceinline__ void tile_epilogue(const Epi& e, uint32_t taddr, int 
   }
 }
 
-constexpr int kThreads = 256;  // 8 warps: warp 0 TMA, warp 1 MMA, all 8 share the epilogue
+constexpr int kThreads = 256;  // 8 warps: warps 0 and 3 TMA, warp 1 MMA, all 8 share the epilogue
+constexpr long long kDrainPolls = 1LL << 22;   // bounded wait for a CTA's own copies after an abort
 
 // Memory later kernels read, to be pulled into L2 while this kernel runs.
 struct L2Ahead {
@@ -254,27 +255,6 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint32_t (&o)[8
       o[2 * i + h] = *reinterpret_cast<uint32_t*>(&b);
     }
   }
-}
-
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-      "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-// D (+)= A B^T with A (M = 128 rows, K = 16) read from tensor memory.
-__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((int)accumulate)
-      : "memory");
 }
 
 template <int BN, int STAGES, int WF>
@@ -345,7 +325,7 @@ __device__ __forceinline__ void ta_main_loop(const CUtensorMap& tmW, const CUten
 #pragma unroll
         for (int k = 0; k < BKX / 16; ++k) {   // 8 columns (16 K elements) of A per step; B: 64-column boxes
           const uint64_t bd = ptx::sdesc_sw128(ptx::smem_u32(sB + s * L::B_BYTES + (k >> 2) * (BN * 128)));
-          mma_bf16_ta(tmem, ta + 8 * k, bd + 2 * (k & 3), idesc, (i | k) != 0);
+          ptx::mma_bf16_tmem_a(tmem, ta + 8 * k, bd + 2 * (k & 3), idesc, (i | k) != 0);
         }
         ptx::mma_commit(&empty[s]);
       }
@@ -376,9 +356,8 @@ __device__ __forceinline__ void ta_main_loop(const CUtensorMap& tmW, const CUten
 #pragma unroll
         for (int j = 0; j < 8; ++j) a[8 * c + j] = o[j];
       }
-      tmem_st32u(ta, a);
-      tmem_st32u(ta + 32, a + 32);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      ptx::tmem_st32u(ta, a);
+      ptx::tmem_st32u(ta + 32, a + 32);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -422,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&full[s], TA ? 1 : 2);   // bf16 weights: the weight and the activation producer arrive
       ptx::mbar_init(&empty[s], 1);
     }
     ptx::mbar_init(done, 1);
@@ -452,38 +431,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (TA) {
     ta_main_loop<BN, STAGES, WF>(tmW, tmX, sA, sB, sRaw, full, empty, done, cvt_full, raw_full, raw_empty, tmem,
                              abort_flag, err, wait_limit, n0, m0, kb0, nkb, warp, lane);
-  } else if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pw = ptx::policy_evict_first(), px = ptx::policy_evict_last();
-      // weights first: no earlier kernel writes them, so they stream before the dependency wait
-      const int pre = nkb < STAGES ? nkb : STAGES;
-      for (int i = 0; i < pre; ++i) {
-        ptx::mbar_arrive_expect_tx(&full[i], L::STAGE_BYTES);
-        ptx::tma_load_2d(sA + i * L::A_STAGE, &tmW, &full[i], (kb0 + i) * BK, n0, pw);
-      }
+  } else if ((warp == 0 || warp == 3) && lane == 0) {
+    // two producers, each with its own stream of TMA requests (a thread's requests are
+    // served one after another): warp 0 the weight tiles -- no kernel writes weights, so
+    // they need no dependency wait and run ahead of it -- and warp 3 the activation tiles
+    // after the wait.  Each arrives on the stage's full barrier with its own bytes.
+    const bool wprod = warp == 0;
+    if (!wprod) {
       ptx::pdl_wait();
-      int issued = pre;
-      bool ok = true;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % STAGES;
-        if (i >= STAGES) {
-          if (!ptx::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, wait_limit)) {
-            ok = false;
-            break;
-          }
-          ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
-          ptx::tma_load_2d(sA + s * L::A_STAGE, &tmW, &full[s], (kb0 + i) * BK, n0, pw);
-          issued = i + 1;
-        }
-        ptx::tma_load_2d(sB + s * L::B_BYTES, &tmX, &full[s], (kb0 + i) * BK, m0, px);
-      }
-      if (!ok) {
+      kstamp(e.ts);
+    }
+    const uint64_t pol = wprod ? ptx::policy_evict_first() : ptx::policy_evict_last();
+    const uint32_t bytes = wprod ? (uint32_t)L::A_STAGE : (uint32_t)L::B_BYTES;
+    int issued = 0;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % STAGES;
+      if (i >= STAGES && !ptx::mbar_wait(&empty[s], ((i / STAGES) & 1) ^ 1, wait_limit)) {
         atomicExch(abort_flag, 1);
         atomicExch(err, 1);
-        // drain: wait (bounded) for the copies this thread armed last on each stage
-        for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
-          ptx::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, wait_limit);
+        break;
       }
+      if (*(volatile int*)abort_flag) break;
+      ptx::mbar_arrive_expect_tx(&full[s], bytes);
+      if (wprod)
+        ptx::tma_load_2d(sA + s * L::A_STAGE, &tmW, &full[s], (kb0 + i) * BK, n0, pol);
+      else
+        ptx::tma_load_2d(sB + s * L::B_BYTES, &tmX, &full[s], (kb0 + i) * BK, m0, pol);
+      issued = i + 1;
+    }
+    if (*(volatile int*)abort_flag) {
+      // drain: wait (bounded) for the stages this thread armed last, whose copies may be in flight
+      const long long drain = wait_limit > kDrainPolls ? wait_limit : kDrainPolls;
+      for (int i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
+        ptx::mbar_wait(&full[i % STAGES], (i / STAGES) & 1, drain);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -507,10 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncwarp();
-  // every thread but the producer (which waited before its activation loads)
-  // waits for the previous kernel before touching activation memory
-  if (TA || threadIdx.x != 0) ptx::pdl_wait();
-  if (threadIdx.x == 96) kstamp(e.ts);   // warp 3 has no main-loop role on either weight path
+  // every thread waits for the previous kernel before touching activation memory
+  ptx::pdl_wait();
+  if (TA && threadIdx.x == 96) kstamp(e.ts);   // warp 3 has no main-loop role on the E4M3 path
 
   if (!ptx::mbar_wait(done, 0, wait_limit)) {
     atomicExch(abort_flag, 1);
@@ -656,13 +635,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // Persistent variant for many tiles (large token counts): one CTA per SM walks
-// the tiles; warp 0 streams TMA stages continuously across tiles, warp 1
-// issues the MMAs into one of two TMEM accumulators (2 x BN columns), and
-// warps 2..9 drain the other accumulator through the epilogue, so the
-// epilogue of tile i overlaps the main loop of tile i + 1.  Tiles are ordered
-// token-tile fastest: concurrently running CTAs share weight tiles in L2.
+// the tiles; warp 0 streams the weight tiles and warp 10 the activation tiles
+// continuously across tiles (two TMA request streams), warp 1 issues the MMAs
+// into one of two TMEM accumulators (2 x BN columns), and warps 2..9 drain the
+// other accumulator through the epilogue, so the epilogue of tile i overlaps
+// the main loop of tile i + 1.  Tiles are ordered token-tile fastest:
+// concurrently running CTAs share weight tiles in L2.
+//
+// CL = 2: the CTAs run as clusters of two over adjacent weight tiles of the
+// same token tile.  Each loads its own weight tile and one half of the shared
+// activation tile, multicast into both CTAs' shared memory, so the L2 serves
+// each activation tile once per pair (a third less L2 traffic per MMA).  A
+// stage's slot is refilled only once both CTAs' MMAs released it (each MMA
+// warp arrives on both CTAs' empty barriers).
 // ---------------------------------------------------------------------------
-constexpr int kPersThreads = 320;
+constexpr int kPersThreads = 352;   // warp 0 weight TMA, 1 MMA, 2..9 epilogue, 10 activation TMA
+constexpr int kPersEpiWarps = 8;
 
 template <int BN, int STAGES>
 struct PersSmem {
@@ -673,7 +661,7 @@ struct PersSmem {
   static constexpr int TOTAL = PIPE + BAR + 1024;
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CL>
 __global__ void __launch_bounds__(kPersThreads, 1)
     gemm_tc_persistent(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
                        int N, int KB, Epi e, int* err, long long wait_limit) {
@@ -691,13 +679,20 @@ __global__ void __launch_bounds__(kPersThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mt = (M + BN - 1) / BN;
-  const int tiles = ((N + BM - 1) / BM) * mt;
-  constexpr int kEpiWarps = kPersThreads / 32 - 2;
+  const int nt_pairs = ((N + BM - 1) / BM + CL - 1) / CL;   // groups of CL adjacent weight tiles
+  const int ptiles = nt_pairs * mt;
+  const int rank = CL > 1 ? (int)(blockIdx.x % CL) : 0;   // rank in the cluster (clusters of consecutive CTAs)
+  const int cid = (int)blockIdx.x / CL, ncl = (int)gridDim.x / CL;
+  constexpr int kEpiWarps = kPersEpiWarps;
+  constexpr uint16_t kAll = (uint16_t)((1u << CL) - 1);
+  // tile p of this cluster: weight rows n0 (this CTA's of the group), tokens m0
+  auto tile_n0 = [&](int p) { return ((p / mt) * CL + rank) * BM; };
+  auto tile_m0 = [&](int p) { return (p % mt) * BN; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&full[s], 2);    // the weight and the activation producer arrive
+      ptx::mbar_init(&empty[s], CL);  // every CTA's MMA warp of the cluster releases the slot
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&tfull[b], 1);
@@ -712,6 +707,7 @@ __global__ void __launch_bounds__(kPersThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  if (CL > 1) ptx::cluster_sync_all();   // the peer's barriers exist before anything targets them
   const uint32_t tmem = *tmem_slot;
   ptx::pdl_launch_dependents();
 
@@ -719,44 +715,54 @@ __global__ void __launch_bounds__(kPersThreads, 1)
     *abort_flag = 1;
     atomicExch(err, 1);
   };
+  long long stages_used = 0;   // weight producer: stage uses issued (for the final release wait)
 
-  if (warp == 0) {
-    if (lane == 0) {
-      const uint64_t pw = ptx::policy_evict_first(), px = ptx::policy_evict_last();
-      const int t0 = blockIdx.x;
-      const int pre = (t0 < tiles) ? (KB < STAGES ? KB : STAGES) : 0;
-      for (int i = 0; i < pre; ++i) {  // first tile's weights before the dependency wait
-        ptx::mbar_arrive_expect_tx(&full[i], L::STAGE_BYTES);
-        ptx::tma_load_2d(sA + i * A_BYTES, &tmW, &full[i], i * BK, (t0 / mt) * BM, pw);
-      }
+  if ((warp == 0 || warp == 10) && lane == 0) {
+    // two producers with their own TMA request streams (a thread's requests are served
+    // one after another): warp 0 the weight tiles, which no kernel writes, so they run
+    // ahead of the dependency wait; warp 10 the activation tiles (this CTA's 1/CL of
+    // each, multicast to the cluster) after it
+    const bool wprod = warp == 0;
+    if (!wprod) {
       ptx::pdl_wait();
-      long long it = 0, issued = pre;
-      for (int t = t0; t < tiles && !*abort_flag; t += gridDim.x) {
-        const int n0 = (t / mt) * BM, m0 = (t % mt) * BN;
-        for (int kb = 0; kb < KB; ++kb, ++it) {
-          const int s = (int)(it % STAGES);
-          if (!(t == t0 && kb < pre)) {
-            if (it >= STAGES && !ptx::mbar_wait(&empty[s], (uint32_t)(((it / STAGES) & 1) ^ 1), wait_limit)) {
-              fail();
-              break;
-            }
-            ptx::mbar_arrive_expect_tx(&full[s], L::STAGE_BYTES);
-            ptx::tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], kb * BK, n0, pw);
-            issued = it + 1;
-          }
-          ptx::tma_load_2d(sB + s * L::B_BYTES, &tmX, &full[s], kb * BK, m0, px);
-        }
-      }
-      if (*abort_flag)  // drain this thread's in-flight copies (bounded)
-        for (long long i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
-          ptx::mbar_wait(&full[i % STAGES], (uint32_t)((i / STAGES) & 1), wait_limit);
+      kstamp(e.ts);
     }
+    const uint64_t pol = wprod ? ptx::policy_evict_first() : ptx::policy_evict_last();
+    const uint32_t bytes = wprod ? (uint32_t)A_BYTES : (uint32_t)L::B_BYTES;   // B: all CL parts land here
+    long long it = 0, issued = 0;
+    for (int p = cid; p < ptiles && !*abort_flag; p += ncl) {
+      const int n0 = tile_n0(p), m0 = tile_m0(p);
+      for (int kb = 0; kb < KB; ++kb, ++it) {
+        const int s = (int)(it % STAGES);
+        if (it >= STAGES && !ptx::mbar_wait(&empty[s], (uint32_t)(((it / STAGES) & 1) ^ 1), wait_limit)) {
+          fail();
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(&full[s], bytes);
+        if (wprod) {
+          ptx::tma_load_2d(sA + s * A_BYTES, &tmW, &full[s], kb * BK, n0, pol);
+        } else if (CL == 1) {
+          ptx::tma_load_2d(sB + s * L::B_BYTES, &tmX, &full[s], kb * BK, m0, pol);
+        } else {
+          constexpr int HB = BN / CL;   // rows of this CTA's part (the map's box)
+          ptx::tma_load_2d_mc(sB + s * L::B_BYTES + rank * HB * 128, &tmX, &full[s], kb * BK, m0 + rank * HB, kAll,
+                              pol);
+        }
+        issued = it + 1;
+      }
+    }
+    if (*abort_flag) {  // drain the copies into this CTA (bounded)
+      const long long drain = wait_limit > kDrainPolls ? wait_limit : kDrainPolls;
+      for (long long i = issued - 1; i >= 0 && i >= issued - STAGES; --i)
+        ptx::mbar_wait(&full[i % STAGES], (uint32_t)((i / STAGES) & 1), drain);
+    }
+    stages_used = it;
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = ptx::idesc_bf16(BM, BN);
       long long it = 0;
       int lt = 0;
-      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++lt) {
+      for (int p = cid; p < ptiles && !*abort_flag; p += ncl, ++lt) {
         const int b = lt & 1;
         if (lt >= 2 && !ptx::mbar_wait(&tempty[b], (uint32_t)(((lt >> 1) & 1) ^ 1), wait_limit)) {
           fail();
@@ -777,15 +783,17 @@ __global__ void __launch_bounds__(kPersThreads, 1)
           const uint64_t bd = ptx::sdesc_sw128(ptx::smem_u32(sB + s * L::B_BYTES));
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) ptx::mma_bf16(d, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0);
-          ptx::mma_commit(&empty[s]);
+          if (CL == 1)
+            ptx::mma_commit(&empty[s]);
+          else
+            ptx::mma_commit_mc(&empty[s], kAll);
         }
         ptx::mma_commit(&tfull[b]);
         if (!ok) break;
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 2 + kEpiWarps) {
     ptx::pdl_wait();
-    if (threadIdx.x == 64) kstamp(e.ts);
     const int ew = warp - 2;
     const int quad = warp & 3;
     const int c_begin = (ew >> 2) * (BN / 2), c_end = c_begin + BN / 2;
@@ -796,7 +804,7 @@ __global__ void __launch_bounds__(kPersThreads, 1)
       // no token in range (M = 0: nothing is stored).  The epilogue code runs
       // once per tile on a cold instruction cache otherwise (measured: the
       // first 32 columns of a tile took ~2.5 us longer than the next ones).
-      const int n_even = (blockIdx.x < tiles ? (blockIdx.x / mt) * BM : 0) + quad * 32 + (lane & ~1);
+      const int n_even = (cid < ptiles ? tile_n0(cid) : 0) + quad * 32 + (lane & ~1);
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)BN;
       switch (e.kind) {
         case EPI_STORE:
@@ -813,7 +821,7 @@ __global__ void __launch_bounds__(kPersThreads, 1)
       }
     }
     int lt = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++lt) {
+    for (int p = cid; p < ptiles; p += ncl, ++lt) {
       const int b = lt & 1;
       if (!ptx::mbar_wait(&tfull[b], (uint32_t)((lt >> 1) & 1), wait_limit)) {
         fail();
@@ -821,7 +829,7 @@ __global__ void __launch_bounds__(kPersThreads, 1)
       }
       ptx::tc_fence_after();
       if (*abort_flag) break;
-      const int n0 = (t / mt) * BM, m0 = (t % mt) * BN;
+      const int n0 = tile_n0(p), m0 = tile_m0(p);
       const int n_even = n0 + quad * 32 + (lane & ~1);
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN);
       switch (e.kind) {
@@ -842,36 +850,49 @@ __global__ void __launch_bounds__(kPersThreads, 1)
       if (lane == 0) ptx::mbar_arrive(&tempty[b]);
     }
   }
+  if (CL > 1 && warp == 0 && lane == 0) {
+    // every release of this CTA's slots (its own MMA warp's and the peer's) has arrived:
+    // after this no MMA warp of the cluster signals this CTA's barriers any more
+    const long long drain = wait_limit > kDrainPolls ? wait_limit : kDrainPolls;
+    for (long long i = stages_used - 1; i >= 0 && i >= stages_used - STAGES; --i)
+      ptx::mbar_wait(&empty[i % STAGES], (uint32_t)((i / STAGES) & 1), drain);
+  }
   ptx::tc_fence_before();
   __syncthreads();
+  if (CL > 1) ptx::cluster_sync_all();   // no copy or release targets a CTA that has left
   if (warp == 2) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 2 * BN);
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int CL>
 cudaError_t launch_persistent(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int sm_count,
                               int* err, long long lim, cudaStream_t s, bool pdl) {
   using L = PersSmem<BN, STAGES>;
-  auto kern = gemm_tc_persistent<BN, STAGES>;
+  auto kern = gemm_tc_persistent<BN, STAGES, CL>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e1 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
     if (e1 != cudaSuccess) return e1;
     configured = true;
   }
-  const int tiles = ((a.N + BM - 1) / BM) * ((a.M + BN - 1) / BN);
+  const int ptiles = (((a.N + BM - 1) / BM + CL - 1) / CL) * ((a.M + BN - 1) / BN);
+  const int clusters = ptiles < sm_count / CL ? ptiles : sm_count / CL;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles < sm_count ? tiles : sm_count);
+  cfg.gridDim = dim3(clusters * CL);
   cfg.blockDim = dim3(kPersThreads);
   cfg.dynamicSmemBytes = L::TOTAL;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, a.K / BK, a.epi, err, lim);
 }
 
@@ -1048,8 +1069,12 @@ cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& 
                                       cudaStream_t s, bool pdl) {
   if (!tc_supported(a.M, a.N, a.K) || p.S != 1) return cudaErrorInvalidValue;
   switch (p.BN) {
-    case 128: return launch_persistent<128, 6>(tw, tx, a, sm_count, err, wait_limit, s, pdl);
-    case 256: return launch_persistent<256, 4>(tw, tx, a, sm_count, err, wait_limit, s, pdl);
+    case 128:
+      return p.CL == 2 ? launch_persistent<128, 6, 2>(tw, tx, a, sm_count, err, wait_limit, s, pdl)
+                       : launch_persistent<128, 6, 1>(tw, tx, a, sm_count, err, wait_limit, s, pdl);
+    case 256:
+      return p.CL == 2 ? launch_persistent<256, 4, 2>(tw, tx, a, sm_count, err, wait_limit, s, pdl)
+                       : launch_persistent<256, 4, 1>(tw, tx, a, sm_count, err, wait_limit, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -11,6 +11,8 @@ namespace g3 {
 struct TcPlan {
   int BN = 64;  // token columns per CTA (MMA N): 64, 128 or 256
   int S = 1;    // split-K factor = cluster size along K (power of two, <= 16)
+  int CL = 1;   // persistent kernel: CTAs per cluster sharing each activation tile by multicast (1 or 2);
+                // its activation map's box is BN / CL rows
 };
 
 // K-major bf16 tensor map over a [rows][cols] matrix with leading dimension
@@ -38,7 +40,9 @@ cudaError_t gemm_tc_e4m3(const CUtensorMap& tw, const CUtensorMap& tx, const Gem
                          float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl);
 
 // Large token counts (no split, M > 64): persistent CTAs with a double-buffered
-// TMEM accumulator so each tile's epilogue overlaps the next tile's MMAs.
+// TMEM accumulator so each tile's epilogue overlaps the next tile's MMAs;
+// with plan.CL = 2, clusters of two CTAs over adjacent weight tiles share each
+// activation tile by TMA multicast (X map box: BN / 2 rows).
 bool tc_use_persistent(const TcPlan& p, int M);
 cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a,
                                       const TcPlan& p, int sm_count, int* err, long long wait_limit,

@@ -162,6 +162,7 @@ struct AttnT5Args {
   void* pool_k = nullptr;     // a bound pool's K and V planes: this step's suffix K/V go to
   void* pool_v = nullptr;     // rows [P, P + H) of each sample's slot (nullptr: no pool)
   int pool_cap = 0;
+  int ct = 1;                 // CTAs per cluster sharing every key tile by multicast (attn_t5_cluster)
   unsigned long long* ts = nullptr;    // dependency-release stamp of the main kernel (nullable)
   unsigned long long* ts2 = nullptr;   // ... and of the split merge (nullable)
 };
@@ -170,6 +171,7 @@ struct AttnT5Args {
 namespace g3 {
 bool attn_t5_supported(int Dh, int Hq);
 int attn_t5_splits(const AttnT5Args& a, int sm_count, int cap = 0);   // cap > 0: at most cap splits
+int attn_t5_cluster(const AttnT5Args& a);   // the cluster size for a.ct (1: no multicast)
 long long attn_t5_workspace_floats(const AttnT5Args& a, int S);
 // maps[8]: Q, prefix K, prefix V, suffix K, suffix V, the output tile (S: the key splits), pool K, pool V
 cudaError_t attn_t5_maps(const AttnT5Args& a, const void* kp, const void* vp, int S, CUtensorMap* maps);

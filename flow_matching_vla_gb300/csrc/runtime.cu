@@ -102,6 +102,8 @@ struct gr00t_ctx {
   int opt_pdl = 1;
   int opt_attn_splits = 0;  // expert attention key-split cap (0: automatic)
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
+  int opt_mcast = 1;        // persistent GEMM: pairs of CTAs share activation tiles by TMA multicast
+  int opt_attn_mcast = 1;   // expert attention: the row tiles of a sample share key tiles by TMA multicast
   int opt_l2_ahead = 0;     // each layer's first GEMM prefetches the next layer into L2 (off: measured slower)
   long long noalloc_limit = -1;   // scratch bound of the allocation-free step (-1: the whole fixed array)
   int split_cap = 4;        // GEMMs that reduce their split-K partials in-kernel
@@ -573,11 +575,14 @@ int gemm(gr00t_ctx* c, GemmArgs a, int cls = GR00T_KCLASS_OTHER) {
   }
   if (c->dt == DT_BF16 && c->opt_gemm == 0 && tc_supported(a.M, a.N, a.K)) {
     const bool partial = a.epi.kind == EPI_PARTIAL;
-    const TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, partial ? c->resid_split_cap : c->split_cap, partial);
+    TcPlan p = tc_plan(a.M, a.N, a.K, c->sm_count, partial ? c->resid_split_cap : c->split_cap, partial);
+    const bool pers = c->opt_persistent && tc_use_persistent(p, a.M);
+    // persistent tiles over two or more weight tiles: pairs of CTAs share each activation tile
+    if (pers && c->opt_mcast && (a.N + 127) / 128 >= 2) p.CL = 2;
     const CUtensorMap* tw = tmap(c, a.W, a.N, a.K, a.ldw, 128);
-    const CUtensorMap* tx = tmap(c, a.A, a.M, a.K, a.lda, p.BN);
+    const CUtensorMap* tx = tmap(c, a.A, a.M, a.K, a.lda, p.BN / p.CL);
     if (!tw || !tx) return set_err(c, GR00T_ECUDA, "TMA descriptor encode failed (alignment?)");
-    if (c->opt_persistent && tc_use_persistent(p, a.M))
+    if (pers)
       CK(c, gemm_tc_persistent_launch(*tw, *tx, a, p, c->sm_count, c->err_flag, c->wait_limit, c->stream,
                                       c->opt_pdl != 0));
     else
@@ -733,6 +738,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
           a5.pool_k = c->pool[l];
           a5.pool_v = (char*)c->pool[l] + (size_t)B * c->pool_cap * c->Dh * es;
         }
+        a5.ct = c->opt_attn_mcast ? attn_t5_cluster(a5) : 1;
         CUtensorMap maps[8];
         CK(c, attn_t5_maps(a5, c->host_table[2 * l], c->host_table[2 * l + 1], splits, maps));
         a5.ts = next_ts(c, GR00T_KCLASS_ATTENTION);
@@ -1326,6 +1332,12 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
       break;
     case GR00T_OPT_PERSISTENT_GEMM:
       c->opt_persistent = value ? 1 : 0;
+      break;
+    case GR00T_OPT_GEMM_MULTICAST:
+      c->opt_mcast = value ? 1 : 0;
+      break;
+    case GR00T_OPT_ATTN_MULTICAST:
+      c->opt_attn_mcast = value ? 1 : 0;
       break;
     case GR00T_OPT_L2_PREFETCH:
       c->opt_l2_ahead = value ? 1 : 0;

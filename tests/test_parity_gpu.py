@@ -188,6 +188,23 @@ def test_expert_attention_paths(path, kw):
     check_case(synth.make_case("small_bf16", **kw), options=[(fmv.OPT_ATTN_PATH, path)])
 
 
+# key tiles shared by the row tiles of a sample through cluster multicast: 2 row tiles
+# (2 heads x 100 tokens) and 4 (4 heads x 100 tokens); the data movement must not change
+# a single bit of the result
+@pytest.mark.parametrize("kw", [dict(q_heads=2, horizon=100, batch=2, prefix=300),
+                                dict(q_heads=4, horizon=100, batch=2, prefix=700)])
+def test_attention_key_tile_multicast(kw):
+    fmv = _fmv()
+    case = synth.make_case("small_bf16", **kw)
+    loop, _, _, _ = check_case(case)
+    x0 = torch.from_numpy(case["x_noise"]).cuda()
+    a = loop.denoise(x0).clone()
+    loop.set_option(fmv.OPT_ATTN_MULTICAST, 0)
+    b = loop.denoise(x0).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
 def test_tcgen05_attention_head_dim_64():
     fmv = _fmv()
     c = synth.make_case("small_bf16", q_heads=4, head_dim=64, batch=4, prefix=150)
@@ -295,9 +312,9 @@ def test_bind_context_refused_without_context_dim():
 # the pages' plane-major paged K/V pool bound directly: [2, B, capacity, 1, Dh]
 # per layer, prefix in slot rows [0, P), every step's action K/V appended into
 # rows [P, P + H); the filler rows must neither be read nor overwritten
-def _pool_case(capacity=384):
+def _pool_case(capacity=384, **kw):
     import torch
-    case = synth.make_case("small_bf16", batch=2, prefix=200)
+    case = synth.make_case("small_bf16", **dict(dict(batch=2, prefix=200), **kw))
     g = case["geom"]
     B, P, Dh = g["batch"], g["prefix"], g["head_dim"]
     pools = []
@@ -309,10 +326,13 @@ def _pool_case(capacity=384):
     return case, pools
 
 
-def test_expert_paged_kv_pool_parity():
+# the second case runs the attention's row tiles as a 4-CTA multicast cluster (4 heads x
+# 100 tokens), with the first row tile's CTA also storing the suffix K/V into the pool
+@pytest.mark.parametrize("kw", [dict(), dict(q_heads=4, horizon=100)])
+def test_expert_paged_kv_pool_parity(kw):
     import torch
     fmv = _fmv()
-    case, pools = _pool_case()
+    case, pools = _pool_case(**kw)
     g = case["geom"]
     B, P, H = g["batch"], g["prefix"], g["horizon"]
     keep = [p.clone() for p in pools]
