@@ -219,6 +219,21 @@ struct L2Ahead {
   const void* p[3];
   long long bytes[3];
 };
+// This CTA's share of each range, 128-byte lines spread over ``nthreads`` threads (t < nthreads).
+__device__ __forceinline__ void prefetch_lines_l2(const L2Ahead& ah, int t, int nthreads) {
+  const long long ctas = (long long)gridDim.x * gridDim.y * gridDim.z;
+  const long long cta = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+#pragma unroll 1
+  for (int i = 0; i < 3; ++i) {
+    if (!ah.p[i] || ah.bytes[i] < 128) continue;
+    const long long lines = ah.bytes[i] / 128;
+    const long long per = (lines + ctas - 1) / ctas;
+    const long long l0 = cta * per, l1 = l0 + per < lines ? l0 + per : lines;
+    const char* base = static_cast<const char*>(ah.p[i]);
+    for (long long l = l0 + t; l < l1; l += nthreads)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(base + l * 128) : "memory");
+  }
+}
 inline L2Ahead l2_ahead(const GemmArgs& a) {
   L2Ahead r;
   for (int i = 0; i < 3; ++i) {
@@ -419,14 +434,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmW);
     ptx::prefetch_tmap(&tmX);
   }
-  if (!TA && threadIdx.x == 32)
-    for (int i = 0; i < 3; ++i) ptx::prefetch_l2_slice(ahead.p[i], ahead.bytes[i]);
   if (warp == 2) ptx::tmem_alloc(tmem_slot, L::TMEM_COLS);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   ptx::pdl_launch_dependents();
+  // warps with no main-loop role pull the memory the next kernels read into L2 by plain
+  // line prefetches, which leave this CTA's TMA stream alone: warps 4..7 on the bf16
+  // path, warp 3 on the E4M3 path
+  if (!TA && warp >= 4) prefetch_lines_l2(ahead, threadIdx.x - 128, 128);
+  if (TA && warp == 3) prefetch_lines_l2(ahead, lane, 32);
 
   if constexpr (TA) {
     ta_main_loop<BN, STAGES, WF>(tmW, tmX, sA, sB, sRaw, full, empty, done, cvt_full, raw_full, raw_empty, tmem,
@@ -926,7 +944,7 @@ cudaError_t launch_ta(const CUtensorMap& tw, const CUtensorMap& tx, const GemmAr
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const int KB = a.K / L::BKX;
-  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim, L2Ahead{});
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim, l2_ahead(a));
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;

@@ -104,7 +104,7 @@ struct gr00t_ctx {
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
   int opt_mcast = 1;        // persistent GEMM: pairs of CTAs share activation tiles by TMA multicast
   int opt_attn_mcast = 1;   // expert attention: the row tiles of a sample share key tiles by TMA multicast
-  int opt_l2_ahead = 0;     // each layer's first GEMM prefetches the next layer into L2 (off: measured slower)
+  int opt_l2_ahead = 0;     // each GEMM's idle warps prefetch the next GEMM's weights into L2 (measured: no gain)
   long long noalloc_limit = -1;   // scratch bound of the allocation-free step (-1: the whole fixed array)
   int split_cap = 4;        // GEMMs that reduce their split-K partials in-kernel
   int resid_split_cap = 8;  // residual GEMMs whose partials the next kernel folds in
@@ -668,6 +668,21 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
   RC(stall_probe(c));
 
   auto site = [&](int si) { return (const void*)(mod_k + (long long)si * R * es); };
+  // GR00T_OPT_L2_PREFETCH: each GEMM's idle warps pull the next GEMM's weights (and the
+  // attention's bound K/V) into L2 while its own weights stream
+  const size_t wes = c->fp8w ? 1 : es;
+  const int up_rows = (c->g.mlp_kind == GR00T_MLP_GEGLU ? 2 : 1) * c->F;
+  (void)up_rows;
+  auto wbytes = [&](long long rows, long long cols) { return rows * cols * (long long)wes; };
+  auto ahead = [&](GemmArgs& g, const void* p, long long bytes) {
+    if (!c->opt_l2_ahead || !p || bytes <= 0) return;
+    for (auto& slot : g.l2)
+      if (!slot.p) {
+        slot.p = p;
+        slot.bytes = bytes;
+        return;
+      }
+  };
   // Kernels read the modulation table before their programmatic-launch wait.
   // The table is written when the schedule is set, so the head of step 0 is
   // launched without the early-launch attribute: it (and so every later
@@ -705,18 +720,13 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       g.epi.kind = EPI_ROPE; g.epi.out = c->qkv; g.epi.ldo = nq;
       g.epi.rope_cols = (c->Hq + 1) * c->Dh; g.epi.hd = c->Dh; g.epi.rope_tab = c->rope_tab;
       g.epi.tok_rope = tok;
-      if (c->opt_l2_ahead) {  // pull the next layer's weights (and flat prefix K/V) into L2 meanwhile
-        const int ln = (l + 1) % L;
-        g.l2[0].p = c->w_qkv[ln];
-        g.l2[0].bytes = ((const char*)c->w_down[ln] + (size_t)D * c->F * es) - (const char*)c->w_qkv[ln];
-        // a bound pool keeps samples ``capacity`` rows apart: a contiguous range would
-        // prefetch mostly other rows, so only flat prefix K/V is prefetched
-        if (P > 0 && c->pool.empty()) {
-          g.l2[1].p = c->host_table[2 * ln];
-          g.l2[1].bytes = (long long)B * P * c->Dh * es;
-          g.l2[2].p = c->host_table[2 * ln + 1];
-          g.l2[2].bytes = g.l2[1].bytes;
-        }
+      // while this GEMM streams its weights: the O projection's weights and this layer's
+      // prefix K/V into L2 (a bound pool keeps samples ``capacity`` rows apart, so only a
+      // flat binding's K/V is one contiguous range)
+      ahead(g, c->w_o[l], wbytes(D, c->qd));
+      if (P > 0 && c->pool.empty()) {
+        ahead(g, c->host_table[2 * l], (long long)B * P * c->Dh * es);
+        ahead(g, c->host_table[2 * l + 1], (long long)B * P * c->Dh * es);
       }
       RC(gemm(c, g, GR00T_KCLASS_QKV_GEMM));
 
@@ -773,6 +783,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       go.epi.wscale = c->fp8w ? c->s_o[l] : nullptr;
       go.epi.kind = EPI_RESID_GATED; go.epi.resid = c->h; go.epi.ldr = D;
       go.epi.gate = ptr_at(site(2 * l), 2LL * D, es); go.epi.gate_bstride = bstride; go.epi.tok = tok;
+      ahead(go, c->w_up[l], wbytes(up_rows, D));
       RC(gemm_resid(c, go, GR00T_KCLASS_O_GEMM));
 
       NormArgs n2 = na;
@@ -788,6 +799,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
         gu.N = c->F; gu.epi.kind = EPI_STORE; gu.epi.act = ACT_GELU;
       }
       gu.epi.out = c->u; gu.epi.ldo = c->F;
+      ahead(gu, c->w_down[l], wbytes(D, c->F));
       RC(gemm(c, gu, GR00T_KCLASS_UP_GEMM));
 
       GemmArgs gd;
@@ -795,6 +807,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
       gd.epi.wscale = c->fp8w ? c->s_down[l] : nullptr;
       gd.epi.kind = EPI_RESID_GATED; gd.epi.resid = c->h; gd.epi.ldr = D;
       gd.epi.gate = ptr_at(site(2 * l + 1), 2LL * D, es); gd.epi.gate_bstride = bstride; gd.epi.tok = tok;
+      ahead(gd, c->w_qkv[(l + 1) % L], wbytes(c->nqkv[(l + 1) % L], D));
       RC(gemm_resid(c, gd, GR00T_KCLASS_DOWN_GEMM));
 
       if (l + 1 < L) {
@@ -853,6 +866,12 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     g.A = c->n; g.lda = D; g.W = c->w_qkv[i]; g.ldw = D; g.M = M; g.N = nq; g.K = D;
     g.epi.wscale = c->fp8w ? c->s_qkv[i] : nullptr;
     g.epi.kind = EPI_STORE; g.epi.out = c->qkv; g.epi.ldo = nq;
+    ahead(g, c->w_o[i], wbytes(D, c->qd));
+    if (i % 2 == 0) {   // the cross block's context K/V
+      const long long kvb = (long long)B * P * c->Hkv * c->Dh * es;
+      ahead(g, c->host_table[2 * i], kvb);
+      ahead(g, c->host_table[2 * i + 1], kvb);
+    }
     RC(gemm(c, g, GR00T_KCLASS_QKV_GEMM));
     AttnArgs at;
     at.q = c->qkv; at.ldq = nq; at.B = B; at.Tq = tok; at.Hq = c->Hq; at.Hkv = c->Hkv; at.Dh = c->Dh;
@@ -878,6 +897,7 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     go.A = c->att; go.lda = c->qd; go.W = c->w_o[i]; go.ldw = c->qd; go.M = M; go.N = D; go.K = c->qd;
     go.epi.wscale = c->fp8w ? c->s_o[i] : nullptr;
     go.epi.kind = EPI_RESID; go.epi.resid = c->h; go.epi.ldr = D;
+    ahead(go, c->w_up[i], wbytes(c->F, D));
     RC(gemm_resid(c, go, GR00T_KCLASS_O_GEMM));
     NormArgs n3 = na;
     n3.mod = nullptr;
@@ -886,11 +906,13 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
     gu.A = c->n; gu.lda = D; gu.W = c->w_up[i]; gu.ldw = D; gu.M = M; gu.N = c->F; gu.K = D;
     gu.epi.wscale = c->fp8w ? c->s_up[i] : nullptr;
     gu.epi.kind = EPI_STORE; gu.epi.act = ACT_GELU; gu.epi.out = c->u; gu.epi.ldo = c->F;
+    ahead(gu, c->w_down[i], wbytes(D, c->F));
     RC(gemm(c, gu, GR00T_KCLASS_UP_GEMM));
     GemmArgs gd;
     gd.A = c->u; gd.lda = c->F; gd.W = c->w_down[i]; gd.ldw = c->F; gd.M = M; gd.N = D; gd.K = c->F;
     gd.epi.wscale = c->fp8w ? c->s_down[i] : nullptr;
     gd.epi.kind = EPI_RESID; gd.epi.resid = c->h; gd.epi.ldr = D;
+    ahead(gd, c->w_qkv[(i + 1) % L], wbytes(c->nqkv[(i + 1) % L], D));
     RC(gemm_resid(c, gd, GR00T_KCLASS_DOWN_GEMM));
   }
   NormArgs nf = na;

@@ -365,8 +365,9 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
 #define GR00T_OPT_SPLIT_CAP 6     /* largest split-K factor of GEMMs that reduce in-kernel (1..16, power of 2; default 4) */
 #define GR00T_OPT_RESID_SPLIT_CAP 7 /* same for residual GEMMs whose partials the next kernel folds in (default 8) */
 #define GR00T_OPT_PERSISTENT_GEMM 8 /* 1 (default): persistent tensor-core GEMM for unsplit shapes with > 64 tokens */
-#define GR00T_OPT_L2_PREFETCH 9   /* 1: each layer's first GEMM prefetches the next layer's weights (default 0)
-                                     and prefix K/V into L2 */
+#define GR00T_OPT_L2_PREFETCH 9   /* 1: the idle warps of every split tensor-core GEMM prefetch, with plain line
+                                     prefetches, the next GEMM's weights (and the attention's bound K/V) into
+                                     L2 while the GEMM streams its own (default 0: measured no gain) */
 #define GR00T_OPT_NOALLOC_LIMIT 10 /* scratch (fp32 elements) gr00t_denoise_step_noalloc may take from its fixed
                                       array: 0 .. 3 * 2^20 (default: the whole array).  With the split planner's
                                       one-wave rule no step on a 152-SM GPU needs the whole array, so a lower
