@@ -29,7 +29,7 @@ from . import _abi
 from ._abi import (DTYPE_BF16, DTYPE_FP32, FAMILY_DIT, FAMILY_EXPERT, MLP_GEGLU, MLP_GELU,
                    OPT_ATTN_PATH, OPT_GEMM_PATH, OPT_TIME_KERNELS, OPT_USE_GRAPH, OPT_WAIT_LIMIT,
                    OPT_SPLIT_CAP, OPT_RESID_SPLIT_CAP, OPT_PERSISTENT_GEMM, OPT_L2_PREFETCH, OPT_NOALLOC_LIMIT,
-                   OPT_ATTN_SPLIT_CAP, OPT_TEST_STALL, OPT_GEMM_MULTICAST, OPT_ATTN_MULTICAST, ETIMEOUT,
+                   OPT_ATTN_SPLIT_CAP, OPT_TEST_STALL, OPT_GEMM_MULTICAST, OPT_ATTN_MULTICAST, OPT_GEMM_TSTORE, ETIMEOUT,
                    INFO_DEVICE_BYTES, INFO_ERROR_FLAG, INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES,
                    KCLASS_ATTENTION, KCLASS_DOWN_GEMM, KCLASS_NORM, KCLASS_O_GEMM, KCLASS_QKV_GEMM,
                    KCLASS_UP_GEMM, KCLASS_OTHER, KCLASS_NAMES, WFMT_NATIVE, WFMT_FP8)

@@ -27,6 +27,7 @@ OPT_ATTN_SPLIT_CAP = 11
 OPT_TEST_STALL = 12
 OPT_GEMM_MULTICAST = 13
 OPT_ATTN_MULTICAST = 14
+OPT_GEMM_TSTORE = 15
 OPT_NOALLOC_LIMIT = 10
 KCLASS_QKV_GEMM, KCLASS_ATTENTION, KCLASS_O_GEMM, KCLASS_UP_GEMM, KCLASS_DOWN_GEMM, KCLASS_NORM = 1, 2, 3, 4, 5, 6
 KCLASS_OTHER = 7

@@ -245,8 +245,25 @@ __device__ __forceinline__ void epi_columns(const EpiRun<KIND, ACT>& run, const 
     run.compute(odd ? recv : v[c], odd ? v[c + 1] : recv, KIND == EPI_ROPE ? cs[c >> 1] : make_float2(1.f, 0.f),
                 o0[c >> 1], o1[c >> 1]);
   }
+  if constexpr (KIND == EPI_RESID || KIND == EPI_RESID_GATED) {
+    // read-modify-write of the residual rows: the residual (and gate) loads of 8
+    // columns are issued before their stores, so they are in flight together (a
+    // store between them would order each load after the previous store)
 #pragma unroll
-  for (int q = 0; q < 16; ++q)
-    if (m_first + 2 * q < M) run.store(m_first + 2 * q, o0[q], o1[q]);
+    for (int q0 = 0; q0 < 16; q0 += 8) {
+      EpiPre pre[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (m_first + 2 * (q0 + q) < M) pre[q] = epi_prefetch<bf16>(run.e_, m_first + 2 * (q0 + q), run.n_);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (m_first + 2 * (q0 + q) < M)
+          epi_pair<bf16>(run.e_, m_first + 2 * (q0 + q), run.n_, o0[q0 + q], o1[q0 + q], pre[q]);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 16; ++q)
+      if (m_first + 2 * q < M) run.store(m_first + 2 * q, o0[q], o1[q]);
+  }
 }
 }  // namespace g3

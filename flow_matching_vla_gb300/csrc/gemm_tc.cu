@@ -669,26 +669,122 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 constexpr int kPersThreads = 352;   // warp 0 weight TMA, 1 MMA, 2..9 epilogue, 10 activation TMA
 constexpr int kPersEpiWarps = 8;
+constexpr int kStgBox = 32 * 16 * 2;   // one staged output box: [32 tokens][16 outputs] bf16
+constexpr int kStgChunk = 2 * kStgBox;   // a chunk of 32 token columns: up to two boxes
 
 template <int BN, int STAGES>
 struct PersSmem {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int PIPE = STAGES * STAGE_BYTES;
+  static constexpr int STG = PIPE;   // per epilogue warp: two chunk buffers (double-buffered tensor stores)
+  static constexpr int BAR_OFF = STG + kPersEpiWarps * 2 * kStgChunk;
   static constexpr int BAR = (2 * STAGES + 4) * 8 + 16;
-  static constexpr int TOTAL = PIPE + BAR + 1024;
+  static constexpr int TOTAL = BAR_OFF + BAR + 1024;
+  static_assert(TOTAL <= 232448, "shared memory of the persistent GEMM");
 };
+
+// 2-D tensor store of one staged box, completion tracked by bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(ptx::smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
+// Epilogue of accumulator columns [c_begin, c_end) of this warp's 32 TMEM lanes
+// (output rows n_base .. n_base + 31, all < N) with the outputs staged in shared
+// memory and written by tensor stores.  Per 32-token chunk the warp's outputs
+// leave as one or two [32 tokens][16 outputs] boxes issued by lane 0, instead of
+// 16 to 32 scattered 2- or 4-byte stores per lane (measured ~90 cycles each when
+// all epilogue warps store at once).  Box x origins: plain pairs (EPI_STORE, and
+// the non-rotated rows of EPI_ROPE) n_base and n_base + 16; RoPE rows the two
+// halves of the head, head * hd + i and head * hd + i + hd / 2 for the warp's 16
+// frequencies i; GeGLU n_base / 2.  Two chunk buffers per warp: before one is
+// rewritten, the group that read it two chunks earlier has finished reading
+// (``ck`` counts this warp's chunks).  M = 0: compute and staging only (the
+// instruction-cache warm-up), nothing is stored and ``ck`` is unchanged.
+template <int KIND, int ACT>
+__device__ __forceinline__ void tile_epilogue_ts(const Epi& e, const CUtensorMap* tmO, uint32_t taddr, int c_begin,
+                                                 int c_end, int m0, int n_base, int M, int lane, uint8_t* stg,
+                                                 int& ck) {
+  const bool odd = lane & 1;
+  const int p = lane >> 1;   // this lane's pair: rows n_base + 2p, n_base + 2p + 1
+  const EpiRun<KIND, ACT> run(e, n_base + 2 * p);
+  const bool rot = KIND == EPI_ROPE && run.rope_;
+  int x0 = n_base, x1 = n_base + 16;
+  if (rot) {
+    x0 = (n_base / e.hd) * e.hd + (n_base % e.hd) / 2;
+    x1 = x0 + e.hd / 2;
+  } else if (KIND == EPI_GEGLU) {
+    x0 = n_base / 2;
+  }
+  constexpr bool kTwo = KIND != EPI_GEGLU;
+#pragma unroll 1
+  for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+    if (M > 0 && m0 + c0 >= M) break;   // every later chunk is past the last token too
+    float v[32];
+    ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+    float2 cs[16];
+    if (KIND == EPI_ROPE) {
+      int j = (m0 + c0 + (odd ? 1 : 0)) % e.tok_rope;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        cs[q] = run.rope_ ? run.rope_cs(j) : make_float2(1.f, 0.f);
+        j += 2;
+        if (j >= e.tok_rope) j -= e.tok_rope;
+        if (j >= e.tok_rope) j -= e.tok_rope;
+      }
+    }
+    float o0[16], o1[16];
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) {
+      const float send = odd ? v[c] : v[c + 1];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+      run.compute(odd ? recv : v[c], odd ? v[c + 1] : recv, KIND == EPI_ROPE ? cs[c >> 1] : make_float2(1.f, 0.f),
+                  o0[c >> 1], o1[c >> 1]);
+    }
+    uint8_t* buf = stg + (ck & 1) * kStgChunk;
+    if (M > 0 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    __syncwarp();
+    // token row 2q + odd of the chunk; [token][16 outputs] bf16 rows of 32 bytes
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int row = (2 * q + (odd ? 1 : 0)) * 32;
+      if (rot) {
+        *reinterpret_cast<bf16*>(buf + row + 2 * p) = __float2bfloat16_rn(o0[q]);
+        *reinterpret_cast<bf16*>(buf + kStgBox + row + 2 * p) = __float2bfloat16_rn(o1[q]);
+      } else if (KIND == EPI_GEGLU) {
+        *reinterpret_cast<bf16*>(buf + row + 2 * p) = __float2bfloat16_rn(o0[q]);
+      } else {
+        *reinterpret_cast<__nv_bfloat162*>(buf + (p >> 3) * kStgBox + row + 4 * (p & 7)) =
+            __floats2bfloat162_rn(o0[q], o1[q]);
+      }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the tensor store reads these writes
+    __syncwarp();
+    if (M > 0) {
+      if (lane == 0) {
+        tma_store_2d(tmO, buf, x0, m0 + c0);
+        if (kTwo) tma_store_2d(tmO, buf + kStgBox, x1, m0 + c0);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+      ++ck;
+    }
+  }
+}
 
 template <int BN, int STAGES, int CL>
 __global__ void __launch_bounds__(kPersThreads, 1)
-    gemm_tc_persistent(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
-                       int N, int KB, Epi e, int* err, long long wait_limit) {
+    gemm_tc_persistent(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ CUtensorMap tmO, int M, int N, int KB, Epi e, int* err,
+                       long long wait_limit) {
   using L = PersSmem<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::PIPE);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;   // accumulator b ready for the epilogue
   uint64_t* tempty = tfull + 2;       // accumulator b drained by the epilogue
@@ -816,7 +912,32 @@ __global__ void __launch_bounds__(kPersThreads, 1)
     const int quad = warp & 3;
     const int c_begin = (ew >> 2) * (BN / 2), c_end = c_begin + BN / 2;
     const bool odd = lane & 1;
-    {
+    const bool ts = e.tstore != 0;   // outputs leave through shared memory and tensor stores
+    uint8_t* stg = smem + L::STG + ew * 2 * kStgChunk;
+    int ck = 0;   // this warp's staged chunks (tensor-store path)
+    // one tensor-store epilogue pass of kind KIND over columns [cb, ce) (rows n_base < N)
+    auto ts_pass = [&](uint32_t taddr, int cb, int ce, int m0, int n_base, int Mx, int& k) {
+      switch (e.kind) {
+        case EPI_STORE:
+          if (e.act == ACT_SWISH)
+            tile_epilogue_ts<EPI_STORE, ACT_SWISH>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+          else if (e.act == ACT_GELU)
+            tile_epilogue_ts<EPI_STORE, ACT_GELU>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+          else
+            tile_epilogue_ts<EPI_STORE, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+          break;
+        case EPI_ROPE: tile_epilogue_ts<EPI_ROPE, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k); break;
+        case EPI_GEGLU: tile_epilogue_ts<EPI_GEGLU, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k); break;
+        default: break;
+      }
+    };
+    if (ts) {
+      // instruction-cache warm-up as below, through the tensor-store epilogue
+      const int n_base = (cid < ptiles ? tile_n0(cid) : 0) + quad * 32;
+      int ck_warm = 0;
+      if (n_base < N) ts_pass(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)BN, c_begin, c_begin + 32, 0, n_base, 0,
+                              ck_warm);
+    } else {
       // Warm-up while the first tile's main loop runs: one pass of this
       // kernel's epilogue over 32 columns of the idle second accumulator with
       // no token in range (M = 0: nothing is stored).  The epilogue code runs
@@ -850,7 +971,9 @@ __global__ void __launch_bounds__(kPersThreads, 1)
       const int n0 = tile_n0(p), m0 = tile_m0(p);
       const int n_even = n0 + quad * 32 + (lane & ~1);
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN);
-      switch (e.kind) {
+      if (ts) {
+        if (n0 + quad * 32 < N) ts_pass(taddr, c_begin, c_end, m0, n0 + quad * 32, M, ck);
+      } else switch (e.kind) {
         case EPI_STORE:
           if (e.act == ACT_SWISH)
             tile_epilogue<EPI_STORE, ACT_SWISH>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
@@ -867,6 +990,9 @@ __global__ void __launch_bounds__(kPersThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tempty[b]);
     }
+    // the tensor stores have read their staging buffers and written their outputs
+    if (ts && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
   }
   if (CL > 1 && warp == 0 && lane == 0) {
     // every release of this CTA's slots (its own MMA warp's and the peer's) has arrived:
@@ -885,8 +1011,8 @@ __global__ void __launch_bounds__(kPersThreads, 1)
 }
 
 template <int BN, int STAGES, int CL>
-cudaError_t launch_persistent(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int sm_count,
-                              int* err, long long lim, cudaStream_t s, bool pdl) {
+cudaError_t launch_persistent(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& to, const GemmArgs& a,
+                              int sm_count, int* err, long long lim, cudaStream_t s, bool pdl) {
   using L = PersSmem<BN, STAGES>;
   auto kern = gemm_tc_persistent<BN, STAGES, CL>;
   static bool configured = false;
@@ -911,7 +1037,7 @@ cudaError_t launch_persistent(const CUtensorMap& tw, const CUtensorMap& tx, cons
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CL > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, a.K / BK, a.epi, err, lim);
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, to, a.M, a.N, a.K / BK, a.epi, err, lim);
 }
 
 template <int BN, int STAGES, int WF>
@@ -1082,19 +1208,49 @@ namespace g3 {
 
 bool tc_use_persistent(const TcPlan& p, int M) { return p.S == 1 && M > 64; }
 
-cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a,
-                                      const TcPlan& p, int sm_count, int* err, long long wait_limit,
-                                      cudaStream_t s, bool pdl) {
+cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap* to,
+                                      const GemmArgs& a, const TcPlan& p, int sm_count, int* err,
+                                      long long wait_limit, cudaStream_t s, bool pdl) {
   if (!tc_supported(a.M, a.N, a.K) || p.S != 1) return cudaErrorInvalidValue;
+  if (a.epi.tstore && (!to || !tc_tstore_ok(a.epi, a.N))) return cudaErrorInvalidValue;
+  const CUtensorMap& o = to ? *to : tw;   // unused unless a.epi.tstore
   switch (p.BN) {
     case 128:
-      return p.CL == 2 ? launch_persistent<128, 6, 2>(tw, tx, a, sm_count, err, wait_limit, s, pdl)
-                       : launch_persistent<128, 6, 1>(tw, tx, a, sm_count, err, wait_limit, s, pdl);
+      return p.CL == 2 ? launch_persistent<128, 6, 2>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl)
+                       : launch_persistent<128, 6, 1>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl);
     case 256:
-      return p.CL == 2 ? launch_persistent<256, 4, 2>(tw, tx, a, sm_count, err, wait_limit, s, pdl)
-                       : launch_persistent<256, 4, 1>(tw, tx, a, sm_count, err, wait_limit, s, pdl);
+      return p.CL == 2 ? launch_persistent<256, 4, 2>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl)
+                       : launch_persistent<256, 4, 1>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl);
     default: return cudaErrorInvalidValue;
   }
+}
+
+bool tc_tstore_ok(const Epi& e, int N) {
+  if (N % 32 || !e.out || ((uintptr_t)e.out & 15) || (e.ldo * 2) % 16) return false;
+  switch (e.kind) {
+    case EPI_STORE: return !e.out_f32 && e.rg == 0;
+    case EPI_ROPE: return e.hd > 0 && e.hd % 32 == 0 && e.rope_cols % 32 == 0;
+    case EPI_GEGLU: return true;
+    default: return false;
+  }
+}
+
+cudaError_t tc_make_out_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld) {
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&g_encode, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode) return cudaErrorNotSupported;
+  }
+  if (((uintptr_t)ptr & 15) || (ld * 2) % 16 || cols % 16 || rows <= 0) return cudaErrorInvalidValue;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {16, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace g3

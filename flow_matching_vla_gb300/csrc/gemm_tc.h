@@ -43,9 +43,19 @@ cudaError_t gemm_tc_e4m3(const CUtensorMap& tw, const CUtensorMap& tx, const Gem
 // TMEM accumulator so each tile's epilogue overlaps the next tile's MMAs;
 // with plan.CL = 2, clusters of two CTAs over adjacent weight tiles share each
 // activation tile by TMA multicast (X map box: BN / 2 rows).
+// With a.epi.tstore set, its epilogue stages the outputs in shared memory and
+// writes them with tensor stores through ``to`` (from tc_make_out_map over the
+// output, cols = N for EPI_STORE / EPI_ROPE and N / 2 for EPI_GEGLU; only where
+// tc_tstore_ok holds); ``to`` may be null otherwise.
 bool tc_use_persistent(const TcPlan& p, int M);
-cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a,
-                                      const TcPlan& p, int sm_count, int* err, long long wait_limit,
-                                      cudaStream_t s, bool pdl);
+cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap* to,
+                                      const GemmArgs& a, const TcPlan& p, int sm_count, int* err,
+                                      long long wait_limit, cudaStream_t s, bool pdl);
+// The epilogue kinds and layouts the tensor-store path covers: bf16 EPI_STORE
+// without row remap, EPI_ROPE with hd % 32 == 0, EPI_GEGLU; N % 32 == 0, a
+// 16-byte aligned output with a leading dimension of a multiple of 8 elements.
+bool tc_tstore_ok(const Epi& e, int N);
+// bf16 [rows][cols] output map with leading dimension ``ld``: boxes of 16 columns x 32 rows, no swizzle.
+cudaError_t tc_make_out_map(CUtensorMap* m, const void* ptr, long long rows, long long cols, long long ld);
 
 }  // namespace g3

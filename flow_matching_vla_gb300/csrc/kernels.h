@@ -46,6 +46,9 @@ struct Epi {
   const float* wscale = nullptr;
   // dependency-release stamp of this launch (nullable; see kstamp in common.cuh)
   unsigned long long* ts = nullptr;
+  // persistent tensor-core GEMM: outputs staged in shared memory and written by
+  // tensor stores through the output map passed beside (set by the launcher)
+  int tstore = 0;
 };
 
 struct GemmArgs {

@@ -104,6 +104,7 @@ struct gr00t_ctx {
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
   int opt_mcast = 1;        // persistent GEMM: pairs of CTAs share activation tiles by TMA multicast
   int opt_attn_mcast = 1;   // expert attention: the row tiles of a sample share key tiles by TMA multicast
+  int opt_tstore = 1;       // persistent GEMM epilogues through shared memory and tensor stores
   int opt_l2_ahead = 0;     // each GEMM's idle warps prefetch the next GEMM's weights into L2 (measured: no gain)
   long long noalloc_limit = -1;   // scratch bound of the allocation-free step (-1: the whole fixed array)
   int split_cap = 4;        // GEMMs that reduce their split-K partials in-kernel
@@ -530,9 +531,11 @@ const CUtensorMap* tmap(gr00t_ctx* c, const void* ptr, long long rows, long long
   auto it = c->tmaps.find(key);
   if (it != c->tmaps.end()) return &it->second;
   CUtensorMap m;
-  // box_rows -1: E4M3 codes (uint8, 128 x 128-byte boxes); else bf16, 64 columns x box_rows
-  const cudaError_t e = box_rows < 0 ? tc_make_map_e4m3(&m, ptr, rows, cols, ld)
-                                     : tc_make_map(&m, ptr, rows, cols, ld, box_rows);
+  // box_rows -1: E4M3 codes (uint8, 128 x 128-byte boxes); -2: a bf16 GEMM output for
+  // tensor stores (16 columns x 32 rows); else bf16, 64 columns x box_rows
+  const cudaError_t e = box_rows == -2 ? tc_make_out_map(&m, ptr, rows, cols, ld)
+                        : box_rows < 0 ? tc_make_map_e4m3(&m, ptr, rows, cols, ld)
+                                       : tc_make_map(&m, ptr, rows, cols, ld, box_rows);
   if (e != cudaSuccess) return nullptr;
   if (c->no_host_alloc) {
     // the allocation-free step adds nothing to the cache: the descriptor goes to
@@ -582,8 +585,14 @@ int gemm(gr00t_ctx* c, GemmArgs a, int cls = GR00T_KCLASS_OTHER) {
     const CUtensorMap* tw = tmap(c, a.W, a.N, a.K, a.ldw, 128);
     const CUtensorMap* tx = tmap(c, a.A, a.M, a.K, a.lda, p.BN / p.CL);
     if (!tw || !tx) return set_err(c, GR00T_ECUDA, "TMA descriptor encode failed (alignment?)");
+    const CUtensorMap* to = nullptr;
+    if (pers && c->opt_tstore && tc_tstore_ok(a.epi, a.N)) {
+      // the persistent GEMM's outputs leave by tensor stores
+      to = tmap(c, a.epi.out, a.M, a.epi.kind == EPI_GEGLU ? a.N / 2 : a.N, a.epi.ldo, -2);
+      a.epi.tstore = to ? 1 : 0;
+    }
     if (pers)
-      CK(c, gemm_tc_persistent_launch(*tw, *tx, a, p, c->sm_count, c->err_flag, c->wait_limit, c->stream,
+      CK(c, gemm_tc_persistent_launch(*tw, *tx, to, a, p, c->sm_count, c->err_flag, c->wait_limit, c->stream,
                                       c->opt_pdl != 0));
     else
       CK(c, gemm_tc(*tw, *tx, a, p, c->gemm_ws, c->gemm_ws_floats, c->err_flag, c->wait_limit, c->stream,
@@ -1360,6 +1369,9 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
       break;
     case GR00T_OPT_ATTN_MULTICAST:
       c->opt_attn_mcast = value ? 1 : 0;
+      break;
+    case GR00T_OPT_GEMM_TSTORE:
+      c->opt_tstore = value ? 1 : 0;
       break;
     case GR00T_OPT_L2_PREFETCH:
       c->opt_l2_ahead = value ? 1 : 0;

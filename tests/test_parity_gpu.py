@@ -205,6 +205,29 @@ def test_attention_key_tile_multicast(kw):
     assert torch.equal(a, b)
 
 
+# the persistent GEMM's tensor-store epilogue (outputs staged in shared memory, written
+# by tensor stores) against per-lane stores: RoPE (head_dim 256 and 64), GeGLU and
+# plain/GELU outputs, one and several tiles per CTA, a ragged last token tile.  Checked
+# against the oracle with the tensor stores on (the default), then bit for bit against
+# the per-lane stores.
+@pytest.mark.parametrize("name,kw,split_cap", [
+    ("small_bf16", dict(batch=8), 1),
+    ("small_bf16", dict(batch=32, mlp_dim=2048), 4),
+    ("small_bf16", dict(q_heads=4, head_dim=64, batch=6, prefix=150), 1),
+    ("small_dit", dict(batch=16, prefix=120), 1),
+])
+def test_gemm_tensor_store_epilogue(name, kw, split_cap):
+    fmv = _fmv()
+    case = synth.make_case(name, **kw)
+    loop, _, _, _ = check_case(case, options=[(fmv.OPT_SPLIT_CAP, split_cap)])
+    x0 = torch.from_numpy(case["x_noise"]).cuda()
+    a = loop.denoise(x0).clone()
+    loop.set_option(fmv.OPT_GEMM_TSTORE, 0)
+    b = loop.denoise(x0).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
 def test_tcgen05_attention_head_dim_64():
     fmv = _fmv()
     c = synth.make_case("small_bf16", q_heads=4, head_dim=64, batch=4, prefix=150)
