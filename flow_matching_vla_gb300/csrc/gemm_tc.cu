@@ -774,7 +774,10 @@ __device__ __forceinline__ void tile_epilogue_ts(const Epi& e, const CUtensorMap
   }
 }
 
-template <int BN, int STAGES, int CL>
+// EK >= 0: the tensor-store epilogue of that kind is the only one compiled in
+// (a smaller kernel: its epilogue runs once per tile on a cold instruction cache);
+// EK = -1: every epilogue kind, chosen at run time.
+template <int BN, int STAGES, int CL, int EK>
 __global__ void __launch_bounds__(kPersThreads, 1)
     gemm_tc_persistent(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const __grid_constant__ CUtensorMap tmO, int M, int N, int KB, Epi e, int* err,
@@ -912,51 +915,67 @@ __global__ void __launch_bounds__(kPersThreads, 1)
     const int quad = warp & 3;
     const int c_begin = (ew >> 2) * (BN / 2), c_end = c_begin + BN / 2;
     const bool odd = lane & 1;
-    const bool ts = e.tstore != 0;   // outputs leave through shared memory and tensor stores
+    constexpr bool kSpec = EK >= 0;
+    const bool ts = kSpec || e.tstore != 0;   // outputs leave through shared memory and tensor stores
     uint8_t* stg = smem + L::STG + ew * 2 * kStgChunk;
     int ck = 0;   // this warp's staged chunks (tensor-store path)
-    // one tensor-store epilogue pass of kind KIND over columns [cb, ce) (rows n_base < N)
+    // tensor-store epilogue over columns [cb, ce) of rows n_base .. n_base + 31 (< N)
     auto ts_pass = [&](uint32_t taddr, int cb, int ce, int m0, int n_base, int Mx, int& k) {
-      switch (e.kind) {
-        case EPI_STORE:
-          if (e.act == ACT_SWISH)
-            tile_epilogue_ts<EPI_STORE, ACT_SWISH>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
-          else if (e.act == ACT_GELU)
-            tile_epilogue_ts<EPI_STORE, ACT_GELU>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
-          else
-            tile_epilogue_ts<EPI_STORE, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
-          break;
-        case EPI_ROPE: tile_epilogue_ts<EPI_ROPE, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k); break;
-        case EPI_GEGLU: tile_epilogue_ts<EPI_GEGLU, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k); break;
-        default: break;
+      if constexpr (EK == EPI_ROPE) {
+        tile_epilogue_ts<EPI_ROPE, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+      } else if constexpr (EK == EPI_GEGLU) {
+        tile_epilogue_ts<EPI_GEGLU, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+      } else {
+        switch (e.kind) {
+          case EPI_STORE:
+            if (e.act == ACT_SWISH)
+              tile_epilogue_ts<EPI_STORE, ACT_SWISH>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+            else if (e.act == ACT_GELU)
+              tile_epilogue_ts<EPI_STORE, ACT_GELU>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+            else
+              tile_epilogue_ts<EPI_STORE, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+            break;
+          case EPI_ROPE:
+            tile_epilogue_ts<EPI_ROPE, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+            break;
+          case EPI_GEGLU:
+            tile_epilogue_ts<EPI_GEGLU, ACT_NONE>(e, &tmO, taddr, cb, ce, m0, n_base, Mx, lane, stg, k);
+            break;
+          default: break;
+        }
       }
     };
-    if (ts) {
-      // instruction-cache warm-up as below, through the tensor-store epilogue
-      const int n_base = (cid < ptiles ? tile_n0(cid) : 0) + quad * 32;
-      int ck_warm = 0;
-      if (n_base < N) ts_pass(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)BN, c_begin, c_begin + 32, 0, n_base, 0,
-                              ck_warm);
-    } else {
+    // per-lane stores (and the residual kinds) over columns [cb, ce)
+    auto lane_pass = [&](uint32_t taddr, int cb, int ce, int m0, int n_even, int Mx) {
+      if constexpr (!kSpec) {
+        switch (e.kind) {
+          case EPI_STORE:
+            if (e.act == ACT_SWISH)
+              tile_epilogue<EPI_STORE, ACT_SWISH>(e, taddr, cb, ce, m0, n_even, Mx, N, odd);
+            else if (e.act == ACT_GELU)
+              tile_epilogue<EPI_STORE, ACT_GELU>(e, taddr, cb, ce, m0, n_even, Mx, N, odd);
+            else
+              tile_epilogue<EPI_STORE, ACT_NONE>(e, taddr, cb, ce, m0, n_even, Mx, N, odd);
+            break;
+          case EPI_ROPE: tile_epilogue<EPI_ROPE>(e, taddr, cb, ce, m0, n_even, Mx, N, odd); break;
+          case EPI_GEGLU: tile_epilogue<EPI_GEGLU>(e, taddr, cb, ce, m0, n_even, Mx, N, odd); break;
+          default: tile_epilogue<EPI_RESID>(e, taddr, cb, ce, m0, n_even, Mx, N, odd); break;
+        }
+      }
+    };
+    {
       // Warm-up while the first tile's main loop runs: one pass of this
       // kernel's epilogue over 32 columns of the idle second accumulator with
       // no token in range (M = 0: nothing is stored).  The epilogue code runs
       // once per tile on a cold instruction cache otherwise (measured: the
       // first 32 columns of a tile took ~2.5 us longer than the next ones).
-      const int n_even = (cid < ptiles ? tile_n0(cid) : 0) + quad * 32 + (lane & ~1);
+      const int n_base = (cid < ptiles ? tile_n0(cid) : 0) + quad * 32;
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)BN;
-      switch (e.kind) {
-        case EPI_STORE:
-          if (e.act == ACT_SWISH)
-            tile_epilogue<EPI_STORE, ACT_SWISH>(e, taddr, c_begin, c_begin + 32, 0, n_even, 0, N, odd);
-          else if (e.act == ACT_GELU)
-            tile_epilogue<EPI_STORE, ACT_GELU>(e, taddr, c_begin, c_begin + 32, 0, n_even, 0, N, odd);
-          else
-            tile_epilogue<EPI_STORE, ACT_NONE>(e, taddr, c_begin, c_begin + 32, 0, n_even, 0, N, odd);
-          break;
-        case EPI_ROPE: tile_epilogue<EPI_ROPE>(e, taddr, c_begin, c_begin + 32, 0, n_even, 0, N, odd); break;
-        case EPI_GEGLU: tile_epilogue<EPI_GEGLU>(e, taddr, c_begin, c_begin + 32, 0, n_even, 0, N, odd); break;
-        default: break;
+      int ck_warm = 0;
+      if (ts) {
+        if (n_base < N) ts_pass(taddr, c_begin, c_begin + 32, 0, n_base, 0, ck_warm);
+      } else {
+        lane_pass(taddr, c_begin, c_begin + 32, 0, n_base + (lane & ~1), 0);
       }
     }
     int lt = 0;
@@ -969,22 +988,11 @@ __global__ void __launch_bounds__(kPersThreads, 1)
       ptx::tc_fence_after();
       if (*abort_flag) break;
       const int n0 = tile_n0(p), m0 = tile_m0(p);
-      const int n_even = n0 + quad * 32 + (lane & ~1);
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(b * BN);
       if (ts) {
         if (n0 + quad * 32 < N) ts_pass(taddr, c_begin, c_end, m0, n0 + quad * 32, M, ck);
-      } else switch (e.kind) {
-        case EPI_STORE:
-          if (e.act == ACT_SWISH)
-            tile_epilogue<EPI_STORE, ACT_SWISH>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
-          else if (e.act == ACT_GELU)
-            tile_epilogue<EPI_STORE, ACT_GELU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
-          else
-            tile_epilogue<EPI_STORE, ACT_NONE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd);
-          break;
-        case EPI_ROPE: tile_epilogue<EPI_ROPE>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
-        case EPI_GEGLU: tile_epilogue<EPI_GEGLU>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
-        default: tile_epilogue<EPI_RESID>(e, taddr, c_begin, c_end, m0, n_even, M, N, odd); break;
+      } else {
+        lane_pass(taddr, c_begin, c_end, m0, n0 + quad * 32 + (lane & ~1), M);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -1010,11 +1018,11 @@ __global__ void __launch_bounds__(kPersThreads, 1)
   }
 }
 
-template <int BN, int STAGES, int CL>
+template <int BN, int STAGES, int CL, int EK>
 cudaError_t launch_persistent(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& to, const GemmArgs& a,
                               int sm_count, int* err, long long lim, cudaStream_t s, bool pdl) {
   using L = PersSmem<BN, STAGES>;
-  auto kern = gemm_tc_persistent<BN, STAGES, CL>;
+  auto kern = gemm_tc_persistent<BN, STAGES, CL, EK>;
   static bool configured = false;
   if (!configured) {
     cudaError_t e1 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::TOTAL);
@@ -1214,15 +1222,19 @@ cudaError_t gemm_tc_persistent_launch(const CUtensorMap& tw, const CUtensorMap& 
   if (!tc_supported(a.M, a.N, a.K) || p.S != 1) return cudaErrorInvalidValue;
   if (a.epi.tstore && (!to || !tc_tstore_ok(a.epi, a.N))) return cudaErrorInvalidValue;
   const CUtensorMap& o = to ? *to : tw;   // unused unless a.epi.tstore
+  // tensor-store RoPE and GeGLU epilogues (the projections of every layer) run in
+  // kernels specialised to that one epilogue
+  const int ek = !a.epi.tstore ? -1 : a.epi.kind == EPI_ROPE ? EPI_ROPE : a.epi.kind == EPI_GEGLU ? EPI_GEGLU : -1;
+#define G3_PERS(BN_, ST_, CL_)                                                                            \
+  (ek == EPI_ROPE    ? launch_persistent<BN_, ST_, CL_, EPI_ROPE>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl) \
+   : ek == EPI_GEGLU ? launch_persistent<BN_, ST_, CL_, EPI_GEGLU>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl) \
+                     : launch_persistent<BN_, ST_, CL_, -1>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl))
   switch (p.BN) {
-    case 128:
-      return p.CL == 2 ? launch_persistent<128, 6, 2>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl)
-                       : launch_persistent<128, 6, 1>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl);
-    case 256:
-      return p.CL == 2 ? launch_persistent<256, 4, 2>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl)
-                       : launch_persistent<256, 4, 1>(tw, tx, o, a, sm_count, err, wait_limit, s, pdl);
+    case 128: return p.CL == 2 ? G3_PERS(128, 6, 2) : G3_PERS(128, 6, 1);
+    case 256: return p.CL == 2 ? G3_PERS(256, 4, 2) : G3_PERS(256, 4, 1);
     default: return cudaErrorInvalidValue;
   }
+#undef G3_PERS
 }
 
 bool tc_tstore_ok(const Epi& e, int N) {
