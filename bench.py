@@ -140,16 +140,25 @@ def load_peaks():
 
 # DRAM traffic per launch of a kernel class from ncu captures (profiles/traffic.json,
 # written with `python bench.py --record-traffic ...`): reported only while the
-# kernel sources hashed there are unchanged.
+# sources of that class's kernels, hashed there, are unchanged.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ("gemm_tc.cu", "epilogue.cuh", "attention_tc5.cu", "attention_dit.cu", "norm.cu", "tc_ptx.cuh")
+KERNEL_SOURCES = {
+    "attention": ("attention_tc5.cu", "attention_dit.cu", "tc_ptx.cuh", "common.cuh", "launch.cuh"),
+    "gemm": ("gemm_tc.cu", "gemm_tc_impl.cuh", "gemm_tc_pers.cu", "gemm_tc_spec.cu", "epilogue.cuh", "tc_ptx.cuh",
+             "common.cuh", "launch.cuh"),
+    "norm": ("norm.cu", "common.cuh", "launch.cuh"),
+}
 
 
-def source_digest():
+def source_group(kernel: str) -> str:
+    return kernel if kernel in ("attention", "norm") else "gemm"
+
+
+def source_digest(kernel: str = "attention"):
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "flow_matching_vla_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[source_group(kernel)]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -157,12 +166,13 @@ def source_digest():
 
 def measured_traffic(workload: str, kernel: str):
     """Per-launch DRAM bytes of ``kernel`` from the recorded capture, or None when none
-    is recorded for this workload or the kernel sources changed since."""
+    is recorded for this workload or the class's kernel sources changed since."""
     try:
         t = json.load(open(TRAFFIC_FILE))
     except (OSError, ValueError):
         return None
-    if t.get("sources") != source_digest():
+    src = t.get("sources")
+    if not isinstance(src, dict) or src.get(kernel) != source_digest(kernel):
         return None
     return t.get("bytes_per_launch", {}).get(workload, {}).get(kernel)
 
@@ -188,8 +198,15 @@ def record_traffic(csv_path: str, workload: str, kernel: str, command: str):
         t = json.load(open(TRAFFIC_FILE))
     except (OSError, ValueError):
         t = {}
-    if t.get("sources") != source_digest():
-        t = {"sources": source_digest(), "bytes_per_launch": {}, "commands": {}}
+    if not isinstance(t.get("sources"), dict):
+        t = {"sources": {}, "bytes_per_launch": {}, "commands": {}}
+    if t["sources"].get(kernel) != source_digest(kernel):
+        # the class's kernels changed: its earlier numbers (every workload) are stale
+        for w in t["bytes_per_launch"].values():
+            w.pop(kernel, None)
+        for w in t["commands"].values():
+            w.pop(kernel, None)
+        t["sources"][kernel] = source_digest(kernel)
     t["bytes_per_launch"].setdefault(workload, {})[kernel] = float(np.mean(list(vals.values())))
     t["commands"].setdefault(workload, {})[kernel] = command
     with open(TRAFFIC_FILE, "w") as f:

@@ -30,6 +30,12 @@ long long tc_workspace_floats(const TcPlan& p, int M, int N);
 cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
                     float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl);
 
+// gemm_tc for one epilogue kind ``ek`` (EPI_PARTIAL, or EPI_ROPE / EPI_GEGLU /
+// EPI_STORE with plan.S == 1 or plan.BN <= 128) through a kernel holding only that epilogue.
+cudaError_t gemm_tc_split_spec(int ek, const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a,
+                               const TcPlan& p, float* ws, int* err, long long wait_limit, cudaStream_t s,
+                               bool pdl);
+
 // E4M3 weights (uint8 codes [N][K], one fp32 scale per row in a.epi.wscale):
 // K a multiple of 128; the W map from tc_make_map_e4m3 (box 128 x 128 bytes),
 // the X map as above.

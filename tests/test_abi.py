@@ -207,5 +207,5 @@ def test_bench_traffic_needs_unchanged_sources(monkeypatch, tmp_path):
     bench.record_traffic(str(csv), "pi05_b32", "attention", "ncu ...")
     assert bench.measured_traffic("pi05_b32", "attention") == pytest.approx(12e6)
     # a digest that no longer matches the kernel sources hides the number
-    monkeypatch.setattr(bench, "source_digest", lambda: "0" * 16)
+    monkeypatch.setattr(bench, "source_digest", lambda kernel="attention": "0" * 16)
     assert bench.measured_traffic("pi05_b32", "attention") is None
