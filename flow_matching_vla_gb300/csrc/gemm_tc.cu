@@ -91,19 +91,21 @@ long long tc_workspace_floats(const TcPlan& p, int M, int N) {
   return tiles * p.S * p.BN * BM;
 }
 
-cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
-                    float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl) {
+cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap* to, const GemmArgs& a,
+                    const TcPlan& p, float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s,
+                    bool pdl) {
   if (!tc_supported(a.M, a.N, a.K) || (a.K / BK) % p.S) return cudaErrorInvalidValue;
   if (a.epi.kind != EPI_PARTIAL && tc_workspace_floats(p, a.M, a.N) > ws_floats) return cudaErrorInvalidValue;
   // kernels specialised to one epilogue: residual partials, and RoPE / GeGLU / plain
   // outputs without a split or with the on-chip reduction (tiles of up to 128 tokens)
   const int k = a.epi.kind;
   if (k == EPI_PARTIAL || ((k == EPI_ROPE || k == EPI_GEGLU || k == EPI_STORE) && (p.S == 1 || p.BN <= 128)))
-    return gemm_tc_split_spec(k, tw, tx, a, p, ws, err, wait_limit, s, pdl);
+    return gemm_tc_split_spec(k, tw, tx, to, a, p, ws, err, wait_limit, s, pdl);
+  if (a.epi.tstore) return cudaErrorInvalidValue;
   switch (p.BN) {
-    case 64: return launch<64, 8>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);    // 8 x 24 KB stages
-    case 128: return launch<128, 6>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);   // 6 x 32 KB stages
-    case 256: return launch<256, 4>(tw, tx, a, p.S, ws, err, wait_limit, s, pdl);
+    case 64: return launch<64, 8>(tw, tx, tw, a, p.S, ws, err, wait_limit, s, pdl);    // 8 x 24 KB stages
+    case 128: return launch<128, 6>(tw, tx, tw, a, p.S, ws, err, wait_limit, s, pdl);   // 6 x 32 KB stages
+    case 256: return launch<256, 4>(tw, tx, tw, a, p.S, ws, err, wait_limit, s, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -113,6 +115,28 @@ cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs
 namespace g3 {
 
 bool tc_use_persistent(const TcPlan& p, int M) { return p.S == 1 && M > 64; }
+
+bool tc_partial_tstore_ok(const Epi& e, int N) {
+  return e.kind == EPI_PARTIAL && N % 32 == 0 && e.out && !((uintptr_t)e.out & 15) && (e.ldo * 4) % 16 == 0;
+}
+
+cudaError_t tc_make_part_map(CUtensorMap* m, const void* ptr, long long M, long long N, long long ld, int S) {
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", (void**)&g_encode, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !g_encode) return cudaErrorNotSupported;
+  }
+  if (((uintptr_t)ptr & 15) || (ld * 4) % 16 || N % 32 || M <= 0 || S <= 0) return cudaErrorInvalidValue;
+  cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)S};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)(M * ld * 4)};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 bool tc_tstore_ok(const Epi& e, int N) {
   if (N % 32 || !e.out || ((uintptr_t)e.out & 15) || (e.ldo * 2) % 16) return false;

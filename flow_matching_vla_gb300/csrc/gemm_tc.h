@@ -26,15 +26,23 @@ bool tc_supported(int M, int N, int K);
 TcPlan tc_plan(int M, int N, int K, int sm_count, int max_split, bool partial);
 // Split-K partials the plan needs (fp32 elements of the workspace).
 long long tc_workspace_floats(const TcPlan& p, int M, int N);
-// W map: box_rows 128 over [N][K]; X map: box_rows plan.BN over [M][K].
-cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, const TcPlan& p,
-                    float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s, bool pdl);
+// W map: box_rows 128 over [N][K]; X map: box_rows plan.BN over [M][K].  With
+// a.epi.tstore set (EPI_PARTIAL only), the split partials leave by tensor stores
+// through ``to`` (from tc_make_part_map over the [S][M][ldo] partial buffer);
+// ``to`` may be null otherwise.
+cudaError_t gemm_tc(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap* to, const GemmArgs& a,
+                    const TcPlan& p, float* ws, long long ws_floats, int* err, long long wait_limit, cudaStream_t s,
+                    bool pdl);
+// Split partials by tensor stores: N % 32 == 0, a 16-byte aligned buffer, ldo % 4 == 0.
+bool tc_partial_tstore_ok(const Epi& e, int N);
+// fp32 [S][M][N] map (row stride ld, split stride M * ld) with boxes of 32 x 32 x 1.
+cudaError_t tc_make_part_map(CUtensorMap* m, const void* ptr, long long M, long long N, long long ld, int S);
 
 // gemm_tc for one epilogue kind ``ek`` (EPI_PARTIAL, or EPI_ROPE / EPI_GEGLU /
 // EPI_STORE with plan.S == 1 or plan.BN <= 128) through a kernel holding only that epilogue.
-cudaError_t gemm_tc_split_spec(int ek, const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a,
-                               const TcPlan& p, float* ws, int* err, long long wait_limit, cudaStream_t s,
-                               bool pdl);
+cudaError_t gemm_tc_split_spec(int ek, const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap* to,
+                               const GemmArgs& a, const TcPlan& p, float* ws, int* err, long long wait_limit,
+                               cudaStream_t s, bool pdl);
 
 // E4M3 weights (uint8 codes [N][K], one fp32 scale per row in a.epi.wscale):
 // K a multiple of 128; the W map from tc_make_map_e4m3 (box 128 x 128 bytes),

@@ -91,6 +91,14 @@ __device__ __forceinline__ void bulk_to_peer(uint32_t rdst, uint32_t src, uint32
       : "memory");
 }
 
+// 3-D tensor store of one staged box (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(ptx::smem_u32(src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Element (r, c) of an fp32 [BM rows][BN] tile in shared memory: 16-byte chunk
 // c / 4 of row r stored at chunk (c / 4) ^ ((r / 2) % 8), so both the
 // row-per-lane writes from TMEM and the row-pair-per-lane reads of the
@@ -389,9 +397,9 @@ __device__ __forceinline__ void ta_main_loop(const CUtensorMap& tmW, const CUten
 // once-per-CTA code on a cold instruction cache; EK = -1: every kind and path.
 template <int BN, int STAGES, int WF = WF_SMEM, int EK = -1>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, int M,
-                   int N, int kb_per_split, Epi e, float* __restrict__ ws, int* err, long long wait_limit,
-                   L2Ahead ahead) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   const __grid_constant__ CUtensorMap tmO, int M, int N, int kb_per_split, Epi e,
+                   float* __restrict__ ws, int* err, long long wait_limit, L2Ahead ahead) {
   using L = TcSmem<BN, STAGES, WF>;
   constexpr bool F8 = L::F8, TA = L::TA;
   extern __shared__ uint8_t smem_raw[];
@@ -531,7 +539,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   // F8: the accumulator holds sum_k e4m3(code) x; the row's scale finishes it
   const float wsc = F8 ? (n0 + row < N ? e.wscale[n0 + row] : 0.f) : 1.f;
 
-  if (kind == EPI_PARTIAL) {
+  if (EK == EPI_PARTIAL && e.tstore) {
+    // split partial to the consumer's buffer [split][M][ldo] by tensor stores: each warp
+    // stages its [BN/2 tokens][32 rows] fp32 block, [token][row] (128-byte rows), in the
+    // idle pipeline memory (every MMA has completed), and its lane 0 writes one
+    // [32 tokens][32 rows] box per 32 tokens through a [split][M][N] map, which clips
+    // tokens past M within the split
+    float* stg = reinterpret_cast<float*>(smem) + warp * (BN / 2) * 32;
+    const int nb = n0 + quad * 32;   // this warp's first row (N % 32 == 0: all its rows or none are < N)
+    if (!aborted && nb < N) {
+#pragma unroll 1
+      for (int c0 = c_begin; c0 < c_end; c0 += 32) {
+        if (m0 + c0 >= M) break;
+        float v[32];
+        ptx::tmem_ld32(taddr + (uint32_t)c0, v);
+        float* sp = stg + (c0 - c_begin) * 32;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sp[j * 32 + lane] = F8 ? v[j] * wsc : v[j];
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the tensor stores read these writes
+      __syncwarp();
+      if (lane == 0) {
+        for (int c0 = c_begin; c0 < c_end && m0 + c0 < M; c0 += 32)
+          tma_store_3d(&tmO, stg + (c0 - c_begin) * 32, nb, m0 + c0, (int)blockIdx.z);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+      }
+      __syncwarp();
+    }
+  } else if (kind == EPI_PARTIAL) {
     // split partial straight to the consumer's buffer: out[(split * M + m) * ldo + n]
     float* part = reinterpret_cast<float*>(e.out) + (long long)blockIdx.z * M * e.ldo;
     const int n = n0 + row;
@@ -1108,12 +1144,12 @@ cudaError_t launch_ta(const CUtensorMap& tw, const CUtensorMap& tx, const GemmAr
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const int KB = a.K / L::BKX;
-  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim, l2_ahead(a));
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, tw, a.M, a.N, KB / S, a.epi, ws, err, lim, l2_ahead(a));
 }
 
 template <int BN, int STAGES, int EK = -1>
-cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs& a, int S, float* ws,
-                   int* err, long long lim, cudaStream_t s, bool pdl) {
+cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const CUtensorMap& to, const GemmArgs& a, int S,
+                   float* ws, int* err, long long lim, cudaStream_t s, bool pdl) {
   using L = TcSmem<BN, STAGES>;
   auto kern = gemm_tc_kernel<BN, STAGES, WF_SMEM, EK>;
   static bool configured = false;
@@ -1139,7 +1175,7 @@ cudaError_t launch(const CUtensorMap& tw, const CUtensorMap& tx, const GemmArgs&
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const int KB = a.K / BK;
-  return cudaLaunchKernelEx(&cfg, kern, tw, tx, a.M, a.N, KB / S, a.epi, ws, err, lim, l2_ahead(a));
+  return cudaLaunchKernelEx(&cfg, kern, tw, tx, to, a.M, a.N, KB / S, a.epi, ws, err, lim, l2_ahead(a));
 }
 
 }  // namespace

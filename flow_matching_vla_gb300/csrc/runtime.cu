@@ -532,8 +532,10 @@ const CUtensorMap* tmap(gr00t_ctx* c, const void* ptr, long long rows, long long
   if (it != c->tmaps.end()) return &it->second;
   CUtensorMap m;
   // box_rows -1: E4M3 codes (uint8, 128 x 128-byte boxes); -2: a bf16 GEMM output for
-  // tensor stores (16 columns x 32 rows); else bf16, 64 columns x box_rows
-  const cudaError_t e = box_rows == -2 ? tc_make_out_map(&m, ptr, rows, cols, ld)
+  // tensor stores (16 columns x 32 rows); <= -100: fp32 split partials [S = -100 - box_rows]
+  // [rows][cols] for tensor stores (32 x 32 boxes); else bf16, 64 columns x box_rows
+  const cudaError_t e = box_rows <= -100 ? tc_make_part_map(&m, ptr, rows, cols, ld, -100 - box_rows)
+                        : box_rows == -2 ? tc_make_out_map(&m, ptr, rows, cols, ld)
                         : box_rows < 0 ? tc_make_map_e4m3(&m, ptr, rows, cols, ld)
                                        : tc_make_map(&m, ptr, rows, cols, ld, box_rows);
   if (e != cudaSuccess) return nullptr;
@@ -594,9 +596,17 @@ int gemm(gr00t_ctx* c, GemmArgs a, int cls = GR00T_KCLASS_OTHER) {
     if (pers)
       CK(c, gemm_tc_persistent_launch(*tw, *tx, to, a, p, c->sm_count, c->err_flag, c->wait_limit, c->stream,
                                       c->opt_pdl != 0));
-    else
-      CK(c, gemm_tc(*tw, *tx, a, p, c->gemm_ws, c->gemm_ws_floats, c->err_flag, c->wait_limit, c->stream,
+    else {
+      if (a.epi.kind == EPI_PARTIAL && p.BN <= 128 && c->opt_tstore && tc_partial_tstore_ok(a.epi, a.N)) {
+        // the split partials of tiles of up to 128 tokens leave by tensor stores (measured:
+        // faster for 64-token tiles; 256-token tiles keep the per-lane stores, which already
+        // write whole 128-byte lines, where staging only adds shared-memory traffic)
+        to = tmap(c, a.epi.out, a.M, a.N, a.epi.ldo, -100 - p.S);
+        a.epi.tstore = to ? 1 : 0;
+      }
+      CK(c, gemm_tc(*tw, *tx, to, a, p, c->gemm_ws, c->gemm_ws_floats, c->err_flag, c->wait_limit, c->stream,
                     c->opt_pdl != 0));
+    }
   } else {
     CK(c, gemm_simt(c->dt, a, c->stream, c->opt_pdl != 0));
   }

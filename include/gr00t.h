@@ -381,8 +381,9 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
                                        as one cluster that fetches every key tile once and multicasts it;
                                        0: each row tile fetches its own copies */
 #define GR00T_OPT_GEMM_TSTORE 15   /* 1 (default): the persistent tensor-core GEMM stages its bf16 outputs (plain,
-                                      RoPE, GeGLU epilogues) in shared memory and writes them with tensor stores;
-                                      0: every lane stores its own outputs */
+                                      RoPE, GeGLU epilogues), and the split GEMM with tiles of up to 128 tokens
+                                      its fp32 residual partials, in shared memory and writes them with tensor
+                                      stores; 0: every lane stores its own outputs */
 #define GR00T_OPT_TEST_STALL 12   /* test hook: > 0 enqueues ahead of every step a one-thread kernel
                                      that waits this many polls for a device word nothing writes, then
                                      sets the device error word -- the bounded-wait error path with no

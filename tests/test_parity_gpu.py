@@ -205,16 +205,19 @@ def test_attention_key_tile_multicast(kw):
     assert torch.equal(a, b)
 
 
-# the persistent GEMM's tensor-store epilogue (outputs staged in shared memory, written
-# by tensor stores) against per-lane stores: RoPE (head_dim 256 and 64), GeGLU and
-# plain/GELU outputs, one and several tiles per CTA, a ragged last token tile.  Checked
-# against the oracle with the tensor stores on (the default), then bit for bit against
-# the per-lane stores.
+# the tensor-store epilogues (outputs staged in shared memory, written by tensor
+# stores) against per-lane stores: the persistent GEMM's RoPE (head_dim 256 and 64),
+# GeGLU and plain/GELU outputs, one and several tiles per CTA, a ragged last token
+# tile; and the split GEMMs' fp32 residual partials (64- and 256-token tiles, 2 to 8
+# splits, tokens past M clipped within each split).  Checked against the oracle with
+# the tensor stores on (the default), then bit for bit against the per-lane stores.
 @pytest.mark.parametrize("name,kw,split_cap", [
     ("small_bf16", dict(batch=8), 1),
     ("small_bf16", dict(batch=32, mlp_dim=2048), 4),
     ("small_bf16", dict(q_heads=4, head_dim=64, batch=6, prefix=150), 1),
     ("small_dit", dict(batch=16, prefix=120), 1),
+    ("small_bf16", dict(), 4),
+    ("small_dit", dict(), 4),
 ])
 def test_gemm_tensor_store_epilogue(name, kw, split_cap):
     fmv = _fmv()
