@@ -102,8 +102,9 @@ struct gr00t_ctx {
   int opt_pdl = 1;
   int opt_attn_splits = 0;  // expert attention key-split cap (0: automatic)
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
-  int opt_mcast = 1;        // persistent GEMM: pairs of CTAs share activation tiles by TMA multicast
-  int opt_attn_mcast = 1;   // expert attention: the row tiles of a sample share key tiles by TMA multicast
+  // TMA multicast (measured ~1 % slower each at batch 32 with the current kernels: off)
+  int opt_mcast = 0;        // persistent GEMM: pairs of CTAs share activation tiles by TMA multicast
+  int opt_attn_mcast = 0;   // expert attention: the row tiles of a sample share key tiles by TMA multicast
   int opt_tstore = 1;       // persistent GEMM epilogues through shared memory and tensor stores
   int opt_l2_ahead = 0;     // each GEMM's idle warps prefetch the next GEMM's weights into L2 (measured: no gain)
   long long noalloc_limit = -1;   // scratch bound of the allocation-free step (-1: the whole fixed array)

@@ -374,12 +374,12 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
                                       limit is how the refusal is exercised */
 #define GR00T_OPT_ATTN_SPLIT_CAP 11 /* expert family, tcgen05 attention: at most this many key splits
                                        (1 .. 32; 0 = automatic: as many as fill the SMs, up to 32) */
-#define GR00T_OPT_GEMM_MULTICAST 13 /* 1 (default): the persistent tensor-core GEMM runs as clusters of two
-                                       CTAs over adjacent weight tiles that share each activation tile by
-                                       TMA multicast; 0: one CTA per tile stream */
-#define GR00T_OPT_ATTN_MULTICAST 14 /* 1 (default): the expert attention runs the 2 or 4 row tiles of a sample
-                                       as one cluster that fetches every key tile once and multicasts it;
-                                       0: each row tile fetches its own copies */
+#define GR00T_OPT_GEMM_MULTICAST 13 /* 1: the persistent tensor-core GEMM runs as clusters of two CTAs over
+                                       adjacent weight tiles that share each activation tile by TMA
+                                       multicast; 0 (default, measured faster): one CTA per tile stream */
+#define GR00T_OPT_ATTN_MULTICAST 14 /* 1: the expert attention runs the 2 or 4 row tiles of a sample as one
+                                       cluster that fetches every key tile once and multicasts it; 0
+                                       (default, measured faster): each row tile fetches its own copies */
 #define GR00T_OPT_GEMM_TSTORE 15   /* 1 (default): the persistent tensor-core GEMM stages its bf16 outputs (plain,
                                       RoPE, GeGLU epilogues), and the split GEMM with tiles of up to 128 tokens
                                       its fp32 residual partials, in shared memory and writes them with tensor

@@ -196,7 +196,7 @@ def test_expert_attention_paths(path, kw):
 def test_attention_key_tile_multicast(kw):
     fmv = _fmv()
     case = synth.make_case("small_bf16", **kw)
-    loop, _, _, _ = check_case(case)
+    loop, _, _, _ = check_case(case, options=[(fmv.OPT_ATTN_MULTICAST, 1)])
     x0 = torch.from_numpy(case["x_noise"]).cuda()
     a = loop.denoise(x0).clone()
     loop.set_option(fmv.OPT_ATTN_MULTICAST, 0)
@@ -226,6 +226,21 @@ def test_gemm_tensor_store_epilogue(name, kw, split_cap):
     x0 = torch.from_numpy(case["x_noise"]).cuda()
     a = loop.denoise(x0).clone()
     loop.set_option(fmv.OPT_GEMM_TSTORE, 0)
+    b = loop.denoise(x0).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# persistent GEMM tiles of two CTAs sharing each activation tile by multicast (one and
+# several tiles per CTA, a ragged last token tile) against one CTA per tile stream
+@pytest.mark.parametrize("kw", [dict(batch=8), dict(batch=32, mlp_dim=2048)])
+def test_gemm_activation_multicast(kw):
+    fmv = _fmv()
+    case = synth.make_case("small_bf16", **kw)
+    loop, _, _, _ = check_case(case, options=[(fmv.OPT_SPLIT_CAP, 1), (fmv.OPT_GEMM_MULTICAST, 1)])
+    x0 = torch.from_numpy(case["x_noise"]).cuda()
+    a = loop.denoise(x0).clone()
+    loop.set_option(fmv.OPT_GEMM_MULTICAST, 0)
     b = loop.denoise(x0).clone()
     torch.cuda.synchronize()
     assert torch.equal(a, b)
