@@ -102,9 +102,10 @@ struct gr00t_ctx {
   int opt_pdl = 1;
   int opt_attn_splits = 0;  // expert attention key-split cap (0: automatic)
   int opt_persistent = 1;   // persistent tensor-core GEMM for unsplit large-M shapes
-  // TMA multicast (measured ~1 % slower each at batch 32 with the current kernels: off)
+  // TMA multicast (measured ~1 % slower each at batch 32 with the current kernels)
   int opt_mcast = 0;        // persistent GEMM: pairs of CTAs share activation tiles by TMA multicast
-  int opt_attn_mcast = 0;   // expert attention: the row tiles of a sample share key tiles by TMA multicast
+  int opt_attn_mcast = 2;   // expert attention: the row tiles of a sample share key tiles by TMA
+                            // multicast (2: where each CTA streams at most 4 key tiles)
   int opt_tstore = 1;       // persistent GEMM epilogues through shared memory and tensor stores
   int opt_l2_ahead = 0;     // each GEMM's idle warps prefetch the next GEMM's weights into L2 (measured: no gain)
   long long noalloc_limit = -1;   // scratch bound of the allocation-free step (-1: the whole fixed array)
@@ -768,7 +769,12 @@ int enqueue_step(gr00t_ctx* c, int k, float* x, float* v_out, int do_euler) {
           a5.pool_k = c->pool[l];
           a5.pool_v = (char*)c->pool[l] + (size_t)B * c->pool_cap * c->Dh * es;
         }
-        a5.ct = c->opt_attn_mcast ? attn_t5_cluster(a5) : 1;
+        // the key-tile cluster pays where each CTA streams only a few key tiles, so the
+        // latency of its first tiles dominates (batch 1: pi05 4.97 vs 5.46 us per launch);
+        // over long key ranges it costs ~1 % (batch 8 with a 4096-token prefix, batch 32)
+        const int key_tiles = (P + 63) / 64 + (H + 63) / 64;
+        const bool few = (key_tiles + splits - 1) / splits <= 4;
+        a5.ct = c->opt_attn_mcast == 1 || (c->opt_attn_mcast == 2 && few) ? attn_t5_cluster(a5) : 1;
         CUtensorMap maps[8];
         CK(c, attn_t5_maps(a5, c->host_table[2 * l], c->host_table[2 * l + 1], splits, maps));
         a5.ts = next_ts(c, GR00T_KCLASS_ATTENTION);
@@ -1379,7 +1385,8 @@ extern "C" int gr00t_set_option(gr00t_ctx* c, int option, int64_t value) {
       c->opt_mcast = value ? 1 : 0;
       break;
     case GR00T_OPT_ATTN_MULTICAST:
-      c->opt_attn_mcast = value ? 1 : 0;
+      if (value < 0 || value > 2) return set_err(c, GR00T_EINVAL, "attention multicast: 0, 1 or 2 (automatic)");
+      c->opt_attn_mcast = (int)value;
       break;
     case GR00T_OPT_GEMM_TSTORE:
       c->opt_tstore = value ? 1 : 0;

@@ -378,8 +378,10 @@ const char* gr00t_last_error(const gr00t_ctx* ctx);
                                        adjacent weight tiles that share each activation tile by TMA
                                        multicast; 0 (default, measured faster): one CTA per tile stream */
 #define GR00T_OPT_ATTN_MULTICAST 14 /* 1: the expert attention runs the 2 or 4 row tiles of a sample as one
-                                       cluster that fetches every key tile once and multicasts it; 0
-                                       (default, measured faster): each row tile fetches its own copies */
+                                       cluster that fetches every key tile once and multicasts it; 0: each
+                                       row tile fetches its own copies; 2 (default): the cluster where
+                                       each CTA streams at most 4 key tiles (many key splits, e.g. batch 1),
+                                       else not (both measured faster there) */
 #define GR00T_OPT_GEMM_TSTORE 15   /* 1 (default): the persistent tensor-core GEMM stages its bf16 outputs (plain,
                                       RoPE, GeGLU epilogues), and the split GEMM with tiles of up to 128 tokens
                                       its fp32 residual partials, in shared memory and writes them with tensor
