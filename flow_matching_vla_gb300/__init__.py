@@ -30,7 +30,7 @@ from ._abi import (DTYPE_BF16, DTYPE_FP32, FAMILY_DIT, FAMILY_EXPERT, MLP_GEGLU,
                    OPT_ATTN_PATH, OPT_GEMM_PATH, OPT_TIME_KERNELS, OPT_USE_GRAPH, OPT_WAIT_LIMIT,
                    OPT_SPLIT_CAP, OPT_RESID_SPLIT_CAP, OPT_PERSISTENT_GEMM, OPT_L2_PREFETCH, OPT_NOALLOC_LIMIT,
                    OPT_ATTN_SPLIT_CAP, OPT_TEST_STALL, OPT_GEMM_MULTICAST, OPT_ATTN_MULTICAST, OPT_GEMM_TSTORE, ETIMEOUT,
-                   INFO_DEVICE_BYTES, INFO_ERROR_FLAG, INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES,
+                   INFO_DEVICE_BYTES, INFO_ERROR_FLAG, INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES, INFO_MOD_ROW,
                    KCLASS_ATTENTION, KCLASS_DOWN_GEMM, KCLASS_NORM, KCLASS_O_GEMM, KCLASS_QKV_GEMM,
                    KCLASS_UP_GEMM, KCLASS_OTHER, KCLASS_NAMES, WFMT_NATIVE, WFMT_FP8)
 
@@ -323,6 +323,17 @@ class DenoiseLoop:
             raise ValueError("h_out must be a contiguous CUDA float32 tensor")
         self._check(self._lib.gr00t_debug_dump(self._ctx, int(k), _ptr(x_in), int(layer), _ptr(h_out)))
         return h_out
+
+    def debug_cond_step(self, k: int, batch: int):
+        """gr00t_debug_cond_step: (hoisted, per_step) modulation rows of step k, each
+        [batch, row] in the geometry's dtype (batch = the scheduled batch)."""
+        torch = _torch()
+        row = self.info(INFO_MOD_ROW)
+        dt = torch.bfloat16 if int(self.geom["dtype"]) == DTYPE_BF16 else torch.float32
+        hoisted = torch.empty((int(batch), row), dtype=dt, device="cuda")
+        per_step = torch.empty_like(hoisted)
+        self._check(self._lib.gr00t_debug_cond_step(self._ctx, int(k), _ptr(hoisted), _ptr(per_step)))
+        return hoisted, per_step
 
     def info(self, what: int) -> int:
         v = ctypes.c_int64()

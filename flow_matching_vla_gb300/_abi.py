@@ -34,6 +34,7 @@ KCLASS_OTHER = 7
 KCLASS_NAMES = {1: "qkv_gemm", 2: "attention", 3: "o_gemm", 4: "up_gemm", 5: "down_gemm", 6: "norm",
                 7: "other"}
 INFO_KERNELS_PER_STEP, INFO_WEIGHT_BYTES, INFO_DEVICE_BYTES, INFO_ERROR_FLAG = 1, 2, 3, 4
+INFO_MOD_ROW = 5
 
 STATUS_NAMES = {OK: "OK", EINVAL: "EINVAL", ENOMEM: "ENOMEM", ECUDA: "ECUDA", ESTATE: "ESTATE",
                 EUNSUPPORTED: "EUNSUPPORTED", ETIMEOUT: "ETIMEOUT"}
@@ -82,6 +83,7 @@ SIGNATURES = {
                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
     "gr00t_sync": (ctypes.c_int, [_VP]),
     "gr00t_debug_dump": (ctypes.c_int, [_VP, ctypes.c_int, _VP, ctypes.c_int, _VP]),
+    "gr00t_debug_cond_step": (ctypes.c_int, [_VP, ctypes.c_int, _VP, _VP]),
 }
 
 _lib = None

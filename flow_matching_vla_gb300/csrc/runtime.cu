@@ -1317,6 +1317,36 @@ extern "C" int gr00t_set_schedule(gr00t_ctx* c, int steps, int batch) {
   return GR00T_OK;
 }
 
+extern "C" int gr00t_debug_cond_step(gr00t_ctx* c, int k, void* hoisted, void* per_step) {
+  if (!c) return GR00T_EINVAL;
+  if (!hoisted || !per_step) return set_err(c, GR00T_EINVAL, "hoisted/per_step is NULL");
+  if (!c->scheduled) return set_err(c, GR00T_ESTATE, "no schedule (call gr00t_set_schedule)");
+  if (k < 0 || k >= c->sT) return set_err(c, GR00T_EINVAL, "step %d outside [0, %d)", k, c->sT);
+  const int B = c->sB, E = c->E, SR = c->S * c->R;
+  const size_t rows_bytes = (size_t)B * SR * c->esz;
+  CK(c, cudaMemcpyAsync(hoisted, (const char*)c->mod + (size_t)k * rows_bytes, rows_bytes,
+                        cudaMemcpyDeviceToDevice, c->stream));
+  // the same chain as gr00t_set_schedule on the B time-embedding rows of step k alone
+  // (the hoist's intermediates t1 / cvec serve as scratch: no kernel of a step reads them)
+  const void* temb_k = (const char*)c->temb + (size_t)k * B * E * c->esz;
+  const void* cin = temb_k;
+  if (c->g.time_mlp) {
+    GemmArgs a;
+    a.A = temb_k; a.lda = E; a.W = c->w_tin; a.ldw = E; a.M = B; a.N = E; a.K = E;
+    a.epi.kind = EPI_STORE; a.epi.act = ACT_SWISH; a.epi.bias = c->b_tin; a.epi.out = c->t1; a.epi.ldo = E;
+    RC(gemm(c, a));
+    GemmArgs b2 = a;
+    b2.A = c->t1; b2.W = c->w_tout; b2.epi.bias = c->b_tout; b2.epi.out = c->cvec;
+    RC(gemm(c, b2));
+    cin = c->cvec;
+  }
+  GemmArgs m;
+  m.A = cin; m.lda = E; m.W = c->w_cond; m.ldw = E; m.M = B; m.N = SR; m.K = E;
+  m.epi.kind = EPI_STORE; m.epi.bias = c->b_cond; m.epi.out = per_step; m.epi.ldo = SR;
+  RC(gemm(c, m));
+  return GR00T_OK;
+}
+
 extern "C" int gr00t_denoise(gr00t_ctx* c, const float* x_noise, float* actions) {
   if (!c) return GR00T_EINVAL;
   if (!x_noise || !actions) return set_err(c, GR00T_EINVAL, "x_noise/actions is NULL");
@@ -1460,6 +1490,9 @@ extern "C" int gr00t_get_info(gr00t_ctx* c, int what, int64_t* value) {
     }
     case GR00T_INFO_DEVICE_BYTES:
       *value = (int64_t)c->arena_bytes;
+      return GR00T_OK;
+    case GR00T_INFO_MOD_ROW:
+      *value = (int64_t)c->S * c->R;
       return GR00T_OK;
     case GR00T_INFO_ERROR_FLAG: {
       int f = 0;

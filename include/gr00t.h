@@ -396,6 +396,7 @@ int gr00t_set_option(gr00t_ctx* ctx, int option, int64_t value);
 #define GR00T_INFO_WEIGHT_BYTES 2       /* bytes of weights one step reads                */
 #define GR00T_INFO_DEVICE_BYTES 3       /* device memory the context owns                 */
 #define GR00T_INFO_ERROR_FLAG 4         /* device error word (bounded waits), 0 if clean  */
+#define GR00T_INFO_MOD_ROW 5            /* elements of one modulation-table row (all sites of a step and request) */
 int gr00t_get_info(gr00t_ctx* ctx, int what, int64_t* value);
 
 /* Kernel classes of one denoise step (gr00t_kernel_times). */
@@ -442,6 +443,19 @@ int gr00t_sync(gr00t_ctx* ctx);
  * -1 <= layer < layers.  Asynchronous on the stream.
  */
 int gr00t_debug_dump(gr00t_ctx* ctx, int k, const float* x_in, int layer, float* h_out);
+
+/*
+ * Test-only: the hoist check ("pi0.5 Design", cond component: the hoisted cond
+ * work must equal its per-step evaluation).  Copies the modulation rows of step
+ * k that gr00t_set_schedule hoisted into ``hoisted`` and evaluates the same
+ * step's cond work on its own -- time MLP (where the geometry has one) and the
+ * cond Dense over that step's ``batch`` time-embedding rows only, a GEMM of
+ * batch rows instead of steps x batch -- into ``per_step``.  Both DEVICE
+ * [batch][GR00T_INFO_MOD_ROW] in the geometry's dtype, batch = the scheduled
+ * batch.  The two differ only in the GEMMs' accumulation order.  GR00T_ESTATE
+ * without a schedule; 0 <= k < steps.  Asynchronous on the stream.
+ */
+int gr00t_debug_cond_step(gr00t_ctx* ctx, int k, void* hoisted, void* per_step);
 
 #ifdef __cplusplus
 }

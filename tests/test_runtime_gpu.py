@@ -226,3 +226,35 @@ def test_debug_dump_matches_the_oracle_trace(name):
         worst = max(worst, rel)
         assert rel <= 1e-2, f"block {layer}: residual rel-L2 {rel:.3e}"
     print(f"debug dump {name}: worst residual rel-L2 {worst:.3e} over {L + 1} dumps")
+
+
+def _bf16_ulp(x):
+    # one unit in the last place of bf16 (8 significant bits) at |x|
+    m, e = torch.frexp(x.abs().float())
+    return torch.ldexp(torch.ones_like(m), (e - 8).clamp(min=-133))
+
+
+@pytest.mark.parametrize("name,kw,exact", [
+    ("small_bf16", dict(), True),          # steps x batch <= 64 rows: the same GEMM plan either way
+    ("small_dit", dict(), True),
+    ("pi05", dict(batch=8), False),        # 80 hoisted rows: 128-token tiles against 64-token ones
+])
+def test_hoisted_cond_equals_per_step_evaluation_on_gpu(name, kw, exact):
+    """The hoist ("pi0.5 Design", cond component): for every step, the modulation rows that
+    gr00t_set_schedule computed for all steps at once equal the same cond work evaluated for
+    that step alone -- bit for bit where both run the same GEMM plan, else within one bf16 ulp
+    (only the accumulation order of the GEMMs differs)."""
+    fmv = _fmv()
+    c = synth.make_case(name, **kw)
+    g = c["geom"]
+    loop, held = fmv.from_case(c)
+    worst = 0.0
+    for k in range(g["steps"]):
+        h, p = loop.debug_cond_step(k, g["batch"])
+        torch.cuda.synchronize()
+        if exact:
+            assert torch.equal(h, p), f"step {k}"
+        d = (h.float() - p.float()).abs() / _bf16_ulp(torch.maximum(h.float().abs(), p.float().abs()))
+        worst = max(worst, float(d.max()))
+    print(f"hoist check {name}: worst difference {worst:.2f} bf16 ulp")
+    assert worst <= 1.0
