@@ -54,7 +54,7 @@ extern "C" {
 #define GR00T_ENOMEM (-2)      /* a device allocation failed                   */
 #define GR00T_ECUDA (-3)       /* a CUDA runtime/driver call failed            */
 #define GR00T_ESTATE (-4)      /* call out of order (e.g. denoise before bind) */
-#define GR00T_EUNSUPPORTED (-5)/* valid request this build does not implement  */
+#define GR00T_EUNSUPPORTED (-5)/* valid request the library does not implement */
 #define GR00T_ETIMEOUT (-6)    /* a bounded device wait gave up                */
 
 /* ---- enumerations ------------------------------------------------------ */
