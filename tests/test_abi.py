@@ -209,3 +209,23 @@ def test_bench_traffic_needs_unchanged_sources(monkeypatch, tmp_path):
     # a digest that no longer matches the kernel sources hides the number
     monkeypatch.setattr(bench, "source_digest", lambda kernel="attention": "0" * 16)
     assert bench.measured_traffic("pi05_b32", "attention") is None
+
+
+def test_bench_traffic_digest_is_per_kernel_class(monkeypatch, tmp_path):
+    # a change to the GEMM sources leaves the attention's recorded traffic valid, and a
+    # record for one class never vouches for another
+    import bench
+    f = tmp_path / "traffic.json"
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    csv = tmp_path / "cap.csv"
+    csv.write_text('"ID","Kernel Name","Metric Name","Metric Unit","Metric Value"\n'
+                   '"0","k","dram__bytes_read.sum","Mbyte","8.0"\n'
+                   '"0","k","dram__bytes_write.sum","Mbyte","2.0"\n')
+    bench.record_traffic(str(csv), "pi05_b32", "attention", "ncu ...")
+    assert bench.measured_traffic("pi05_b32", "attention") == pytest.approx(10e6)
+    assert bench.measured_traffic("pi05_b32", "up_gemm") is None
+    real = bench.source_digest
+    monkeypatch.setattr(bench, "source_digest",
+                        lambda kernel="attention": "f" * 16 if bench.source_group(kernel) == "gemm" else real(kernel))
+    assert bench.measured_traffic("pi05_b32", "attention") == pytest.approx(10e6)
+    assert bench.source_group("qkv_gemm") == "gemm" and bench.source_group("norm") == "norm"
